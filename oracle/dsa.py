@@ -1,0 +1,136 @@
+"""Plain definitions of the DSA decode step (test infrastructure only).
+
+Every function takes host numpy arrays in the library's layouts:
+
+``q_idx`` int8 [R, H_i, D_i]   indexer query of each row, one vector per head
+``w_idx`` int32 [R, H_i]       indexer head weights of each row
+``k_idx`` int8 [L_total, D_i]  indexer keys, one per cached position (all heads)
+``q``     bf16 bits [R, H_q, D_k] attention queries
+``kv``    bf16 bits [L_total, D_k] latent cache rows (key = all D_k columns,
+                                value = the first D_v columns)
+``offsets`` [B+1]      cache rows of request b are offsets[b]..offsets[b+1]-1
+``row_offsets`` [B+1]  query rows of request b are row_offsets[b]..row_offsets[b+1]-1
+``row_len`` [R]        row r sees request-local positions 0..row_len[r]-1
+"""
+from __future__ import annotations
+
+import numpy as np
+
+INT32_MIN = -(1 << 31)
+INT32_MAX = (1 << 31) - 1
+
+
+def _row_request(row_offsets, R):
+    req = np.empty(R, dtype=np.int64)
+    for b in range(len(row_offsets) - 1):
+        req[int(row_offsets[b]):int(row_offsets[b + 1])] = b
+    return req
+
+
+def _bf16_to_f64(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def indexer_scores(q_idx, w_idx, k_idx, offsets, row_offsets, row_len, relu=True, rows=None):
+    """Lightning-indexer scores, one int64 vector per row.
+
+    For row r of request b and visible position t < row_len[r]:
+
+        s[r, t] = sum_h  w[r, h] * max(0, sum_d q[r, h, d] * k[offsets[b] + t, d])
+
+    (without the ``max(0, .)`` when ``relu`` is False).  The position is scored
+    against every indexer head of the current query and the head results are
+    combined with the query's own weights ("ds4 glm53-m3ultra", page 1: the
+    search over all cached positions; the ReLU-weighted head sum is the reading
+    taken where the pages give no formula).  Validity comes from each row's own
+    length, never from the packed layout ("GLM-5.3-Flash-Alis-MLX-4bit", page 3,
+    the indexer padding fix).
+
+    Raises ``OverflowError`` if any score does not fit int32, the type the
+    library's scores are stored in.
+    """
+    R = q_idx.shape[0]
+    req = _row_request(row_offsets, R)
+    out = []
+    for r in (range(R) if rows is None else rows):
+        b = int(req[r])
+        lo = int(offsets[b])
+        n = int(row_len[r])
+        keys = k_idx[lo:lo + n].astype(np.int64)              # [n, D_i]
+        qr = q_idx[r].astype(np.int64)                         # [H_i, D_i]
+        dots = keys @ qr.T                                     # [n, H_i]
+        if relu:
+            dots = np.maximum(dots, 0)
+        s = dots @ w_idx[r].astype(np.int64)                   # [n]
+        if s.size and (s.min() < INT32_MIN or s.max() > INT32_MAX):
+            raise OverflowError("indexer score outside int32")
+        out.append(s)
+    return out
+
+
+def topk_indices(scores, k):
+    """Ordered top-k of one row's scores.
+
+    Returns int64 [k]: the positions of the min(k, n) largest scores, ordered by
+    score descending and, among equal scores, by position ascending; entries past
+    min(k, n) are -1.  A full stable sort of all n positions -- the plain
+    definition of "same positions selected, same order" ("ds4 glm53-m3ultra",
+    page 1), with the tie rule "lower index first".  A row with n <= k selects
+    every position.
+    """
+    s = np.asarray(scores, dtype=np.int64)
+    n = s.shape[0]
+    order = np.argsort(-s, kind="stable")   # stable: equal scores keep index order
+    m = min(k, n)
+    out = np.full(k, -1, dtype=np.int64)
+    out[:m] = order[:m]
+    return out
+
+
+def sparse_attention(q_row, kv_req, idx, D_v, softmax_scale):
+    """Attention of every head of one query row over the selected latent rows.
+
+    ``q_row`` bf16 bits [H_q, D_k]; ``kv_req`` bf16 bits [L_b, D_k] (the
+    request's own cache rows); ``idx`` the selected request-local positions
+    (entries < 0 are unused).  In float64, for head h:
+
+        z_j  = softmax_scale * sum_{d < D_k} q[h, d] * kv[idx_j, d]
+        p_j  = exp(z_j - max z) / sum_j' exp(z_j' - max z)
+        o[h, c] = sum_j p_j * kv[idx_j, c]          for c < D_v
+
+    -- attention over only the selected positions ("ds4 glm53-m3ultra", page 1),
+    with keys and values read from one shared latent row per position (the
+    latent, absorbed-MLA cache of "glm53-tensorfold-spark", page 4; value = the
+    first D_v columns).  Returns float64 [H_q, D_v]; with no selected position
+    the output is all zeros.
+    """
+    sel = np.asarray(idx)
+    sel = sel[sel >= 0]
+    H_q, D_k = q_row.shape
+    if sel.size == 0:
+        return np.zeros((H_q, D_v), dtype=np.float64)
+    Q = _bf16_to_f64(q_row)                                   # [H_q, D_k]
+    K = _bf16_to_f64(kv_req[sel])                             # [n, D_k]
+    z = softmax_scale * (Q @ K.T)                             # [H_q, n]
+    z = z - z.max(axis=1, keepdims=True)
+    e = np.exp(z)
+    p = e / e.sum(axis=1, keepdims=True)
+    return p @ K[:, :D_v]                                     # [H_q, D_v]
+
+
+def decode_step(inp, relu=True, rows=None):
+    """Scores -> ordered top-k -> sparse attention for the rows of ``inp``
+    (a ``DecodeInputs``-like object).  Returns (scores list, idx int64 [R', k],
+    out float64 [R', H_q, D_v]) for the requested rows (all rows by default)."""
+    rows = list(range(inp.R)) if rows is None else list(rows)
+    req = _row_request(inp.row_offsets, inp.R)
+    scores = indexer_scores(inp.q_idx, inp.w_idx, inp.k_idx, inp.offsets, inp.row_offsets,
+                            inp.row_len, relu=relu, rows=rows)
+    idx = np.stack([topk_indices(s, inp.k) for s in scores]) if rows else np.zeros((0, inp.k), np.int64)
+    outs = []
+    for j, r in enumerate(rows):
+        b = int(req[r])
+        lo, hi = int(inp.offsets[b]), int(inp.offsets[b + 1])
+        outs.append(sparse_attention(inp.q[r], inp.kv[lo:hi], idx[j], inp.D_v, inp.softmax_scale))
+    out = np.stack(outs) if outs else np.zeros((0, inp.H_q, inp.D_v))
+    return scores, idx, out
