@@ -1,0 +1,397 @@
+"""Benchmark of the DSA decode step on one GB300 (or N independent replicas).
+
+Workload (default): long-context single-stream decode, L = 307200 cached
+positions, 11 DSA layers run back to back, each layer with its own seeded
+caches: indexer 64 heads x 128 (int8), top-k 2048, MLA attention with 64
+heads over a 576-wide bf16 latent (512 value columns).  A step is one token:
+the fused decode step of all 11 layers.  The metric is microseconds per layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on stdout (rank 0).  The 11 layers hold 4.3 GB of inputs, far
+above the 129 MB L2, so every layer's keys and latent rows come from HBM.
+"--impl reference" times the CPU oracle (the only reference there is) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dsa_inputs as gen  # noqa: E402
+
+METRIC = "DSA decode-step us/layer at L=300k (11 layers back to back); achieved HBM GB/s vs GB300 peak"
+UNIT = "us/layer"
+LAYERS = 11
+L_LONG = 307200
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_layers(n_layers, L, device):
+    import torch
+    import dsa_sparse_attention_03_gb300 as dsa
+    layers = []
+    for layer in range(n_layers):
+        x = gen.l300k(layer=layer, L=L) if L == L_LONG else gen.l64k(layer=layer, L=L)
+        prob, t = dsa.upload_inputs(x, device=device)
+        layers.append((x, prob, t))
+    ws = dsa.alloc_workspace(layers[0][1], device=device)   # same sizes for every layer
+    k = layers[0][0].k
+    H_q, D_v = layers[0][0].H_q, layers[0][0].D_v
+    idx = torch.empty((n_layers, 1, k), dtype=torch.int32, device=device)
+    nsel = torch.empty((n_layers, 1), dtype=torch.int32, device=device)
+    out = torch.empty((n_layers, 1, H_q, D_v), dtype=torch.int16, device=device)
+    return layers, ws, idx, nsel, out
+
+
+def kernels_per_step():
+    import dsa_sparse_attention_03_gb300 as dsa
+    return dsa.KERNELS_PER_DECODE_STEP
+
+
+def bench_ours(args):
+    import torch
+    import torch.distributed as dist
+    import dsa_sparse_attention_03_gb300 as dsa
+
+    world, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    stream = torch.cuda.Stream(device=device)
+    sp = stream.cuda_stream
+
+    layers, ws, idx, nsel, out = make_layers(LAYERS, L_LONG, device)
+    x0 = layers[0][0]
+
+    def step():
+        for i, (_, prob, _) in enumerate(layers):
+            dsa.dsa_decode_step(prob, idx[i], nsel[i], out[i], ws, stream=sp)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                graph.replay()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    ms_per_step = ms / args.steps
+    us_per_layer = ms_per_step * 1000.0 / LAYERS / world   # whole-job: N replicas in parallel
+    status = dsa.dsa_read_device_status(ws, stream=sp)
+
+    # Dominant kernel: the indexer, timed alone per launch on the same stream.
+    scores = torch.empty((1, L_LONG), dtype=torch.int32, device=device)
+    idx_ms = []
+    with torch.cuda.stream(stream):
+        for rep in range(3):
+            for _, prob, _ in layers:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                dsa.dsa_index_scores(prob, scores, ws, stream=sp)
+                e1.record(stream)
+                idx_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    idx_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in idx_ms[LAYERS:])
+    idx_bytes = L_LONG * x0.D_i + x0.H_i * x0.D_i + x0.H_i * 4
+    idx_gbs = idx_bytes / (idx_avg_ms * 1e-3) / 1e9
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    step_bytes = LAYERS * (L_LONG * x0.D_i + x0.k * x0.D_k * 2 + x0.H_q * x0.D_k * 2)
+    step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    e2e = bench_e2e(args, layers, ws, idx, nsel, out, stream, device)
+
+    # The L = 65536 single-layer point of the metric: 12 independent layers
+    # (1.0 GB, > 4x L2) rotated, one decode step per layer.
+    sec = bench_l64k(args, stream, device)
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+    res = {
+        "metric": METRIC, "value": round(us_per_layer, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8+bf16", "data": "synthetic",
+        "config": {"workload": "l300k: 1 query, L=307200, 11 layers back to back; indexer 64x128 "
+                               "int8 (10% near-parallel keys), k=2048, 64 heads x 576 bf16 latent "
+                               "(D_v=512), scale 1/24",
+                   "layers": LAYERS, "L": L_LONG, "k": x0.k, "batch": 1,
+                   "l2": "inputs 4.3 GB > L2 (129 MB); not flushed", "cuda_graph": graph is not None,
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(1e6 / (us_per_layer * LAYERS * world) * world, 2),
+        "step_gbs": round(step_gbs, 1),
+        "roofline": {"kernel": "indexer (" + ("tc" if dsa.indexer_kind(layers[0][1]) == "tc" else "dp4a") + ")",
+                     "bound": "hbm", "achieved": round(idx_gbs, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(idx_gbs / hbm_peak, 4),
+                     "peak_source": peak_src, "traffic": None,
+                     "algorithmic_bytes_per_launch": idx_bytes,
+                     "avg_launch_us": round(idx_avg_ms * 1000, 3)},
+        "secondary": sec,
+        "e2e": e2e,
+        "gpu_launches": args.steps * LAYERS * kernels_per_step(),
+        "clocks": clk,
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        res["cpu_baseline"] = cpu_baseline(layers_for_cpu=[x for x, _, _ in layers[:4]])
+    return res
+
+
+def bench_e2e(args, layers, ws, idx, nsel, out, stream, device):
+    """The same step through the public API with host buffers: every step copies
+    each layer's query inputs and the new token's cache row (indexer key and
+    latent row, appended at the last position) from pinned host memory, runs
+    the decode step, and reads back the output and the selected indices."""
+    import torch
+    import dsa_sparse_attention_03_gb300 as dsa
+    sp = stream.cuda_stream
+    host_in, host_out = [], []
+    h2d = d2h = 0
+    for x, prob, t in layers:
+        hi = {
+            "q_idx": torch.from_numpy(x.q_idx).pin_memory(),
+            "w_idx": torch.from_numpy(x.w_idx).pin_memory(),
+            "q": torch.from_numpy(x.q.view(np.int16)).pin_memory(),
+            "k_row": torch.from_numpy(x.k_idx[-1:]).pin_memory(),
+            "kv_row": torch.from_numpy(x.kv[-1:].view(np.int16)).pin_memory(),
+        }
+        host_in.append(hi)
+        host_out.append({"out": torch.empty((1, x.H_q, x.D_v), dtype=torch.int16).pin_memory(),
+                         "idx": torch.empty((1, x.k), dtype=torch.int32).pin_memory()})
+    h2d = sum(v.numel() * v.element_size() for v in host_in[0].values()) * len(layers)
+    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values()) * len(layers)
+
+    def step():
+        for i, (x, prob, t) in enumerate(layers):
+            hi, ho = host_in[i], host_out[i]
+            t["q_idx"].copy_(hi["q_idx"], non_blocking=True)
+            t["w_idx"].copy_(hi["w_idx"], non_blocking=True)
+            t["q"].copy_(hi["q"], non_blocking=True)
+            t["k_idx"][-1:].copy_(hi["k_row"], non_blocking=True)
+            t["kv"][-1:].copy_(hi["kv_row"], non_blocking=True)
+            dsa.dsa_decode_step(prob, idx[i], nsel[i], out[i], ws, stream=sp)
+            ho["out"].copy_(out[i], non_blocking=True)
+            ho["idx"].copy_(idx[i], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        steps = max(3, args.steps // 2)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(ms * 1000.0 / LAYERS, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "cuda_graph": False}
+
+
+def bench_l64k(args, stream, device):
+    import torch
+    import dsa_sparse_attention_03_gb300 as dsa
+    n = 12
+    layers, ws, idx, nsel, out = make_layers(n, 65536, device)
+    sp = stream.cuda_stream
+
+    def step(i):
+        _, prob, _ = layers[i % n]
+        dsa.dsa_decode_step(prob, idx[i % n], nsel[i % n], out[i % n], ws, stream=sp)
+
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            step(i)
+        torch.cuda.synchronize()
+        reps = max(2, args.steps) * n
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            step(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / reps
+    x0 = layers[0][0]
+    nbytes = 65536 * x0.D_i + x0.k * x0.D_k * 2 + x0.H_q * x0.D_k * 2
+    del layers, ws
+    return {"workload": "l64k: 1 query, L=65536, 1 layer (12 rotated layer buffers, 1.0 GB)",
+            "us_per_layer": round(us, 3), "step_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "cuda_graph": False}
+
+
+def cpu_baseline(layers_for_cpu):
+    """The CPU oracle, as it stands, on a bounded sample: full decode steps of a
+    few of the long-context layers."""
+    import oracle
+    t0 = time.perf_counter()
+    for x in layers_for_cpu:
+        oracle.decode_step(x)
+    dt = time.perf_counter() - t0
+    n = len(layers_for_cpu)
+    return {"value": round(dt * 1e6 / n, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} of the 11 L=307200 layers, full decode step each (numpy int64 "
+                      f"scores, stable sort, float64 attention; single-threaded int64 matmul)",
+            "seconds": round(dt, 2)}
+
+
+def bench_reference(args):
+    world, rank, local = _dist_env()
+    if rank != 0:
+        return None
+    layers = [gen.l300k(layer=i) for i in range(min(LAYERS, 2))]
+    import oracle
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle.decode_step(layers[0])
+    t0 = time.perf_counter()
+    n = 0
+    for s in range(args.steps):
+        oracle.decode_step(layers[s % len(layers)])
+        n += 1
+    dt = time.perf_counter() - t0
+    us = dt * 1e6 / n
+    return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(us * LAYERS / 1000.0, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64", "data": "synthetic",
+            "config": {"workload": "l300k: 1 query, L=307200 (one layer per timed step: a "
+                                   "bounded sample of the 11-layer token)", "layers": LAYERS},
+            "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{n} single-layer decode steps of the L=307200 workload"},
+            "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    res = bench_reference(args) if args.impl == "reference" else bench_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

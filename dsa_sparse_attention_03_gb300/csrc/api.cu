@@ -1,0 +1,255 @@
+// libdsa C ABI: argument validation, workspace map and the launch sequence of
+// each entry point.  All compute lives in the kernels of the other units.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+
+namespace dsa {
+namespace {
+
+thread_local std::string g_err;
+
+dsa_status fail(dsa_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+dsa_status fail(dsa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+dsa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned(const void* ptr, size_t a) {
+  return (reinterpret_cast<uintptr_t>(ptr) % a) == 0;
+}
+
+enum Need { kNeedIndexer = 1, kNeedTopk = 2, kNeedAttn = 4 };
+
+// Validates the fields an entry point reads and builds the workspace map.
+dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
+  if (!p) return fail(DSA_ERR_INVALID_ARG, "problem is NULL");
+  if (p->R < 0 || p->R > 65535) return fail(DSA_ERR_INVALID_ARG, "R=%d outside [0,65535]", p->R);
+  if (p->B < 1 || p->B > kMaxB) return fail(DSA_ERR_UNSUPPORTED, "B=%d outside [1,%d]", p->B, kMaxB);
+  if (p->L_max < 0) return fail(DSA_ERR_INVALID_ARG, "L_max=%d < 0", p->L_max);
+  if (p->L_total < 0 || p->L_total >= (int64_t(1) << 31))
+    return fail(DSA_ERR_UNSUPPORTED, "L_total=%lld outside [0,2^31)", (long long)p->L_total);
+  if (p->k < 1 || p->k > kMaxK) return fail(DSA_ERR_UNSUPPORTED, "k=%d outside [1,%d]", p->k, kMaxK);
+  if (need && p->R > 0 && (!p->offsets || !p->row_offsets || !p->row_len))
+    return fail(DSA_ERR_INVALID_ARG, "offsets/row_offsets/row_len must be set");
+
+  if (need & kNeedIndexer) {
+    if (p->H_i < 1 || p->H_i > 128) return fail(DSA_ERR_UNSUPPORTED, "H_i=%d outside [1,128]", p->H_i);
+    if (p->D_i != 32 && p->D_i != 64 && p->D_i != 128 && p->D_i != 256)
+      return fail(DSA_ERR_UNSUPPORTED, "D_i=%d not in {32,64,128,256}", p->D_i);
+    if (p->R > 0 && (!p->q_idx || !p->w_idx || (p->L_total > 0 && !p->k_idx)))
+      return fail(DSA_ERR_INVALID_ARG, "q_idx/w_idx/k_idx must be set");
+    if (!aligned(p->k_idx, 16) || !aligned(p->q_idx, 16) || !aligned(p->w_idx, 4))
+      return fail(DSA_ERR_INVALID_ARG, "k_idx/q_idx must be 16-byte aligned, w_idx 4-byte");
+    const int64_t qk = p->qk_abs_max > 0 ? p->qk_abs_max : 128;
+    const int64_t wm = p->w_abs_max > 0 ? p->w_abs_max : 4;
+    if (qk > 128) return fail(DSA_ERR_INVALID_ARG, "qk_abs_max=%d > 128", p->qk_abs_max);
+    const double bound = double(p->H_i) * double(wm) * double(p->D_i) * double(qk * qk);
+    if (bound >= 2147483648.0)
+      return fail(DSA_ERR_OVERFLOW_RISK,
+                  "H_i*w_abs_max*D_i*qk_abs_max^2 = %.0f reaches 2^31 (int32 scores)", bound);
+    const int ix = p->flags & DSA_INDEXER_MASK;
+    if (ix != DSA_INDEXER_AUTO && ix != DSA_INDEXER_DP4A && ix != DSA_INDEXER_TC)
+      return fail(DSA_ERR_INVALID_ARG, "unknown indexer selector %d", ix);
+    if (ix == DSA_INDEXER_TC && !indexer_tc_supported(*p))
+      return fail(DSA_ERR_UNSUPPORTED, "tensor-core indexer does not support this shape");
+  }
+  if (need & kNeedAttn) {
+    if (p->H_q < 1 || p->H_q > 128) return fail(DSA_ERR_UNSUPPORTED, "H_q=%d outside [1,128]", p->H_q);
+    if (p->D_k < 16 || p->D_k > 576 || p->D_k % 16)
+      return fail(DSA_ERR_UNSUPPORTED, "D_k=%d: need a multiple of 16 in [16,576]", p->D_k);
+    if (p->D_v < 32 || p->D_v > 512 || p->D_v % 32 || p->D_v > p->D_k)
+      return fail(DSA_ERR_UNSUPPORTED, "D_v=%d: need a multiple of 32, <= 512 and <= D_k", p->D_v);
+    if (p->R > 0 && (!p->q || (p->L_total > 0 && !p->kv)))
+      return fail(DSA_ERR_INVALID_ARG, "q/kv must be set");
+    if (!aligned(p->q, 16) || !aligned(p->kv, 16))
+      return fail(DSA_ERR_INVALID_ARG, "q/kv must be 16-byte aligned");
+    if (!(p->softmax_scale == p->softmax_scale) || p->softmax_scale <= 0.f)
+      return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be positive");
+  }
+
+  Plan& P = *pl;
+  std::memset(&P, 0, sizeof P);
+  P.R = p->R; P.B = p->B; P.H_i = p->H_i; P.D_i = p->D_i; P.H_q = p->H_q;
+  P.D_k = p->D_k; P.D_v = p->D_v; P.k = p->k; P.L_max = p->L_max; P.flags = p->flags;
+
+  // Top-k: aim for a few CTAs per SM over all rows, 1K..64K positions each.
+  const int64_t work = int64_t(p->L_max) * (p->R > 0 ? p->R : 1);
+  int chunk = 1024;
+  while (chunk < 65536 && int64_t(chunk) * 600 < work) chunk <<= 1;
+  P.chunk = chunk;
+  P.nchunk = p->L_max > 0 ? (p->L_max + chunk - 1) / chunk : 1;
+
+  // Attention: split the k selected positions so that all rows together give
+  // a few hundred CTAs, each over whole 64-position tiles.
+  const int tiles = (p->k + kAttnRows - 1) / kAttnRows;
+  const int hgroups = (p->H_q > 0 ? p->H_q + kAttnHeads - 1 : kAttnHeads) / kAttnHeads;
+  int per = (p->R > 0) ? 600 / (p->R * hgroups) : 1;
+  if (per < 1) per = 1;
+  P.nsplit = per < tiles ? per : tiles;
+
+  const size_t R = size_t(p->R);
+  size_t off = 0;
+  P.off_status = off; off += 256;
+  P.off_state = off; off = align_up(off + R * sizeof(RowState), 256);
+  P.off_hist = off; off = align_up(off + R * kHistBins * 4, 256);
+  P.off_tiecnt = off; off = align_up(off + R * size_t(P.nchunk) * 4, 256);
+  P.zero_end = off;
+  P.off_sel = off; off = align_up(off + R * size_t(p->k) * 8, 256);
+  P.off_scores = off; off = align_up(off + R * size_t(p->L_max) * 4, 256);
+  const int hq = p->H_q > 0 ? p->H_q : 0;
+  const int dv = p->D_v > 0 ? p->D_v : 0;
+  P.off_part = off; off = align_up(off + R * size_t(P.nsplit) * hq * dv * 4, 256);
+  P.off_ml = off; off = align_up(off + R * size_t(P.nsplit) * hq * 2 * 4, 256);
+  P.total = off;
+  return DSA_OK;
+}
+
+dsa_status check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
+  if (!ws) return fail(DSA_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(DSA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < pl.total)
+    return fail(DSA_ERR_INVALID_ARG, "workspace %zu bytes < required %zu", ws_bytes, pl.total);
+  return DSA_OK;
+}
+
+dsa_status run_indexer(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
+                       cudaStream_t st) {
+  if (p.R == 0 || p.L_max == 0) return DSA_OK;
+  const int ix = p.flags & DSA_INDEXER_MASK;
+  const bool tc = ix == DSA_INDEXER_TC || (ix == DSA_INDEXER_AUTO && indexer_tc_supported(p));
+  cudaError_t e = tc ? launch_indexer_tc(p, pl, scores, reinterpret_cast<uint32_t*>(ws + pl.off_status), st)
+                     : launch_indexer_dp4a(p, pl, scores, st);
+  if (e != cudaSuccess) return cuda_fail(e, tc ? "indexer (tensor core)" : "indexer (dp4a)");
+  return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int dsa_version(void) { return 100; }
+
+const char* dsa_last_error_string(void) { return g_err.c_str(); }
+
+int dsa_indexer_kind(const dsa_problem* p) {
+  Plan pl;
+  if (make_plan(p, 0, &pl) != DSA_OK) return -1;
+  const int ix = p->flags & DSA_INDEXER_MASK;
+  const bool tc = ix == DSA_INDEXER_TC || (ix == DSA_INDEXER_AUTO && indexer_tc_supported(*p));
+  return tc ? DSA_INDEXER_TC : DSA_INDEXER_DP4A;
+}
+
+size_t dsa_workspace_size(const dsa_problem* p) {
+  Plan pl;
+  if (make_plan(p, 0, &pl) != DSA_OK) return 0;
+  return pl.total;
+}
+
+dsa_status dsa_index_scores(const dsa_problem* p, int32_t* scores, void* ws, size_t ws_bytes,
+                            void* stream) {
+  g_err.clear();
+  Plan pl;
+  dsa_status s = make_plan(p, kNeedIndexer, &pl);
+  if (s != DSA_OK) return s;
+  if ((s = check_ws(pl, ws, ws_bytes)) != DSA_OK) return s;
+  if (p->R > 0 && p->L_max > 0 && !scores) return fail(DSA_ERR_INVALID_ARG, "scores is NULL");
+  if (!aligned(scores, 16)) return fail(DSA_ERR_INVALID_ARG, "scores must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear status");
+  return run_indexer(*p, pl, scores, static_cast<char*>(ws), st);
+}
+
+dsa_status dsa_topk(const dsa_problem* p, const int32_t* scores, int32_t* idx, int32_t* nsel,
+                    void* ws, size_t ws_bytes, void* stream) {
+  g_err.clear();
+  Plan pl;
+  dsa_status s = make_plan(p, kNeedTopk, &pl);
+  if (s != DSA_OK) return s;
+  if ((s = check_ws(pl, ws, ws_bytes)) != DSA_OK) return s;
+  if (p->R > 0 && (!idx || (p->L_max > 0 && !scores)))
+    return fail(DSA_ERR_INVALID_ARG, "scores/idx is NULL");
+  if (!aligned(scores, 16)) return fail(DSA_ERR_INVALID_ARG, "scores must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, pl.zero_end, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
+  if (p->R == 0) return DSA_OK;
+  e = launch_topk(*p, pl, scores, idx, nsel, static_cast<char*>(ws), st);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k");
+  return DSA_OK;
+}
+
+dsa_status dsa_sparse_attn(const dsa_problem* p, const int32_t* idx, const int32_t* nsel,
+                           uint16_t* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  g_err.clear();
+  Plan pl;
+  dsa_status s = make_plan(p, kNeedAttn, &pl);
+  if (s != DSA_OK) return s;
+  if ((s = check_ws(pl, ws, ws_bytes)) != DSA_OK) return s;
+  if (p->R > 0 && (!idx || !out)) return fail(DSA_ERR_INVALID_ARG, "idx/out is NULL");
+  if (!aligned(out, 4)) return fail(DSA_ERR_INVALID_ARG, "out must be 4-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear status");
+  if (p->R == 0) return DSA_OK;
+  e = launch_attention(*p, pl, idx, nsel, out, lse, static_cast<char*>(ws), st);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse attention");
+  return DSA_OK;
+}
+
+dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* nsel, uint16_t* out,
+                           void* ws, size_t ws_bytes, void* stream) {
+  g_err.clear();
+  Plan pl;
+  dsa_status s = make_plan(p, kNeedIndexer | kNeedTopk | kNeedAttn, &pl);
+  if (s != DSA_OK) return s;
+  if ((s = check_ws(pl, ws, ws_bytes)) != DSA_OK) return s;
+  if (p->R > 0 && (!idx || !out)) return fail(DSA_ERR_INVALID_ARG, "idx/out is NULL");
+  if (!aligned(out, 4)) return fail(DSA_ERR_INVALID_ARG, "out must be 4-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  cudaError_t e = cudaMemsetAsync(ws, 0, pl.zero_end, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
+  if (p->R == 0) return DSA_OK;
+  int32_t* scores = reinterpret_cast<int32_t*>(w + pl.off_scores);
+  if ((s = run_indexer(*p, pl, scores, w, st)) != DSA_OK) return s;
+  e = launch_topk(*p, pl, scores, idx, nsel, w, st);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k");
+  e = launch_attention(*p, pl, idx, nsel, out, nullptr, w, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse attention");
+  return DSA_OK;
+}
+
+dsa_status dsa_read_device_status(void* ws, void* stream, int32_t* bits) {
+  g_err.clear();
+  if (!ws || !bits) return fail(DSA_ERR_INVALID_ARG, "ws/bits is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read status");
+  *bits = static_cast<int32_t>(v);
+  if (v & DSA_DEVICE_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "a bounded device wait ran out");
+  if (v & DSA_DEVICE_BAD_INDEX) return fail(DSA_ERR_DEVICE_INDEX, "an out-of-range index was skipped");
+  return DSA_OK;
+}
+
+}  // extern "C"

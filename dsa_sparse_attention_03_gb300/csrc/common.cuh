@@ -1,0 +1,67 @@
+// Internal definitions shared by the libdsa translation units (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+constexpr int kHistBits = 11;                 // radix digit of the threshold search
+constexpr int kHistBins = 1 << kHistBits;
+constexpr int kAttnRows = 64;                 // selected positions per attention CTA
+constexpr int kAttnHeads = 16;                // query heads per attention CTA (mma M)
+constexpr int kMaxB = 4096;
+constexpr int kMaxK = 4096;
+
+// Per-row state of the threshold search, in the workspace.  Zeroed by the
+// top-k entry before its first kernel.
+struct RowState {
+  uint32_t umax;       // max ordered key of the row
+  uint32_t uminv;      // max of ~ordered key (= ~min)
+  uint32_t prefix;     // candidates satisfy (u >> shift) == prefix
+  uint32_t shift;      // unresolved low bits of the threshold
+  uint32_t k_rem;      // positions still to take from the candidate bin
+  uint32_t n_gt;       // slot counter for strictly-greater selections
+  uint32_t mode;       // 0 search, 1 take every position, 2 empty row
+  uint32_t n_take;     // min(k, row_len)
+  uint32_t arrive[8];  // last-block counters, one per phase
+};
+static_assert(sizeof(RowState) == 64, "RowState is 64 bytes");
+
+enum Phase { kPhaseMinMax = 0, kPhasePass0 = 1, kPhasePass1 = 2, kPhasePass2 = 3 };
+
+// Everything the launchers need: validated sizes and the workspace map.
+struct Plan {
+  int R, B, H_i, D_i, H_q, D_k, D_v, k, L_max;
+  int flags;
+  int chunk, nchunk;       // top-k: positions per CTA, CTAs per row
+  int nsplit;              // attention: CTAs along the selected positions
+  size_t off_status, off_state, off_hist, off_tiecnt, zero_end;
+  size_t off_sel, off_scores, off_part, off_ml, total;
+};
+
+// Order-preserving map of int32 onto uint32.
+__host__ __device__ __forceinline__ uint32_t ordered_key(int32_t s) {
+  return static_cast<uint32_t>(s) ^ 0x80000000u;
+}
+
+__device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// Launchers (one per translation unit).  Each returns the launch error.
+cudaError_t launch_indexer_dp4a(const dsa_problem& p, const Plan& pl, int32_t* scores,
+                                cudaStream_t st);
+cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores,
+                              uint32_t* status, cudaStream_t st);
+bool indexer_tc_supported(const dsa_problem& p);
+cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* scores,
+                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st);
+cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t* idx,
+                             const int32_t* nsel, uint16_t* out, float* lse, char* ws,
+                             cudaStream_t st);
+
+}  // namespace dsa

@@ -26,6 +26,7 @@ from .dsa import (  # noqa: F401
     indexer_scores,
     topk_indices,
     sparse_attention,
+    attention_lse,
     decode_step,
     INT32_MIN,
     INT32_MAX,

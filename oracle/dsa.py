@@ -118,6 +118,19 @@ def sparse_attention(q_row, kv_req, idx, D_v, softmax_scale):
     return p @ K[:, :D_v]                                     # [H_q, D_v]
 
 
+def attention_lse(q_row, kv_req, idx, softmax_scale):
+    """Natural-log log-sum-exp of the scaled logits of each head over the
+    selected rows, log(sum_j exp(z_j)) with z as in ``sparse_attention``;
+    -inf when nothing is selected.  Returns float64 [H_q]."""
+    sel = np.asarray(idx)
+    sel = sel[sel >= 0]
+    if sel.size == 0:
+        return np.full(q_row.shape[0], -np.inf)
+    z = softmax_scale * (_bf16_to_f64(q_row) @ _bf16_to_f64(kv_req[sel]).T)
+    m = z.max(axis=1)
+    return m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+
+
 def decode_step(inp, relu=True, rows=None):
     """Scores -> ordered top-k -> sparse attention for the rows of ``inp``
     (a ``DecodeInputs``-like object).  Returns (scores list, idx int64 [R', k],

@@ -304,3 +304,19 @@ def test_attention_no_selection_is_zero():
     x = gen.tiny(L=10)
     o = oracle.sparse_attention(x.q[0], x.kv, np.full(4, -1), 64, 1.0)
     assert o.shape == (8, 64) and not o.any()
+
+
+def test_attention_lse_closed_forms():
+    # one row: the lse is its own logit; two rows: log(e^a + e^b)
+    D = 64
+    kv = np.zeros((2, D), np.float32)
+    kv[0, 3] = 2.0
+    kv[1, 5] = 1.0
+    q = np.zeros((1, D), np.float32)
+    q[0, 3], q[0, 5] = 0.5, -1.5
+    qb, kvb = _bf16(q), _bf16(kv)
+    a, b = 0.25 * 0.5 * 2.0, 0.25 * -1.5 * 1.0
+    assert oracle.attention_lse(qb, kvb, np.array([0]), 0.25)[0] == a
+    np.testing.assert_allclose(oracle.attention_lse(qb, kvb, np.array([0, 1]), 0.25)[0],
+                               math.log(math.exp(a) + math.exp(b)), rtol=1e-15)
+    assert oracle.attention_lse(qb, kvb, np.array([-1]), 0.25)[0] == -np.inf
