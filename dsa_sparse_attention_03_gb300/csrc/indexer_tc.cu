@@ -1,12 +1,525 @@
-// Lightning indexer on the tcgen05 tensor cores (filled in below).
+// Lightning indexer on the 5th-generation tensor cores (tcgen05, TMEM).
+//
+// s[r, t] = sum_h w[r, h] * max(0, q_idx[r, h, :] . k_idx[t, :])   ("ds4
+// glm53-m3ultra", page 1: every cached position scored against the query).
+//
+// The 64 heads of a query share each 128-byte key, so scoring is a dense
+// contraction [keys x D_i] . [D_i x heads]: 8192 multiply-adds per key, which
+// CUDA-core dp4a cannot sustain at HBM speed.  Here the keys are the M = 128
+// rows of a tcgen05.mma tile and the group's query heads (up to 4 rows x 64
+// heads) are N; K = D_i.  sm_103a has no int8 MMA, so both operands are
+// widened to fp16 in shared memory: every int8 is exact in fp16, every product
+// (|.| <= 2^14) and every per-head sum (|.| <= 2^21 for D_i <= 128) is exact in
+// the fp32 accumulator, so the scores stay bit-exact integers.
+//
+// One persistent CTA per SM walks a contiguous range of 128-key tiles (the
+// tile list of all (request, row group) pairs), with warp roles:
+//   warp 0        TMA producer: cp.async.bulk of each int8 key tile (16 KB,
+//                 contiguous) into an S-stage ring, mbarrier complete_tx;
+//                 also allocates / frees TMEM.
+//   warp 1        MMA issuer (one thread): D[tmem] = A . B^T, K/16 MMAs per
+//                 tile, tcgen05.commit to the accumulator barrier.
+//   warps 2-5     converters: int8 tile -> fp16 A tile in the canonical K-major
+//                 128-byte-swizzled layout; queries -> fp16 B when the row
+//                 group changes.
+//   warps 6-9     epilogue: tcgen05.ld of each key's head dots (one TMEM lane
+//                 per key), ReLU, weight, head sum in exact int32, store.
+// A and the accumulator are double-buffered, so conversion, MMA and epilogue
+// of consecutive tiles overlap the key stream.  Every mbarrier wait is bounded
+// (a few seconds of %globaltimer); on expiry the CTA sets DSA_DEVICE_TIMEOUT,
+// the other roles stop at their next wait, in-flight copies and MMAs are
+// drained (bounded) and TMEM is freed before exit.
 #include "common.cuh"
 
+#include <cuda_fp16.h>
+
 namespace dsa {
+namespace {
 
-bool indexer_tc_supported(const dsa_problem&) { return false; }
+constexpr int kThreads = 320;
+constexpr int kTile = 128;                 // keys per tile (MMA M)
+constexpr uint64_t kWaitNs = 4000000000ull;
+constexpr int kConvWarp0 = 2;
+constexpr int kEpiWarp0 = 6;
+constexpr int kMaxRG = 4;                  // query rows per MMA group (N <= 256)
 
-cudaError_t launch_indexer_tc(const dsa_problem&, const Plan&, int32_t*, uint32_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
+struct TcArgs {
+  const int8_t* q_idx;
+  const int32_t* w_idx;
+  const int8_t* k_idx;
+  const int32_t* offsets;
+  const int32_t* row_offsets;
+  const int32_t* row_len;
+  int32_t* scores;
+  uint32_t* status;
+  int64_t L_max;
+  int B, H_i, D_i, RG, stages, relu;
+  uint32_t off_b, off_stage, off_w, off_bar, off_misc, off_prefix;   // shared-memory map
+  uint32_t tmem_cols;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t cvta_smem(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity`; false if the CTA is aborting
+// or the wait ran out (which starts the abort).
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      uint32_t* status) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try(bar, parity)) return true;
+    if ((n & 15) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitNs) {
+        *abort_flag = 1;
+        raise_status(status, DSA_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// The same, taken by a whole warp: every lane waits (acquire) and the warp
+// proceeds only if all lanes succeeded, so it never diverges before the
+// .sync.aligned tcgen05 instructions that follow.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* status) {
+  const bool ok = wait_bar(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (SBO), descriptor version 1 (tcgen05).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1u << 16) | ((uint64_t)(1024u >> 4) << 32) |
+         ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 accumulator, M x N.
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Four int8 -> four fp16, exactly: bias to unsigned, splice the byte into the
+// mantissa of 1024.0 (0x6400 | u = 1024 + u), subtract 1152 = 1024 + 128.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
+  const uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+// 16 int8 of row m (K elements 16c..16c+15) -> fp16 in a K-major SW128 operand
+// whose K-blocks (64 elements, 128 bytes per row) are `kblock_bytes` apart.
+__device__ __forceinline__ void convert_chunk(const int4 v, unsigned char* base, int m, int c,
+                                              uint32_t kblock_bytes) {
+  uint32_t o[8];
+  i8x4_to_f16x4((uint32_t)v.x, o[0], o[1]);
+  i8x4_to_f16x4((uint32_t)v.y, o[2], o[3]);
+  i8x4_to_f16x4((uint32_t)v.z, o[4], o[5]);
+  i8x4_to_f16x4((uint32_t)v.w, o[6], o[7]);
+  const int kb = c >> 2;
+  const int j0 = (c & 3) * 2;
+  unsigned char* row = base + kb * kblock_bytes + m * 128;
+  const int sw = m & 7;
+  *reinterpret_cast<uint4*>(row + ((j0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint4*>(row + (((j0 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+struct TileInfo {
+  int b, g, j;        // request, row group, tile within the request
+  int r0, nrows;      // first row and rows of the group
+  int L_b;
+  int64_t base;       // offsets[b]
+};
+
+__device__ __forceinline__ TileInfo tile_info(const TcArgs& a, const int* prefix, int gt) {
+  int lo = 0, hi = a.B - 1;  // largest b with prefix[b] <= gt
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= gt) lo = mid; else hi = mid - 1;
+  }
+  TileInfo ti;
+  ti.b = lo;
+  ti.base = a.offsets[lo];
+  ti.L_b = a.offsets[lo + 1] - a.offsets[lo];
+  const int tiles_b = (ti.L_b + kTile - 1) / kTile;
+  const int local = gt - prefix[lo];
+  ti.g = local / tiles_b;
+  ti.j = local - ti.g * tiles_b;
+  const int rb = a.row_offsets[lo];
+  const int rows_b = a.row_offsets[lo + 1] - rb;
+  ti.r0 = rb + ti.g * a.RG;
+  ti.nrows = min(a.RG, rows_b - ti.g * a.RG);
+  return ti;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // Layout (offsets from the 1024-aligned base).
+  unsigned char* A = smem;                                 // 2 x [D_i/64][128][128 B]
+  unsigned char* Bop = smem + a.off_b;                     // [D_i/64][N_max][128 B]
+  unsigned char* stage = smem + a.off_stage;               // S x [128][D_i] int8
+  int* w_s = reinterpret_cast<int*>(smem + a.off_w);       // [RG][H_i] + [RG] sums
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.off_bar);
+  volatile int* misc = reinterpret_cast<volatile int*>(smem + a.off_misc);  // [0] tmem, [1] abort
+  int* prefix = reinterpret_cast<int*>(smem + a.off_prefix);               // [B+1]
+
+  const int S = a.stages;
+  const uint32_t bar_full = cvta_smem(bars);                // S
+  const uint32_t bar_empty = bar_full + 8 * S;              // S
+  const uint32_t bar_afull = bar_empty + 8 * S;             // 2
+  const uint32_t bar_accfull = bar_afull + 16;              // 2
+  const uint32_t bar_accempty = bar_accfull + 16;           // 2
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // Per-request tile counts: groups_b * tiles_b; exclusive prefix by one warp.
+  if (warp == 0) {
+    int run = 0;
+    for (int base = 0; base < a.B; base += 32) {
+      const int b = base + lane;
+      int v = 0;
+      if (b < a.B) {
+        const int L_b = a.offsets[b + 1] - a.offsets[b];
+        const int rows_b = a.row_offsets[b + 1] - a.row_offsets[b];
+        v = ((rows_b + a.RG - 1) / a.RG) * ((L_b + kTile - 1) / kTile);
+      }
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (b < a.B) prefix[b] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) prefix[a.B] = run;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_afull + 8 * i, 4);
+      mbar_init(bar_accfull + 8 * i, 1);
+      mbar_init(bar_accempty + 8 * i, 4);
+    }
+    misc[1] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     cvta_smem((const void*)misc)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = (uint32_t)misc[0];
+  volatile int* abort_flag = misc + 1;
+
+  const int total = prefix[a.B];
+  const int t_begin = (int)(((int64_t)blockIdx.x * total) / gridDim.x);
+  const int t_end = (int)(((int64_t)(blockIdx.x + 1) * total) / gridDim.x);
+  const int n_local = t_end - t_begin;
+  const int D_I = a.D_i;                                   // K of the MMA
+  const int N_max = a.RG * a.H_i;
+  const uint32_t a_bytes = kTile * D_I * 2;                // one fp16 A buffer
+  const uint32_t stage_bytes = kTile * D_I;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n_local; ++i) {
+        const int s = i % S;
+        if (i >= S && !wait_bar(bar_empty + 8 * s, ((i / S) - 1) & 1, abort_flag, a.status)) break;
+        const TileInfo ti = tile_info(a, prefix, t_begin + i);
+        const int rows = min(kTile, ti.L_b - ti.j * kTile);
+        const uint32_t bytes = (uint32_t)rows * D_I;
+        mbar_arrive_tx(bar_full + 8 * s, bytes);
+        tma_load_1d(cvta_smem(stage + s * stage_bytes),
+                    a.k_idx + (ti.base + (int64_t)ti.j * kTile) * D_I, bytes, bar_full + 8 * s);
+        issued = i + 1;
+      }
+      // Drain: every issued copy must have landed before the CTA can exit.
+      for (int i = max(0, issued - S); i < issued; ++i) {
+        const int s = i % S;
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try(bar_full + 8 * s, (i / S) & 1) && globaltimer() - t0 < kWaitNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n_local; ++i) {
+        const int buf = i & 1;
+        if (i >= 2 && !wait_bar(bar_accempty + 8 * buf, ((i - 2) >> 1) & 1, abort_flag, a.status)) break;
+        if (!wait_bar(bar_afull + 8 * buf, (i >> 1) & 1, abort_flag, a.status)) break;
+        tc_fence_after();
+        const TileInfo ti = tile_info(a, prefix, t_begin + i);
+        const uint32_t idesc = idesc_f16(kTile, ti.nrows * a.H_i);
+        const uint32_t a_base = cvta_smem(A + buf * a_bytes);
+        const uint32_t b_base = cvta_smem(Bop);
+        for (int kk = 0; kk < D_I / 16; ++kk) {
+          const uint32_t ka = a_base + (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          const uint32_t kb = b_base + (kk >> 2) * (N_max * 128) + (kk & 3) * 32;
+          mma_f16(tmem + buf * N_max, smem_desc_sw128(ka), smem_desc_sw128(kb), idesc, kk > 0);
+        }
+        mma_commit(bar_accfull + 8 * buf);
+        issued = i + 1;
+      }
+      // Drain: the last MMAs must finish before TMEM is freed.
+      for (int i = max(0, issued - 2); i < issued; ++i) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try(bar_accfull + 8 * (i & 1), (i >> 1) & 1) && globaltimer() - t0 < kWaitNs) {
+        }
+      }
+    }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------------------ converters
+    const int ct = tid - kConvWarp0 * 32;  // 0..127
+    int cur_b = -1, cur_g = -1;
+    const int cpr = D_I / 16;               // 16-byte chunks per int8 row
+    for (int i = 0; i < n_local; ++i) {
+      const int s = i % S, buf = i & 1;
+      const TileInfo ti = tile_info(a, prefix, t_begin + i);
+      if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status)) break;
+      if (i >= 2 && !wait_bar_warp(bar_accfull + 8 * buf, ((i - 2) >> 1) & 1, abort_flag, a.status)) break;
+      if (ti.b != cur_b || ti.g != cur_g) {
+        // New row group: B may be rewritten once every issued MMA has finished.
+        if (i >= 1 &&
+            !wait_bar_warp(bar_accfull + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, a.status))
+          break;
+        const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
+        const int nchunks = ti.nrows * a.H_i * cpr;
+        for (int q = ct; q < nchunks; q += 128)
+          convert_chunk(__ldg(src + q), Bop, q / cpr, q % cpr, (uint32_t)N_max * 128);
+        cur_b = ti.b;
+        cur_g = ti.g;
+      }
+      const int4* st = reinterpret_cast<const int4*>(stage + s * stage_bytes);
+      unsigned char* abuf = A + buf * a_bytes;
+      for (int q = ct; q < kTile * cpr; q += 128) convert_chunk(st[q], abuf, q / cpr, q % cpr, kTile * 128);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_afull + 8 * buf);
+        mbar_arrive(bar_empty + 8 * s);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;            // TMEM lanes this warp may read
+    const int m = quarter * 32 + lane;       // key row of the tile = TMEM lane
+    // Each epilogue warp keeps its own copy of the group's weights (no
+    // cross-warp barrier): [RG][H_i] weights, then [RG] weight sums.
+    int* w_own = w_s + (warp - kEpiWarp0) * (a.RG * a.H_i + a.RG);
+    int* wsum = w_own + a.RG * a.H_i;
+    int cur_b = -1, cur_g = -1;
+    int rlen[kMaxRG];
+    for (int i = 0; i < n_local; ++i) {
+      const int buf = i & 1;
+      const TileInfo ti = tile_info(a, prefix, t_begin + i);
+      if (ti.b != cur_b || ti.g != cur_g) {
+        __syncwarp();
+        for (int q = lane; q < ti.nrows * a.H_i; q += 32) w_own[q] = a.w_idx[(int64_t)ti.r0 * a.H_i + q];
+        __syncwarp();
+        if (lane < ti.nrows) {
+          uint32_t sacc = 0;
+          for (int h = 0; h < a.H_i; ++h) sacc += (uint32_t)w_own[lane * a.H_i + h];
+          wsum[lane] = (int)sacc;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int jr = 0; jr < kMaxRG; ++jr) rlen[jr] = jr < ti.nrows ? a.row_len[ti.r0 + jr] : 0;
+        cur_b = ti.b;
+        cur_g = ti.g;
+      }
+      if (!wait_bar_warp(bar_accfull + 8 * buf, (i >> 1) & 1, abort_flag, a.status)) break;
+      tc_fence_after();
+      const int t = ti.j * kTile + m;
+#pragma unroll
+      for (int jr = 0; jr < kMaxRG; ++jr) {
+        if (jr >= ti.nrows) break;
+        uint32_t acc = 0;  // wraps mod 2^32; the true score fits int32
+        const int* wr = w_own + jr * a.H_i;
+        for (int h0 = 0; h0 < a.H_i; h0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * N_max + jr * a.H_i + h0, v);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) {
+            float d = __uint_as_float(v[h]);
+            if (a.relu) d = fmaxf(d, 0.f);
+            // d is an exact integer with |d| < 2^22: adding 1.5 * 2^23 puts it in
+            // the low mantissa bits (bit pattern 0x4B400000 + d).
+            acc += (uint32_t)__float_as_int(d + 12582912.f) * (uint32_t)wr[h0 + h];
+          }
+        }
+        acc -= 0x4B400000u * (uint32_t)wsum[jr];
+        if (t < rlen[jr]) a.scores[(int64_t)(ti.r0 + jr) * a.L_max + t] = (int32_t)acc;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_accempty + 8 * buf);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+bool indexer_tc_supported(const dsa_problem& p) {
+  return (p.D_i == 64 || p.D_i == 128) && (p.H_i == 32 || p.H_i == 64 || p.H_i == 128);
+}
+
+cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores,
+                              uint32_t* status, cudaStream_t st) {
+  TcArgs a;
+  a.q_idx = p.q_idx; a.w_idx = p.w_idx; a.k_idx = p.k_idx;
+  a.offsets = p.offsets; a.row_offsets = p.row_offsets; a.row_len = p.row_len;
+  a.scores = scores; a.status = status; a.L_max = p.L_max;
+  a.B = p.B; a.H_i = p.H_i; a.D_i = p.D_i; a.relu = (p.flags & DSA_FLAG_NO_RELU) ? 0 : 1;
+  const int per_req = (p.R + p.B - 1) / p.B;
+  int RG = 256 / p.H_i;
+  if (RG > kMaxRG) RG = kMaxRG;
+  if (per_req < RG) RG = per_req < 1 ? 1 : per_req;
+  a.RG = RG;
+  const int N_max = RG * p.H_i;
+  const int D_i = p.D_i;
+  // stages: as many 16 KB key tiles in flight as shared memory allows
+  const uint32_t a_bytes = 2u * 128u * D_i * 2u;
+  const uint32_t b_bytes = (uint32_t)N_max * D_i * 2u;
+  const uint32_t stage_bytes = 128u * D_i;
+  const uint32_t prefix_bytes = ((uint32_t)(p.B + 1) * 4u + 15u) / 16u * 16u;
+  const uint32_t w_bytes = (4u * (uint32_t)(RG * p.H_i + RG) * 4u + 15u) / 16u * 16u;  // per epilogue warp
+  const uint32_t budget = 227u * 1024u - 1024u;   // minus the alignment slack
+  int S = 8;
+  auto total_for = [&](int s) {
+    return a_bytes + b_bytes + s * stage_bytes + w_bytes + (2 * s + 6) * 8 + 16 + prefix_bytes;
+  };
+  while (S > 2 && total_for(S) > budget) --S;
+  if (total_for(S) > budget) return cudaErrorInvalidConfiguration;
+  a.stages = S;
+  a.off_b = a_bytes;
+  a.off_stage = a.off_b + b_bytes;
+  a.off_w = a.off_stage + S * stage_bytes;
+  a.off_bar = a.off_w + w_bytes;
+  a.off_misc = a.off_bar + (2 * S + 6) * 8;
+  a.off_prefix = a.off_misc + 16;
+  uint32_t cols = 32;
+  while (cols < 2u * N_max) cols <<= 1;
+  a.tmem_cols = cols;
+  size_t smem = (size_t)a.off_prefix + prefix_bytes + 1024;
+  if (smem < 120u * 1024u) smem = 120u * 1024u;   // one CTA per SM: TMEM is never contended
+  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  indexer_tc_kernel<<<sms, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace dsa
