@@ -132,7 +132,8 @@ def bench_ours(args):
     stream = torch.cuda.Stream(device=device)
     sp = stream.cuda_stream
 
-    layers, ws, idx, nsel, out = make_layers(LAYERS, L_LONG, device)
+    n_layers = args.layers
+    layers, ws, idx, nsel, out = make_layers(n_layers, L_LONG, device)
     x0 = layers[0][0]
 
     def step():
@@ -181,7 +182,7 @@ def bench_ours(args):
         ms = float(t.item())
         dist.barrier()
     ms_per_step = ms / args.steps
-    us_per_layer = ms_per_step * 1000.0 / LAYERS / world   # whole-job: N replicas in parallel
+    us_per_layer = ms_per_step * 1000.0 / n_layers / world   # whole-job: N replicas in parallel
     status = dsa.dsa_read_device_status(ws, stream=sp)
 
     # Dominant kernel: the indexer, timed alone per launch on the same stream.
@@ -197,7 +198,7 @@ def bench_ours(args):
                 e1.record(stream)
                 idx_ms.append((e0, e1))
     torch.cuda.synchronize()
-    idx_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in idx_ms[LAYERS:])
+    idx_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in idx_ms[n_layers:])
     idx_bytes = L_LONG * x0.D_i + x0.H_i * x0.D_i + x0.H_i * 4
     idx_gbs = idx_bytes / (idx_avg_ms * 1e-3) / 1e9
     peaks = {}
@@ -207,14 +208,14 @@ def bench_ours(args):
         pass
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    step_bytes = LAYERS * (L_LONG * x0.D_i + x0.k * x0.D_k * 2 + x0.H_q * x0.D_k * 2)
+    step_bytes = n_layers * (L_LONG * x0.D_i + x0.k * x0.D_k * 2 + x0.H_q * x0.D_k * 2)
     step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
 
-    e2e = bench_e2e(args, layers, ws, idx, nsel, out, stream, device)
+    e2e = bench_e2e(args, layers, ws, idx, nsel, out, stream, device) if not args.no_extras else None
 
     # The L = 65536 single-layer point of the metric: 12 independent layers
     # (1.0 GB, > 4x L2) rotated, one decode step per layer.
-    sec = bench_l64k(args, stream, device)
+    sec = bench_l64k(args, stream, device) if not args.no_extras else None
 
     if world > 1:
         dist.destroy_process_group()
@@ -225,13 +226,13 @@ def bench_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8+bf16", "data": "synthetic",
-        "config": {"workload": "l300k: 1 query, L=307200, 11 layers back to back; indexer 64x128 "
+        "config": {"workload": f"l300k: 1 query, L=307200, {n_layers} layers back to back; indexer 64x128 "
                                "int8 (10% near-parallel keys), k=2048, 64 heads x 576 bf16 latent "
                                "(D_v=512), scale 1/24",
-                   "layers": LAYERS, "L": L_LONG, "k": x0.k, "batch": 1,
+                   "layers": n_layers, "L": L_LONG, "k": x0.k, "batch": 1,
                    "l2": "inputs 4.3 GB > L2 (129 MB); not flushed", "cuda_graph": graph is not None,
                    "parallelism": f"replicas x{world}"},
-        "tokens_per_s": round(1e6 / (us_per_layer * LAYERS * world) * world, 2),
+        "tokens_per_s": round(1e6 / (us_per_layer * n_layers * world) * world, 2),
         "step_gbs": round(step_gbs, 1),
         "roofline": {"kernel": "indexer (" + ("tc" if dsa.indexer_kind(layers[0][1]) == "tc" else "dp4a") + ")",
                      "bound": "hbm", "achieved": round(idx_gbs, 1), "peak": hbm_peak,
@@ -241,11 +242,11 @@ def bench_ours(args):
                      "avg_launch_us": round(idx_avg_ms * 1000, 3)},
         "secondary": sec,
         "e2e": e2e,
-        "gpu_launches": args.steps * LAYERS * kernels_per_step(),
+        "gpu_launches": args.steps * n_layers * kernels_per_step(),
         "clocks": clk,
         "device_status": status,
     }
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and not args.no_extras and world == 1:
         res["cpu_baseline"] = cpu_baseline(layers_for_cpu=[x for x, _, _ in layers[:4]])
     return res
 
@@ -299,7 +300,7 @@ def bench_e2e(args, layers, ws, idx, nsel, out, stream, device):
         e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    return {"value": round(ms * 1000.0 / LAYERS, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+    return {"value": round(ms * 1000.0 / len(layers), 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps, "cuda_graph": False}
 
 
@@ -380,11 +381,15 @@ def bench_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="layers per token (the headline workload runs 11)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="only the headline timing (no e2e, L=64k point or CPU baseline); for profiling")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -128,11 +128,11 @@ dsa_status check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
 
 dsa_status run_indexer(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                        cudaStream_t st) {
-  if (p.R == 0 || p.L_max == 0) return DSA_OK;
+  if (p.R == 0) return DSA_OK;
   const int ix = p.flags & DSA_INDEXER_MASK;
   const bool tc = ix == DSA_INDEXER_TC || (ix == DSA_INDEXER_AUTO && indexer_tc_supported(p));
-  cudaError_t e = tc ? launch_indexer_tc(p, pl, scores, reinterpret_cast<uint32_t*>(ws + pl.off_status), st)
-                     : launch_indexer_dp4a(p, pl, scores, st);
+  cudaError_t e = tc ? launch_indexer_tc(p, pl, scores, ws, st)
+                     : launch_indexer_dp4a(p, pl, scores, ws, st);
   if (e != cudaSuccess) return cuda_fail(e, tc ? "indexer (tensor core)" : "indexer (dp4a)");
   return DSA_OK;
 }
@@ -172,8 +172,11 @@ dsa_status dsa_index_scores(const dsa_problem* p, int32_t* scores, void* ws, siz
   if (p->R > 0 && p->L_max > 0 && !scores) return fail(DSA_ERR_INVALID_ARG, "scores is NULL");
   if (!aligned(scores, 16)) return fail(DSA_ERR_INVALID_ARG, "scores must be 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
-  if (e != cudaSuccess) return cuda_fail(e, "clear status");
+  if (p->R == 0) {  // nothing to score; still honour "clears the status word"
+    cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status");
+    return DSA_OK;
+  }
   return run_indexer(*p, pl, scores, static_cast<char*>(ws), st);
 }
 
@@ -225,9 +228,12 @@ dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* nsel, ui
   if (!aligned(out, 4)) return fail(DSA_ERR_INVALID_ARG, "out must be 4-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  cudaError_t e = cudaMemsetAsync(ws, 0, pl.zero_end, st);
-  if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
-  if (p->R == 0) return DSA_OK;
+  cudaError_t e;
+  if (p->R == 0) {
+    e = cudaMemsetAsync(ws, 0, 256, st);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status");
+    return DSA_OK;
+  }
   int32_t* scores = reinterpret_cast<int32_t*>(w + pl.off_scores);
   if ((s = run_indexer(*p, pl, scores, w, st)) != DSA_OK) return s;
   e = launch_topk(*p, pl, scores, idx, nsel, w, st);

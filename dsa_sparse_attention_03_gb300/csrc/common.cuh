@@ -53,10 +53,12 @@ __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
 }
 
 // Launchers (one per translation unit).  Each returns the launch error.
-cudaError_t launch_indexer_dp4a(const dsa_problem& p, const Plan& pl, int32_t* scores,
+// Both indexers also clear the workspace's status word and top-k state
+// ([0, Plan::zero_end)), so a decode step needs no separate memset.
+cudaError_t launch_indexer_dp4a(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                                 cudaStream_t st);
-cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores,
-                              uint32_t* status, cudaStream_t st);
+cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
+                              cudaStream_t st);
 bool indexer_tc_supported(const dsa_problem& p);
 cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* scores,
                         int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st);

@@ -27,6 +27,8 @@ struct IdxArgs {
   int B, H_i;
   int relu;
   int total_tiles_bound;
+  uint4* zero;          // workspace words to clear (status + top-k state)
+  int n_zero;
 };
 
 // Exclusive prefix of per-request tile counts into tile_start[0..B], by one block.
@@ -80,6 +82,8 @@ __global__ void __launch_bounds__(kThreads) indexer_dp4a_kernel(IdxArgs a) {
   int4* q_s = reinterpret_cast<int4*>(smem + ts_bytes);                  // [H_i * D_I / 16]
   int* w_s = reinterpret_cast<int*>(smem + ts_bytes + (size_t)a.H_i * D_I);
 
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < a.n_zero; i += gridDim.x * kThreads)
+    a.zero[i] = make_uint4(0, 0, 0, 0);
   tile_prefix(a.offsets, a.B, TILE, tile_start);
   const int total = tile_start[a.B];
   int cached_row = -1;  // row whose q/w are in shared memory
@@ -156,13 +160,15 @@ __global__ void __launch_bounds__(kThreads) indexer_dp4a_kernel(IdxArgs a) {
 }
 
 template <int D_I, int KPT>
-cudaError_t launch(const dsa_problem& p, int32_t* scores, cudaStream_t st) {
+cudaError_t launch(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws, cudaStream_t st) {
   constexpr int TILE = kThreads * KPT;
   IdxArgs a;
   a.q_idx = p.q_idx; a.w_idx = p.w_idx; a.k_idx = p.k_idx;
   a.offsets = p.offsets; a.row_offsets = p.row_offsets; a.row_len = p.row_len;
   a.scores = scores; a.L_max = p.L_max; a.B = p.B; a.H_i = p.H_i;
   a.relu = (p.flags & DSA_FLAG_NO_RELU) ? 0 : 1;
+  a.zero = reinterpret_cast<uint4*>(ws);
+  a.n_zero = (int)(pl.zero_end / 16);
   const int64_t bound = p.L_total / TILE + p.B;
   a.total_tiles_bound = (int)bound;
   const size_t ts_bytes = ((size_t)(p.B + 1) * 4 + 15) / 16 * 16;
@@ -181,13 +187,13 @@ cudaError_t launch(const dsa_problem& p, int32_t* scores, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_indexer_dp4a(const dsa_problem& p, const Plan&, int32_t* scores,
+cudaError_t launch_indexer_dp4a(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                                 cudaStream_t st) {
   switch (p.D_i) {
-    case 32: return launch<32, 2>(p, scores, st);
-    case 64: return launch<64, 2>(p, scores, st);
-    case 128: return launch<128, 2>(p, scores, st);
-    default: return launch<256, 1>(p, scores, st);
+    case 32: return launch<32, 2>(p, pl, scores, ws, st);
+    case 64: return launch<64, 2>(p, pl, scores, ws, st);
+    case 128: return launch<128, 2>(p, pl, scores, ws, st);
+    default: return launch<256, 1>(p, pl, scores, ws, st);
   }
 }
 

@@ -56,6 +56,8 @@ struct TcArgs {
   int B, H_i, D_i, RG, stages, relu;
   uint32_t off_b, off_stage, off_w, off_bar, off_misc, off_prefix;   // shared-memory map
   uint32_t tmem_cols;
+  uint4* zero;          // workspace words to clear (status + top-k state)
+  int n_zero;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -260,6 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   const uint32_t bar_accempty = bar_accfull + 16;           // 2
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  for (int i = blockIdx.x * kThreads + tid; i < a.n_zero; i += gridDim.x * kThreads)
+    a.zero[i] = make_uint4(0, 0, 0, 0);
 
   // Per-request tile counts: groups_b * tiles_b; exclusive prefix by one warp.
   if (warp == 0) {
@@ -473,9 +478,12 @@ bool indexer_tc_supported(const dsa_problem& p) {
   return (p.D_i == 64 || p.D_i == 128) && (p.H_i == 32 || p.H_i == 64 || p.H_i == 128);
 }
 
-cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores,
-                              uint32_t* status, cudaStream_t st) {
+cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
+                              cudaStream_t st) {
   TcArgs a;
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
+  a.zero = reinterpret_cast<uint4*>(ws);
+  a.n_zero = (int)(pl.zero_end / 16);
   a.q_idx = p.q_idx; a.w_idx = p.w_idx; a.k_idx = p.k_idx;
   a.offsets = p.offsets; a.row_offsets = p.row_offsets; a.row_len = p.row_len;
   a.scores = scores; a.status = status; a.L_max = p.L_max;

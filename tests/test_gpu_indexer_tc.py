@@ -1,0 +1,92 @@
+"""The tcgen05 tensor-core indexer: bit-exact scores against the CPU oracle and
+against the dp4a indexer, over the shapes and layouts it serves (one row per
+request, causal row groups of up to four rows, packed varlen caches, ragged
+tiles, extreme int8 values, the linear variant, 32/64/128 heads, D_i 64/128)."""
+import numpy as np
+import pytest
+
+import dsa_inputs as gen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _scores(x, indexer, relu=True):
+    import torch
+    import dsa_sparse_attention_03_gb300 as dsa
+    prob, t = dsa.upload_inputs(x, indexer=indexer, relu=relu)
+    assert dsa.indexer_kind(prob) == indexer
+    ws = dsa.alloc_workspace(prob)
+    s = torch.full((x.R, max(1, x.L_max)), -99, dtype=torch.int32, device="cuda")
+    dsa.dsa_index_scores(prob, s, ws)
+    status = dsa.dsa_read_device_status(ws)
+    return s.cpu().numpy(), status
+
+
+def _check(x, rows=None, relu=True, vs_dp4a=True):
+    got, status = _scores(x, "tc", relu)
+    assert status == 0
+    rows = list(range(x.R)) if rows is None else rows
+    ref = oracle.indexer_scores(x.q_idx, x.w_idx, x.k_idx, x.offsets, x.row_offsets, x.row_len,
+                                relu=relu, rows=rows)
+    for j, r in enumerate(rows):
+        n = int(x.row_len[r])
+        assert np.array_equal(got[r, :n], ref[j]), f"row {r}"
+        assert (got[r, n:] == -99).all(), f"row {r}: wrote past its length"
+    if vs_dp4a:
+        other, _ = _scores(x, "dp4a", relu)
+        for r in range(x.R):
+            n = int(x.row_len[r])
+            assert np.array_equal(got[r, :n], other[r, :n])
+
+
+def test_tc_small_single_row():
+    _check(gen.l64k(L=1000))
+
+
+@pytest.mark.parametrize("L", [1, 127, 128, 129, 4099, 65536])
+def test_tc_lengths(L):
+    _check(gen.l64k(L=L))
+
+
+def test_tc_long_context_layer():
+    _check(gen.l300k(layer=5), vs_dp4a=False)
+
+
+def test_tc_causal_row_groups_with_ties():
+    x = gen.causal64(L=20000, R=64)
+    _check(x, rows=[0, 1, 2, 3, 4, 37, 62, 63])
+
+
+def test_tc_causal_odd_row_count():
+    x = gen.causal64(L=3001, R=7)      # groups of 4 and 3 rows
+    _check(x)
+
+
+def test_tc_varlen_batch():
+    x = gen.make_inputs("v", seed=5, lengths=[0, 77, 128, 3000, 129, 20000], **gen.MLA,
+                        key_mode="near_parallel")
+    _check(x)
+
+
+def test_tc_int8_extremes():
+    x = gen.l64k(L=3000)
+    rng = np.random.default_rng(1)
+    x.k_idx[:] = rng.choice(np.array([-128, 127, -127, 0, 1], np.int8), x.k_idx.shape)
+    x.q_idx[:] = rng.choice(np.array([-128, 127, -1], np.int8), x.q_idx.shape)
+    x.w_idx[:] = rng.choice(np.array([1, 4], np.int32), x.w_idx.shape)
+    _check(x)
+
+
+def test_tc_without_relu_negative_weights():
+    x = gen.l64k(L=5000)
+    x.w_idx[:] = np.where(np.arange(64) % 3 == 0, -3, 2).astype(np.int32)[None]
+    _check(x, relu=False)
+
+
+@pytest.mark.parametrize("H_i,D_i", [(32, 64), (32, 128), (128, 128), (64, 64)])
+def test_tc_head_and_dim_variants(H_i, D_i):
+    x = gen.make_inputs("hd", seed=H_i * 7 + D_i, lengths=[2500, 900], rows_per_request=[3, 2],
+                        row_len=[2500, 2400, 2000, 900, 700], H_i=H_i, D_i=D_i, H_q=16,
+                        D_k=64, D_v=64, k=256, softmax_scale=0.125)
+    _check(x)
