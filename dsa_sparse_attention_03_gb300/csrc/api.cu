@@ -194,7 +194,7 @@ dsa_status dsa_topk(const dsa_problem* p, const int32_t* scores, int32_t* idx, i
   cudaError_t e = cudaMemsetAsync(ws, 0, pl.zero_end, st);
   if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
   if (p->R == 0) return DSA_OK;
-  e = launch_topk(*p, pl, scores, idx, nsel, static_cast<char*>(ws), st);
+  e = launch_topk(*p, pl, scores, idx, nsel, static_cast<char*>(ws), st, false);
   if (e != cudaSuccess) return cuda_fail(e, "top-k");
   return DSA_OK;
 }
@@ -207,7 +207,7 @@ dsa_status dsa_sparse_attn(const dsa_problem* p, const int32_t* idx, const int32
   if (s != DSA_OK) return s;
   if ((s = check_ws(pl, ws, ws_bytes)) != DSA_OK) return s;
   if (p->R > 0 && (!idx || !out)) return fail(DSA_ERR_INVALID_ARG, "idx/out is NULL");
-  if (!aligned(out, 4)) return fail(DSA_ERR_INVALID_ARG, "out must be 4-byte aligned");
+  if (!aligned(out, 8)) return fail(DSA_ERR_INVALID_ARG, "out must be 8-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
   if (e != cudaSuccess) return cuda_fail(e, "clear status");
@@ -225,7 +225,7 @@ dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* nsel, ui
   if (s != DSA_OK) return s;
   if ((s = check_ws(pl, ws, ws_bytes)) != DSA_OK) return s;
   if (p->R > 0 && (!idx || !out)) return fail(DSA_ERR_INVALID_ARG, "idx/out is NULL");
-  if (!aligned(out, 4)) return fail(DSA_ERR_INVALID_ARG, "out must be 4-byte aligned");
+  if (!aligned(out, 8)) return fail(DSA_ERR_INVALID_ARG, "out must be 8-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   cudaError_t e;
@@ -236,7 +236,7 @@ dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* nsel, ui
   }
   int32_t* scores = reinterpret_cast<int32_t*>(w + pl.off_scores);
   if ((s = run_indexer(*p, pl, scores, w, st)) != DSA_OK) return s;
-  e = launch_topk(*p, pl, scores, idx, nsel, w, st);
+  e = launch_topk(*p, pl, scores, idx, nsel, w, st, true);
   if (e != cudaSuccess) return cuda_fail(e, "top-k");
   e = launch_attention(*p, pl, idx, nsel, out, nullptr, w, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention");

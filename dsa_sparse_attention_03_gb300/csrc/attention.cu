@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
   const int g = lane >> 2, c = lane & 3;
   const int r = blockIdx.z, h0 = blockIdx.y * kAttnHeads, split = blockIdx.x;
 
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) req_s = row_request(a.row_offsets, a.B, r);
   __syncthreads();
   const int b = req_s;
@@ -267,6 +269,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
     __syncthreads();  // Ks / Ps / idx_s are rewritten by the next tile
   }
 
+  cp_async_wait_all();  // an empty split still issued its query copies
   // Unnormalised partial output of this split.
   const int64_t prow = ((int64_t)r * a.nsplit + split) * a.H_q;
 #pragma unroll
@@ -285,41 +288,57 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
   }
 }
 
+// One CTA per (head, row): warp 0 derives the split weights exp2(m_s - M) and
+// 1/L in parallel; then every thread merges 4 columns over the splits, in
+// split order, and rounds to bf16.
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int h = blockIdx.x, r = blockIdx.y;
   extern __shared__ float wts[];  // [nsplit]
-  __shared__ float inv_l, lse_v;
-  if (threadIdx.x == 0) {
+  __shared__ float inv_l_s;
+  const int lane = threadIdx.x & 31;
+  const float2* ml = reinterpret_cast<const float2*>(a.ml) + ((int64_t)r * a.nsplit) * a.H_q + h;
+  if (threadIdx.x < 32) {
     float M = -CUDART_INF_F;
-    for (int s = 0; s < a.nsplit; ++s) {
-      const float2 v = *reinterpret_cast<const float2*>(a.ml + (((int64_t)r * a.nsplit + s) * a.H_q + h) * 2);
+    for (int s = lane; s < a.nsplit; s += 32) {
+      const float2 v = ml[(int64_t)s * a.H_q];
       if (v.y > 0.f) M = fmaxf(M, v.x);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
-    for (int s = 0; s < a.nsplit; ++s) {
-      const float2 v = *reinterpret_cast<const float2*>(a.ml + (((int64_t)r * a.nsplit + s) * a.H_q + h) * 2);
+    for (int s = lane; s < a.nsplit; s += 32) {
+      const float2 v = ml[(int64_t)s * a.H_q];
       const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
       wts[s] = w;
       L += w * v.y;
     }
-    inv_l = L > 0.f ? 1.f / L : 0.f;
-    lse_v = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) {
+      inv_l_s = L > 0.f ? 1.f / L : 0.f;
+      if (a.lse) a.lse[(int64_t)r * a.H_q + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
+    }
   }
   __syncthreads();
+  const float inv_l = inv_l_s;
   uint16_t* o = a.out + ((int64_t)r * a.H_q + h) * a.D_v;
-  for (int col = threadIdx.x * 2; col < a.D_v; col += blockDim.x * 2) {
-    float x0 = 0.f, x1 = 0.f;
+  const float* part = a.part + (((int64_t)r * a.nsplit) * a.H_q + h) * a.D_v;
+  const int64_t sstride = (int64_t)a.H_q * a.D_v;
+  for (int col = threadIdx.x * 4; col < a.D_v; col += blockDim.x * 4) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < a.nsplit; ++s) {
       const float w = wts[s];
       if (w == 0.f) continue;
-      const float2 v = *reinterpret_cast<const float2*>(
-          a.part + (((int64_t)r * a.nsplit + s) * a.H_q + h) * a.D_v + col);
-      x0 += w * v.x;
-      x1 += w * v.y;
+      const float4 v = *reinterpret_cast<const float4*>(part + s * sstride + col);
+      x.x += w * v.x; x.y += w * v.y; x.z += w * v.z; x.w += w * v.w;
     }
-    *reinterpret_cast<uint32_t*>(o + col) = pack_bf16(x0 * inv_l, x1 * inv_l);
+    uint2 pk;
+    pk.x = pack_bf16(x.x * inv_l, x.y * inv_l);
+    pk.y = pack_bf16(x.z * inv_l, x.w * inv_l);
+    *reinterpret_cast<uint2*>(o + col) = pk;
   }
-  if (a.lse && threadIdx.x == 0) a.lse[(int64_t)r * a.H_q + h] = lse_v;
 }
 
 template <int NT>
@@ -327,8 +346,7 @@ cudaError_t launch_split(const AttnArgs& a, dim3 grid, size_t smem, cudaStream_t
   cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<NT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  attn_split_kernel<NT><<<grid, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(attn_split_kernel<NT>, grid, dim3(kThreads), smem, st, a);
 }
 
 }  // namespace
@@ -366,8 +384,7 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
     default: e = launch_split<16>(a, grid, smem, st); break;
   }
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3(p.H_q, p.R), 128, (size_t)pl.nsplit * 4, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(attn_combine_kernel, dim3(p.H_q, p.R), dim3(128), (size_t)pl.nsplit * 4, st, a);
 }
 
 }  // namespace dsa

@@ -52,6 +52,46 @@ __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
   if (status) atomicOr(status, bit);
 }
 
+// Programmatic dependent launch: every kernel waits for its predecessor in the
+// stream to complete (and flush) before touching global memory, and lets its
+// successor be scheduled early.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with the programmatic-stream-serialization attribute (captured into
+// CUDA graphs as a programmatic edge).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Per-row running max of the ordered keys and of their complements (= ~min),
+// merged into RowState.umax / uminv by the indexers.
+__device__ __forceinline__ void row_minmax_flush(RowState* st, uint32_t umax, uint32_t uminv) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, o));
+    uminv = max(uminv, __shfl_xor_sync(0xffffffffu, uminv, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    if (umax) atomicMax(&st->umax, umax);
+    if (uminv) atomicMax(&st->uminv, uminv);
+  }
+}
+
 // Launchers (one per translation unit).  Each returns the launch error.
 // Both indexers also clear the workspace's status word and top-k state
 // ([0, Plan::zero_end)), so a decode step needs no separate memset.
@@ -60,8 +100,9 @@ cudaError_t launch_indexer_dp4a(const dsa_problem& p, const Plan& pl, int32_t* s
 cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                               cudaStream_t st);
 bool indexer_tc_supported(const dsa_problem& p);
+// minmax_done: the indexer already merged each row's key range into RowState.
 cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* scores,
-                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st);
+                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st, bool minmax_done);
 cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t* idx,
                              const int32_t* nsel, uint16_t* out, float* lse, char* ws,
                              cudaStream_t st);

@@ -29,6 +29,7 @@ struct IdxArgs {
   int total_tiles_bound;
   uint4* zero;          // workspace words to clear (status + top-k state)
   int n_zero;
+  RowState* rows;       // per-row key range for the top-k
 };
 
 // Exclusive prefix of per-request tile counts into tile_start[0..B], by one block.
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(kThreads) indexer_dp4a_kernel(IdxArgs a) {
   int4* q_s = reinterpret_cast<int4*>(smem + ts_bytes);                  // [H_i * D_I / 16]
   int* w_s = reinterpret_cast<int*>(smem + ts_bytes + (size_t)a.H_i * D_I);
 
+  pdl_wait();
   for (int i = blockIdx.x * kThreads + threadIdx.x; i < a.n_zero; i += gridDim.x * kThreads)
     a.zero[i] = make_uint4(0, 0, 0, 0);
   tile_prefix(a.offsets, a.B, TILE, tile_start);
@@ -150,13 +152,21 @@ __global__ void __launch_bounds__(kThreads) indexer_dp4a_kernel(IdxArgs a) {
         for (int kk = 0; kk < KPT; ++kk) acc[kk] += wh * (a.relu ? max(d[kk], 0) : d[kk]);
       }
       int32_t* out = a.scores + (int64_t)r * a.L_max;
+      uint32_t umax = 0, uminv = 0;
 #pragma unroll
       for (int kk = 0; kk < KPT; ++kk) {
         const int t = t0 + kk * kThreads + threadIdx.x;
-        if (t < len) out[t] = acc[kk];
+        if (t < len) {
+          out[t] = acc[kk];
+          const uint32_t u = ordered_key(acc[kk]);
+          umax = max(umax, u);
+          uminv = max(uminv, ~u);
+        }
       }
+      row_minmax_flush(a.rows + r, umax, uminv);
     }
   }
+  pdl_trigger();
 }
 
 template <int D_I, int KPT>
@@ -169,6 +179,7 @@ cudaError_t launch(const dsa_problem& p, const Plan& pl, int32_t* scores, char* 
   a.relu = (p.flags & DSA_FLAG_NO_RELU) ? 0 : 1;
   a.zero = reinterpret_cast<uint4*>(ws);
   a.n_zero = (int)(pl.zero_end / 16);
+  a.rows = reinterpret_cast<RowState*>(ws + pl.off_state);
   const int64_t bound = p.L_total / TILE + p.B;
   a.total_tiles_bound = (int)bound;
   const size_t ts_bytes = ((size_t)(p.B + 1) * 4 + 15) / 16 * 16;
@@ -181,8 +192,7 @@ cudaError_t launch(const dsa_problem& p, const Plan& pl, int32_t* scores, char* 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int64_t grid = bound < int64_t(sms) * 16 ? bound : int64_t(sms) * 16;
   if (grid < 1) grid = 1;
-  indexer_dp4a_kernel<D_I, KPT><<<(unsigned)grid, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(indexer_dp4a_kernel<D_I, KPT>, dim3((unsigned)grid), dim3(kThreads), smem, st, a);
 }
 
 }  // namespace

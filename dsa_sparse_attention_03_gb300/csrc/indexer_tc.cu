@@ -36,11 +36,13 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kConvWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = (2 + kConvWarps + kEpiWarps) * 32;
 constexpr int kTile = 128;                 // keys per tile (MMA M)
 constexpr uint64_t kWaitNs = 4000000000ull;
 constexpr int kConvWarp0 = 2;
-constexpr int kEpiWarp0 = 6;
+constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
 constexpr int kMaxRG = 4;                  // query rows per MMA group (N <= 256)
 
 struct TcArgs {
@@ -53,6 +55,7 @@ struct TcArgs {
   int32_t* scores;
   uint32_t* status;
   int64_t L_max;
+  RowState* rows;       // per-row key range for the top-k
   int B, H_i, D_i, RG, stages, relu;
   uint32_t off_b, off_stage, off_w, off_bar, off_misc, off_prefix;   // shared-memory map
   uint32_t tmem_cols;
@@ -218,9 +221,10 @@ struct TileInfo {
   int r0, nrows;      // first row and rows of the group
   int L_b;
   int64_t base;       // offsets[b]
+  int lo, hi;         // global tile ids [lo, hi) of this (request, group)
 };
 
-__device__ __forceinline__ TileInfo tile_info(const TcArgs& a, const int* prefix, int gt) {
+__device__ __noinline__ TileInfo tile_lookup(const TcArgs& a, const int* prefix, int gt) {
   int lo = 0, hi = a.B - 1;  // largest b with prefix[b] <= gt
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -234,6 +238,8 @@ __device__ __forceinline__ TileInfo tile_info(const TcArgs& a, const int* prefix
   const int local = gt - prefix[lo];
   ti.g = local / tiles_b;
   ti.j = local - ti.g * tiles_b;
+  ti.lo = prefix[lo] + ti.g * tiles_b;
+  ti.hi = ti.lo + tiles_b;
   const int rb = a.row_offsets[lo];
   const int rows_b = a.row_offsets[lo + 1] - rb;
   ti.r0 = rb + ti.g * a.RG;
@@ -241,20 +247,36 @@ __device__ __forceinline__ TileInfo tile_info(const TcArgs& a, const int* prefix
   return ti;
 }
 
+// Advances a cached TileInfo to global tile `gt` (tiles are visited in order);
+// returns true when the (request, row group) changed.
+__device__ __forceinline__ bool tile_step(const TcArgs& a, const int* prefix, int gt, TileInfo& ti) {
+  if (gt >= ti.lo && gt < ti.hi) {
+    ti.j = gt - ti.lo;
+    return false;
+  }
+  ti = tile_lookup(a, prefix, gt);
+  return true;
+}
+
+template <int D_I, int S>
 __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
+  constexpr int CPR = D_I / 16;                            // 16-byte chunks per int8 key row
+  constexpr uint32_t kABytes = kTile * D_I * 2;             // one fp16 A buffer
+  constexpr uint32_t kStageBytes = kTile * D_I;             // one int8 tile
+  constexpr int kConvThreads = kConvWarps * 32;
+  constexpr int kChunksPerThread = kTile * CPR / kConvThreads;
+
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // Layout (offsets from the 1024-aligned base).
   unsigned char* A = smem;                                 // 2 x [D_i/64][128][128 B]
   unsigned char* Bop = smem + a.off_b;                     // [D_i/64][N_max][128 B]
   unsigned char* stage = smem + a.off_stage;               // S x [128][D_i] int8
-  int* w_s = reinterpret_cast<int*>(smem + a.off_w);       // [RG][H_i] + [RG] sums
+  int* w_s = reinterpret_cast<int*>(smem + a.off_w);       // per epilogue warp
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.off_bar);
   volatile int* misc = reinterpret_cast<volatile int*>(smem + a.off_misc);  // [0] tmem, [1] abort
   int* prefix = reinterpret_cast<int*>(smem + a.off_prefix);               // [B+1]
 
-  const int S = a.stages;
   const uint32_t bar_full = cvta_smem(bars);                // S
   const uint32_t bar_empty = bar_full + 8 * S;              // S
   const uint32_t bar_afull = bar_empty + 8 * S;             // 2
@@ -263,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  pdl_wait();
+  pdl_trigger();
   for (int i = blockIdx.x * kThreads + tid; i < a.n_zero; i += gridDim.x * kThreads)
     a.zero[i] = make_uint4(0, 0, 0, 0);
 
@@ -288,20 +312,21 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
     }
     if (lane == 0) prefix[a.B] = run;
   }
-  if (tid == 0) {
+  if (tid == 32) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 4);
+      mbar_init(bar_empty + 8 * s, kConvWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_afull + 8 * i, 4);
+      mbar_init(bar_afull + 8 * i, kConvWarps);
       mbar_init(bar_accfull + 8 * i, 1);
-      mbar_init(bar_accempty + 8 * i, 4);
+      mbar_init(bar_accempty + 8 * i, kEpiWarps);
     }
     misc[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
+    __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      cvta_smem((const void*)misc)),
                  "r"(a.tmem_cols)
@@ -318,10 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   const int t_begin = (int)(((int64_t)blockIdx.x * total) / gridDim.x);
   const int t_end = (int)(((int64_t)(blockIdx.x + 1) * total) / gridDim.x);
   const int n_local = t_end - t_begin;
-  const int D_I = a.D_i;                                   // K of the MMA
   const int N_max = a.RG * a.H_i;
-  const uint32_t a_bytes = kTile * D_I * 2;                // one fp16 A buffer
-  const uint32_t stage_bytes = kTile * D_I;
+  TileInfo ti;
+  ti.lo = ti.hi = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -330,19 +354,18 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
       for (int i = 0; i < n_local; ++i) {
         const int s = i % S;
         if (i >= S && !wait_bar(bar_empty + 8 * s, ((i / S) - 1) & 1, abort_flag, a.status)) break;
-        const TileInfo ti = tile_info(a, prefix, t_begin + i);
+        tile_step(a, prefix, t_begin + i, ti);
         const int rows = min(kTile, ti.L_b - ti.j * kTile);
         const uint32_t bytes = (uint32_t)rows * D_I;
         mbar_arrive_tx(bar_full + 8 * s, bytes);
-        tma_load_1d(cvta_smem(stage + s * stage_bytes),
+        tma_load_1d(cvta_smem(stage + s * kStageBytes),
                     a.k_idx + (ti.base + (int64_t)ti.j * kTile) * D_I, bytes, bar_full + 8 * s);
         issued = i + 1;
       }
       // Drain: every issued copy must have landed before the CTA can exit.
       for (int i = max(0, issued - S); i < issued; ++i) {
-        const int s = i % S;
         const uint64_t t0 = globaltimer();
-        while (!mbar_try(bar_full + 8 * s, (i / S) & 1) && globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try(bar_full + 8 * (i % S), (i / S) & 1) && globaltimer() - t0 < kWaitNs) {
         }
       }
     }
@@ -350,15 +373,16 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int issued = 0;
+      const uint32_t b_base = cvta_smem(Bop);
       for (int i = 0; i < n_local; ++i) {
         const int buf = i & 1;
+        tile_step(a, prefix, t_begin + i, ti);
+        const uint32_t idesc = idesc_f16(kTile, ti.nrows * a.H_i);
         if (i >= 2 && !wait_bar(bar_accempty + 8 * buf, ((i - 2) >> 1) & 1, abort_flag, a.status)) break;
         if (!wait_bar(bar_afull + 8 * buf, (i >> 1) & 1, abort_flag, a.status)) break;
         tc_fence_after();
-        const TileInfo ti = tile_info(a, prefix, t_begin + i);
-        const uint32_t idesc = idesc_f16(kTile, ti.nrows * a.H_i);
-        const uint32_t a_base = cvta_smem(A + buf * a_bytes);
-        const uint32_t b_base = cvta_smem(Bop);
+        const uint32_t a_base = cvta_smem(A + buf * kABytes);
+#pragma unroll
         for (int kk = 0; kk < D_I / 16; ++kk) {
           const uint32_t ka = a_base + (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
           const uint32_t kb = b_base + (kk >> 2) * (N_max * 128) + (kk & 3) * 32;
@@ -376,29 +400,32 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ converters
-    const int ct = tid - kConvWarp0 * 32;  // 0..127
-    int cur_b = -1, cur_g = -1;
-    const int cpr = D_I / 16;               // 16-byte chunks per int8 row
+    const int ct = tid - kConvWarp0 * 32;
     for (int i = 0; i < n_local; ++i) {
       const int s = i % S, buf = i & 1;
-      const TileInfo ti = tile_info(a, prefix, t_begin + i);
+      const bool new_group = tile_step(a, prefix, t_begin + i, ti);
       if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status)) break;
       if (i >= 2 && !wait_bar_warp(bar_accfull + 8 * buf, ((i - 2) >> 1) & 1, abort_flag, a.status)) break;
-      if (ti.b != cur_b || ti.g != cur_g) {
-        // New row group: B may be rewritten once every issued MMA has finished.
+      if (new_group) {
+        // B may be rewritten once every issued MMA has finished.
         if (i >= 1 &&
             !wait_bar_warp(bar_accfull + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, a.status))
           break;
         const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
-        const int nchunks = ti.nrows * a.H_i * cpr;
-        for (int q = ct; q < nchunks; q += 128)
-          convert_chunk(__ldg(src + q), Bop, q / cpr, q % cpr, (uint32_t)N_max * 128);
-        cur_b = ti.b;
-        cur_g = ti.g;
+        const int nchunks = ti.nrows * a.H_i * CPR;
+        for (int q = ct; q < nchunks; q += kConvThreads)
+          convert_chunk(__ldg(src + q), Bop, q / CPR, q % CPR, (uint32_t)N_max * 128);
       }
-      const int4* st = reinterpret_cast<const int4*>(stage + s * stage_bytes);
-      unsigned char* abuf = A + buf * a_bytes;
-      for (int q = ct; q < kTile * cpr; q += 128) convert_chunk(st[q], abuf, q / cpr, q % cpr, kTile * 128);
+      const int4* st = reinterpret_cast<const int4*>(stage + s * kStageBytes);
+      unsigned char* abuf = A + buf * kABytes;
+      int4 v[kChunksPerThread];
+#pragma unroll
+      for (int it = 0; it < kChunksPerThread; ++it) v[it] = st[ct + it * kConvThreads];
+#pragma unroll
+      for (int it = 0; it < kChunksPerThread; ++it) {
+        const int q = ct + it * kConvThreads;
+        convert_chunk(v[it], abuf, q / CPR, q % CPR, kTile * 128);
+      }
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
@@ -410,16 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;            // TMEM lanes this warp may read
     const int m = quarter * 32 + lane;       // key row of the tile = TMEM lane
-    // Each epilogue warp keeps its own copy of the group's weights (no
-    // cross-warp barrier): [RG][H_i] weights, then [RG] weight sums.
-    int* w_own = w_s + (warp - kEpiWarp0) * (a.RG * a.H_i + a.RG);
+    const int wstride = (a.RG * a.H_i + 4 * kMaxRG + 3) & ~3;
+    int* w_own = w_s + (warp - kEpiWarp0) * wstride;
     int* wsum = w_own + a.RG * a.H_i;
-    int cur_b = -1, cur_g = -1;
+    const float floor_v = a.relu ? 0.f : -3.0e38f;   // max(d, floor) = ReLU or identity
     int rlen[kMaxRG];
+    uint32_t umax[kMaxRG], uminv[kMaxRG];
+    int cur_r0 = -1, cur_n = 0;
     for (int i = 0; i < n_local; ++i) {
       const int buf = i & 1;
-      const TileInfo ti = tile_info(a, prefix, t_begin + i);
-      if (ti.b != cur_b || ti.g != cur_g) {
+      if (tile_step(a, prefix, t_begin + i, ti)) {
+        for (int jr = 0; jr < cur_n; ++jr) row_minmax_flush(a.rows + cur_r0 + jr, umax[jr], uminv[jr]);
         __syncwarp();
         for (int q = lane; q < ti.nrows * a.H_i; q += 32) w_own[q] = a.w_idx[(int64_t)ti.r0 * a.H_i + q];
         __syncwarp();
@@ -430,9 +458,13 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
         }
         __syncwarp();
 #pragma unroll
-        for (int jr = 0; jr < kMaxRG; ++jr) rlen[jr] = jr < ti.nrows ? a.row_len[ti.r0 + jr] : 0;
-        cur_b = ti.b;
-        cur_g = ti.g;
+        for (int jr = 0; jr < kMaxRG; ++jr) {
+          rlen[jr] = jr < ti.nrows ? a.row_len[ti.r0 + jr] : 0;
+          umax[jr] = 0u;
+          uminv[jr] = 0u;
+        }
+        cur_r0 = ti.r0;
+        cur_n = ti.nrows;
       }
       if (!wait_bar_warp(bar_accfull + 8 * buf, (i >> 1) & 1, abort_flag, a.status)) break;
       tc_fence_after();
@@ -441,26 +473,36 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
       for (int jr = 0; jr < kMaxRG; ++jr) {
         if (jr >= ti.nrows) break;
         uint32_t acc = 0;  // wraps mod 2^32; the true score fits int32
-        const int* wr = w_own + jr * a.H_i;
+        const int4* wr = reinterpret_cast<const int4*>(w_own + jr * a.H_i);
         for (int h0 = 0; h0 < a.H_i; h0 += 32) {
           uint32_t v[32];
           tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * N_max + jr * a.H_i + h0, v);
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            float d = __uint_as_float(v[h]);
-            if (a.relu) d = fmaxf(d, 0.f);
-            // d is an exact integer with |d| < 2^22: adding 1.5 * 2^23 puts it in
-            // the low mantissa bits (bit pattern 0x4B400000 + d).
-            acc += (uint32_t)__float_as_int(d + 12582912.f) * (uint32_t)wr[h0 + h];
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const int4 w4 = wr[(h0 >> 2) + h4];
+            const int wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float d = fmaxf(__uint_as_float(v[4 * h4 + e]), floor_v);
+              // d is an exact integer with |d| < 2^22: adding 1.5 * 2^23 puts it in
+              // the low mantissa bits (bit pattern 0x4B400000 + d).
+              acc += (uint32_t)__float_as_int(d + 12582912.f) * (uint32_t)wv[e];
+            }
           }
         }
         acc -= 0x4B400000u * (uint32_t)wsum[jr];
-        if (t < rlen[jr]) a.scores[(int64_t)(ti.r0 + jr) * a.L_max + t] = (int32_t)acc;
+        if (t < rlen[jr]) {
+          a.scores[(int64_t)(ti.r0 + jr) * a.L_max + t] = (int32_t)acc;
+          const uint32_t u = acc ^ 0x80000000u;
+          umax[jr] = max(umax[jr], u);
+          uminv[jr] = max(uminv[jr], ~u);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_accempty + 8 * buf);
     }
+    for (int jr = 0; jr < cur_n; ++jr) row_minmax_flush(a.rows + cur_r0 + jr, umax[jr], uminv[jr]);
   }
 
   tc_fence_before();
@@ -478,15 +520,24 @@ bool indexer_tc_supported(const dsa_problem& p) {
   return (p.D_i == 64 || p.D_i == 128) && (p.H_i == 32 || p.H_i == 64 || p.H_i == 128);
 }
 
+template <int D_I, int S>
+cudaError_t launch_tc(const TcArgs& a, int sms, size_t smem, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<D_I, S>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(indexer_tc_kernel<D_I, S>, dim3(sms), dim3(kThreads), smem, st, a);
+}
+
 cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                               cudaStream_t st) {
   TcArgs a;
-  uint32_t* status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
+  a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
+  a.rows = reinterpret_cast<RowState*>(ws + pl.off_state);
   a.zero = reinterpret_cast<uint4*>(ws);
   a.n_zero = (int)(pl.zero_end / 16);
   a.q_idx = p.q_idx; a.w_idx = p.w_idx; a.k_idx = p.k_idx;
   a.offsets = p.offsets; a.row_offsets = p.row_offsets; a.row_len = p.row_len;
-  a.scores = scores; a.status = status; a.L_max = p.L_max;
+  a.scores = scores; a.L_max = p.L_max;
   a.B = p.B; a.H_i = p.H_i; a.D_i = p.D_i; a.relu = (p.flags & DSA_FLAG_NO_RELU) ? 0 : 1;
   const int per_req = (p.R + p.B - 1) / p.B;
   int RG = 256 / p.H_i;
@@ -495,18 +546,17 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   a.RG = RG;
   const int N_max = RG * p.H_i;
   const int D_i = p.D_i;
-  // stages: as many 16 KB key tiles in flight as shared memory allows
   const uint32_t a_bytes = 2u * 128u * D_i * 2u;
   const uint32_t b_bytes = (uint32_t)N_max * D_i * 2u;
   const uint32_t stage_bytes = 128u * D_i;
   const uint32_t prefix_bytes = ((uint32_t)(p.B + 1) * 4u + 15u) / 16u * 16u;
-  const uint32_t w_bytes = (4u * (uint32_t)(RG * p.H_i + RG) * 4u + 15u) / 16u * 16u;  // per epilogue warp
+  const uint32_t wstride = (uint32_t)((RG * p.H_i + 4 * kMaxRG + 3) & ~3);
+  const uint32_t w_bytes = kEpiWarps * wstride * 4u;
   const uint32_t budget = 227u * 1024u - 1024u;   // minus the alignment slack
-  int S = 8;
   auto total_for = [&](int s) {
     return a_bytes + b_bytes + s * stage_bytes + w_bytes + (2 * s + 6) * 8 + 16 + prefix_bytes;
   };
-  while (S > 2 && total_for(S) > budget) --S;
+  const int S = total_for(8) <= budget ? 8 : 4;
   if (total_for(S) > budget) return cudaErrorInvalidConfiguration;
   a.stages = S;
   a.off_b = a_bytes;
@@ -520,14 +570,11 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   a.tmem_cols = cols;
   size_t smem = (size_t)a.off_prefix + prefix_bytes + 1024;
   if (smem < 120u * 1024u) smem = 120u * 1024u;   // one CTA per SM: TMEM is never contended
-  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  indexer_tc_kernel<<<sms, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  if (D_i == 128) return S == 8 ? launch_tc<128, 8>(a, sms, smem, st) : launch_tc<128, 4>(a, sms, smem, st);
+  return S == 8 ? launch_tc<64, 8>(a, sms, smem, st) : launch_tc<64, 4>(a, sms, smem, st);
 }
 
 }  // namespace dsa

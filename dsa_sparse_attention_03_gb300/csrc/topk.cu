@@ -5,9 +5,11 @@
 // a sort of the small surviving list, and the original exact algorithm for the
 // ambiguous cases -- keeping the same positions in the same order.  Here:
 //
-//   minmax   one scan: the range [umin, umax] of the row's order-preserving
-//            keys u = s ^ 0x80000000; the bits above their highest differing
-//            bit are common to all, so only D = bitlen(umin ^ umax) bits remain.
+//   minmax   the range [umin, umax] of the row's order-preserving keys
+//            u = s ^ 0x80000000 (merged by the indexer's epilogue in a decode
+//            step; a separate scan for dsa_topk); the bits above the highest
+//            bit where umin and umax differ are common to every key, so only
+//            D = bitlen(umin ^ umax) bits remain to be searched.
 //   pass x3  radix search for the k-th largest key T, 11 bits per pass, over
 //            the positions still in the candidate bin (shared-memory histogram,
 //            global merge, the row's last CTA picks the bin).  Rows finish in
@@ -103,48 +105,55 @@ __device__ bool last_arrival(uint32_t* c, uint32_t expected) {
 }
 
 __global__ void __launch_bounds__(kThreads) topk_minmax_kernel(TopkArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.y;
   const int len = a.row_len[r];
   const int start = blockIdx.x * a.chunk;
   const int end = min(start + a.chunk, len);
   const int32_t* s = a.scores + (int64_t)r * a.L_max;
-  RowState* st = a.state + r;
   uint32_t umax = 0, uminv = 0;
   for (int t = start + threadIdx.x; t < end; t += kThreads) {
     const uint32_t u = ordered_key(s[t]);
     umax = max(umax, u);
     uminv = max(uminv, ~u);
   }
-  block_max2(umax, uminv);
-  if (threadIdx.x == 0 && start < end) {
-    atomicMax(&st->umax, umax);
-    atomicMax(&st->uminv, uminv);
-  }
-  if (!last_arrival(&st->arrive[kPhaseMinMax], gridDim.x)) return;
-  if (threadIdx.x != 0) return;
-  const uint32_t n_take = (uint32_t)min(a.k, max(len, 0));
-  st->n_take = n_take;
-  st->n_gt = 0;
-  if (len <= 0) { st->mode = 2; return; }
-  if (len <= a.k) { st->mode = 1; return; }
-  const uint32_t hi = ld_volatile(&st->umax);
-  const uint32_t lo = ~ld_volatile(&st->uminv);
-  const uint32_t diff = hi ^ lo;
-  const uint32_t D = diff ? 32u - __clz(diff) : 0u;
-  st->shift = D;
-  st->prefix = D >= 32 ? 0u : (hi >> D);
-  st->k_rem = (uint32_t)a.k;
-  st->mode = 0;
+  row_minmax_flush(a.state + r, umax, uminv);
 }
 
 __global__ void __launch_bounds__(kThreads) topk_pass_kernel(TopkArgs a, int phase) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.y;
   RowState* st = a.state + r;
-  if (st->mode != 0) return;
-  const uint32_t shift = st->shift;
-  if (shift == 0) return;                       // threshold already exact
-  const uint32_t prefix = st->prefix;
-  const uint32_t k_rem = st->k_rem;             // read before the last CTA rewrites it
+  const int len = a.row_len[r];
+  uint32_t mode, shift, prefix, k_rem;
+  if (phase == kPhasePass0) {
+    // Initial state from the row's key range; every CTA derives the same.
+    mode = len <= 0 ? 2u : (len <= a.k ? 1u : 0u);
+    const uint32_t hi = st->umax, lo = ~st->uminv;
+    const uint32_t diff = hi ^ lo;
+    shift = (mode == 0 && diff) ? 32u - __clz(diff) : 0u;
+    prefix = shift >= 32 ? 0u : (hi >> shift);
+    k_rem = (uint32_t)a.k;
+    if (mode != 0 || shift == 0) {
+      // Nothing to search: the last CTA records the state for the next kernels.
+      if (!last_arrival(&st->arrive[phase], gridDim.x) || threadIdx.x != 0) return;
+      st->mode = mode;
+      st->shift = 0;
+      st->prefix = prefix;
+      st->k_rem = k_rem;
+      st->n_take = (uint32_t)min(a.k, max(len, 0));
+      return;
+    }
+  } else {
+    mode = st->mode;
+    if (mode != 0) return;
+    shift = st->shift;
+    if (shift == 0) return;                     // threshold already exact
+    prefix = st->prefix;
+    k_rem = st->k_rem;                          // read before the last CTA rewrites it
+  }
   const uint32_t bits = min(shift, (uint32_t)kHistBits);
   const uint32_t ns = shift - bits;
   const uint32_t mask = (1u << bits) - 1u;
@@ -154,7 +163,6 @@ __global__ void __launch_bounds__(kThreads) topk_pass_kernel(TopkArgs a, int pha
   for (int i = threadIdx.x; i < nbins; i += kThreads) h[i] = 0;
   __syncthreads();
 
-  const int len = a.row_len[r];
   const int start = blockIdx.x * a.chunk;
   const int end = min(start + a.chunk, len);
   const int32_t* s = a.scores + (int64_t)r * a.L_max;
@@ -202,6 +210,10 @@ __global__ void __launch_bounds__(kThreads) topk_pass_kernel(TopkArgs a, int pha
         st->k_rem = k_rem - acc;
         st->prefix = (prefix << bits) | (uint32_t)bin;
         st->shift = ns;
+        if (phase == kPhasePass0) {
+          st->mode = 0;
+          st->n_take = (uint32_t)a.k;
+        }
         break;
       }
       acc += local[j];
@@ -212,6 +224,8 @@ __global__ void __launch_bounds__(kThreads) topk_pass_kernel(TopkArgs a, int pha
 }
 
 __global__ void __launch_bounds__(kThreads) topk_compact_kernel(TopkArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.y;
   RowState* st = a.state + r;
   const uint32_t mode = st->mode;
@@ -248,6 +262,8 @@ __global__ void __launch_bounds__(kThreads) topk_compact_kernel(TopkArgs a) {
 }
 
 __global__ void __launch_bounds__(kThreads) topk_ties_kernel(TopkArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.y;
   RowState* st = a.state + r;
   if (st->mode != 0) return;
@@ -288,6 +304,8 @@ __global__ void __launch_bounds__(kThreads) topk_ties_kernel(TopkArgs a) {
 }
 
 __global__ void __launch_bounds__(kThreads) topk_rank_kernel(TopkArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.y;
   RowState* st = a.state + r;
   const int n = st->mode == 2 ? 0 : (int)st->n_take;
@@ -315,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) topk_rank_kernel(TopkArgs a) {
 }  // namespace
 
 cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* scores,
-                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st) {
+                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st, bool minmax_done) {
   TopkArgs a;
   a.scores = scores;
   a.row_len = p.row_len;
@@ -328,20 +346,19 @@ cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* sco
   a.L_max = pl.L_max;
   a.k = pl.k;
   a.chunk = pl.chunk;
-  const dim3 grid(pl.nchunk, pl.R);
-  topk_minmax_kernel<<<grid, kThreads, 0, st>>>(a);
-  topk_pass_kernel<<<grid, kThreads, 0, st>>>(a, kPhasePass0);
-  topk_pass_kernel<<<grid, kThreads, 0, st>>>(a, kPhasePass1);
-  topk_pass_kernel<<<grid, kThreads, 0, st>>>(a, kPhasePass2);
-  topk_compact_kernel<<<grid, kThreads, 0, st>>>(a);
-  topk_ties_kernel<<<grid, kThreads, 0, st>>>(a);
+  const dim3 grid(pl.nchunk, pl.R), block(kThreads);
+  cudaError_t e;
+  if (!minmax_done && (e = launch_pdl(topk_minmax_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
+  if ((e = launch_pdl(topk_pass_kernel, grid, block, 0, st, a, (int)kPhasePass0)) != cudaSuccess) return e;
+  if ((e = launch_pdl(topk_pass_kernel, grid, block, 0, st, a, (int)kPhasePass1)) != cudaSuccess) return e;
+  if ((e = launch_pdl(topk_pass_kernel, grid, block, 0, st, a, (int)kPhasePass2)) != cudaSuccess) return e;
+  if ((e = launch_pdl(topk_compact_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
+  if ((e = launch_pdl(topk_ties_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
   const size_t smem = (size_t)pl.k * 8;
-  cudaError_t e = cudaFuncSetAttribute(topk_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  e = cudaFuncSetAttribute(topk_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 rgrid((pl.k + kRankPerBlock - 1) / kRankPerBlock, pl.R);
-  topk_rank_kernel<<<rgrid, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(topk_rank_kernel, rgrid, block, smem, st, a);
 }
 
 }  // namespace dsa

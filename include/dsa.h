@@ -51,7 +51,7 @@
  *   scores  int32 [R, L_max]      entry (r, t) for t < row_len[r]; others untouched
  *   idx     int32 [R, k]          request-local positions; entries past nsel[r] = -1
  *   nsel    int32 [R]             min(k, row_len[r])
- *   out     bf16  [R, H_q, D_v]   round-to-nearest-even
+ *   out     bf16  [R, H_q, D_v]   round-to-nearest-even; 8-byte aligned base
  *   lse     fp32  [R, H_q]        natural-log log-sum-exp of the scaled logits
  */
 #ifndef DSA_H
