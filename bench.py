@@ -103,7 +103,9 @@ def make_layers(n_layers, L, device):
     layers = []
     for layer in range(n_layers):
         x = gen.l300k(layer=layer, L=L) if L == L_LONG else gen.l64k(layer=layer, L=L)
-        prob, t = dsa.upload_inputs(x, device=device)
+        # The caller declares its int8 value range (here the data's own bound).
+        qk = int(max(np.abs(x.q_idx.astype(np.int32)).max(), np.abs(x.k_idx.astype(np.int32)).max()))
+        prob, t = dsa.upload_inputs(x, device=device, qk_abs_max=qk)
         layers.append((x, prob, t))
     ws = dsa.alloc_workspace(layers[0][1], device=device)   # same sizes for every layer
     k = layers[0][0].k

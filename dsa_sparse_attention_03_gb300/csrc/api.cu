@@ -105,10 +105,9 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   size_t off = 0;
   P.off_status = off; off += 256;
   P.off_state = off; off = align_up(off + R * sizeof(RowState), 256);
-  P.off_hist = off; off = align_up(off + R * kHistBins * 4, 256);
-  P.off_tiecnt = off; off = align_up(off + R * size_t(P.nchunk) * 4, 256);
+  P.off_hist = off; off = align_up(off + R * kBuckets * 4, 256);
   P.zero_end = off;
-  P.off_sel = off; off = align_up(off + R * size_t(p->k) * 8, 256);
+  P.off_surv = off; off = align_up(off + R * size_t(kCapFast) * 8, 256);
   P.off_scores = off; off = align_up(off + R * size_t(p->L_max) * 4, 256);
   const int hq = p->H_q > 0 ? p->H_q : 0;
   const int dv = p->D_v > 0 ? p->D_v : 0;
@@ -194,7 +193,7 @@ dsa_status dsa_topk(const dsa_problem* p, const int32_t* scores, int32_t* idx, i
   cudaError_t e = cudaMemsetAsync(ws, 0, pl.zero_end, st);
   if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
   if (p->R == 0) return DSA_OK;
-  e = launch_topk(*p, pl, scores, idx, nsel, static_cast<char*>(ws), st, false);
+  e = launch_topk(*p, pl, scores, idx, nsel, static_cast<char*>(ws), st);
   if (e != cudaSuccess) return cuda_fail(e, "top-k");
   return DSA_OK;
 }
@@ -236,7 +235,7 @@ dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* nsel, ui
   }
   int32_t* scores = reinterpret_cast<int32_t*>(w + pl.off_scores);
   if ((s = run_indexer(*p, pl, scores, w, st)) != DSA_OK) return s;
-  e = launch_topk(*p, pl, scores, idx, nsel, w, st, true);
+  e = launch_topk(*p, pl, scores, idx, nsel, w, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-k");
   e = launch_attention(*p, pl, idx, nsel, out, nullptr, w, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention");

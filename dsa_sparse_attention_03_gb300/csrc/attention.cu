@@ -327,10 +327,22 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
   const float* part = a.part + (((int64_t)r * a.nsplit) * a.H_q + h) * a.D_v;
   const int64_t sstride = (int64_t)a.H_q * a.D_v;
   for (int col = threadIdx.x * 4; col < a.D_v; col += blockDim.x * 4) {
+    // Every split wrote its partial (zeros when it saw no position), so the
+    // loads are unconditional and eight of them are kept in flight.
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < a.nsplit; ++s) {
+    int s = 0;
+    for (; s + 8 <= a.nsplit; s += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const float4*>(part + (s + j) * sstride + col);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w = wts[s + j];
+        x.x += w * v[j].x; x.y += w * v[j].y; x.z += w * v[j].z; x.w += w * v[j].w;
+      }
+    }
+    for (; s < a.nsplit; ++s) {
       const float w = wts[s];
-      if (w == 0.f) continue;
       const float4 v = *reinterpret_cast<const float4*>(part + s * sstride + col);
       x.x += w * v.x; x.y += w * v.y; x.z += w * v.z; x.w += w * v.w;
     }

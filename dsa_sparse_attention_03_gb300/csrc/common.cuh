@@ -9,29 +9,27 @@
 
 namespace dsa {
 
-constexpr int kHistBits = 11;                 // radix digit of the threshold search
-constexpr int kHistBins = 1 << kHistBits;
+constexpr int kBucketBits = 13;               // float-like score code of the top-k histogram
+constexpr int kBuckets = 1 << kBucketBits;
+constexpr int kCapFast = 4096;                // survivors ranked directly (else exact fallback)
 constexpr int kAttnRows = 64;                 // selected positions per attention CTA
 constexpr int kAttnHeads = 16;                // query heads per attention CTA (mma M)
 constexpr int kMaxB = 4096;
 constexpr int kMaxK = 4096;
 
-// Per-row state of the threshold search, in the workspace.  Zeroed by the
-// top-k entry before its first kernel.
+// Per-row state of the top-k, in the workspace.  Zeroed (with the histograms)
+// by the indexer of a decode step, or by dsa_topk before its first kernel.
 struct RowState {
-  uint32_t umax;       // max ordered key of the row
-  uint32_t uminv;      // max of ~ordered key (= ~min)
-  uint32_t prefix;     // candidates satisfy (u >> shift) == prefix
-  uint32_t shift;      // unresolved low bits of the threshold
-  uint32_t k_rem;      // positions still to take from the candidate bin
-  uint32_t n_gt;       // slot counter for strictly-greater selections
-  uint32_t mode;       // 0 search, 1 take every position, 2 empty row
+  uint32_t bstar;      // threshold bucket
+  uint32_t n_above;    // positions in buckets above it (all selected)
+  uint32_t cand;       // positions in the threshold bucket
+  uint32_t n_union;    // survivor slot counter
+  uint32_t mode;       // fast / take all / empty / exact fallback
   uint32_t n_take;     // min(k, row_len)
-  uint32_t arrive[8];  // last-block counters, one per phase
+  uint32_t pad[2];
+  uint32_t arrive[8];  // last-CTA counters
 };
 static_assert(sizeof(RowState) == 64, "RowState is 64 bytes");
-
-enum Phase { kPhaseMinMax = 0, kPhasePass0 = 1, kPhasePass1 = 2, kPhasePass2 = 3 };
 
 // Everything the launchers need: validated sizes and the workspace map.
 struct Plan {
@@ -39,8 +37,8 @@ struct Plan {
   int flags;
   int chunk, nchunk;       // top-k: positions per CTA, CTAs per row
   int nsplit;              // attention: CTAs along the selected positions
-  size_t off_status, off_state, off_hist, off_tiecnt, zero_end;
-  size_t off_sel, off_scores, off_part, off_ml, total;
+  size_t off_status, off_state, off_hist, zero_end;
+  size_t off_surv, off_scores, off_part, off_ml, total;
 };
 
 // Order-preserving map of int32 onto uint32.
@@ -78,31 +76,17 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Per-row running max of the ordered keys and of their complements (= ~min),
-// merged into RowState.umax / uminv by the indexers.
-__device__ __forceinline__ void row_minmax_flush(RowState* st, uint32_t umax, uint32_t uminv) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, o));
-    uminv = max(uminv, __shfl_xor_sync(0xffffffffu, uminv, o));
-  }
-  if ((threadIdx.x & 31) == 0) {
-    if (umax) atomicMax(&st->umax, umax);
-    if (uminv) atomicMax(&st->uminv, uminv);
-  }
-}
 
 // Launchers (one per translation unit).  Each returns the launch error.
-// Both indexers also clear the workspace's status word and top-k state
-// ([0, Plan::zero_end)), so a decode step needs no separate memset.
+// Both indexers also clear the workspace's status word, top-k state and
+// histograms ([0, Plan::zero_end)), so a decode step needs no separate memset.
 cudaError_t launch_indexer_dp4a(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                                 cudaStream_t st);
 cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                               cudaStream_t st);
 bool indexer_tc_supported(const dsa_problem& p);
-// minmax_done: the indexer already merged each row's key range into RowState.
 cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* scores,
-                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st, bool minmax_done);
+                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st);
 cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t* idx,
                              const int32_t* nsel, uint16_t* out, float* lse, char* ws,
                              cudaStream_t st);

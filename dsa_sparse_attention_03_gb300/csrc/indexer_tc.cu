@@ -8,9 +8,16 @@
 // CUDA-core dp4a cannot sustain at HBM speed.  Here the keys are the M = 128
 // rows of a tcgen05.mma tile and the group's query heads (up to 4 rows x 64
 // heads) are N; K = D_i.  sm_103a has no int8 MMA, so both operands are
-// widened to fp16 in shared memory: every int8 is exact in fp16, every product
-// (|.| <= 2^14) and every per-head sum (|.| <= 2^21 for D_i <= 128) is exact in
-// the fp32 accumulator, so the scores stay bit-exact integers.
+// widened to fp16 in shared memory, where every int8 is exact, and the fp32
+// accumulator keeps every per-head dot exact (the host checks the bound):
+//
+//   exact conversion  k -> fp16(k): splice the biased byte into the mantissa
+//                     of 1024 and subtract 1152 (5 ops per 4 keys bytes);
+//   biased conversion k -> fp16(k + 1152) without the subtraction (3 ops per
+//                     4 bytes).  The MMA then returns q.k + 1152 * sum_d q_d,
+//                     and the epilogue removes the per-head constant exactly;
+//                     used when D_i * max|q| * 1279 < 2^24 keeps every partial
+//                     sum exact in fp32.
 //
 // One persistent CTA per SM walks a contiguous range of 128-key tiles (the
 // tile list of all (request, row group) pairs), with warp roles:
@@ -19,11 +26,13 @@
 //                 also allocates / frees TMEM.
 //   warp 1        MMA issuer (one thread): D[tmem] = A . B^T, K/16 MMAs per
 //                 tile, tcgen05.commit to the accumulator barrier.
-//   warps 2-5     converters: int8 tile -> fp16 A tile in the canonical K-major
+//   warps 2-9     converters: int8 tile -> fp16 A tile in the canonical K-major
 //                 128-byte-swizzled layout; queries -> fp16 B when the row
 //                 group changes.
-//   warps 6-9     epilogue: tcgen05.ld of each key's head dots (one TMEM lane
-//                 per key), ReLU, weight, head sum in exact int32, store.
+//   warps 10-17   epilogue, two groups of four taking alternate tiles (one per
+//                 TMEM accumulator buffer): tcgen05.ld of each key's head dots
+//                 (one TMEM lane per key), ReLU, weight, head sum in exact
+//                 int32, store.
 // A and the accumulator are double-buffered, so conversion, MMA and epilogue
 // of consecutive tiles overlap the key stream.  Every mbarrier wait is bounded
 // (a few seconds of %globaltimer); on expiry the CTA sets DSA_DEVICE_TIMEOUT,
@@ -37,13 +46,14 @@ namespace dsa {
 namespace {
 
 constexpr int kConvWarps = 8;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;                 // two groups of four
 constexpr int kThreads = (2 + kConvWarps + kEpiWarps) * 32;
-constexpr int kTile = 128;                 // keys per tile (MMA M)
+constexpr int kTile = 128;                   // keys per tile (MMA M)
 constexpr uint64_t kWaitNs = 4000000000ull;
 constexpr int kConvWarp0 = 2;
 constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
-constexpr int kMaxRG = 4;                  // query rows per MMA group (N <= 256)
+constexpr int kMaxRG = 4;                    // query rows per MMA group (N <= 256)
+constexpr float kMagic = 12582912.f;         // 1.5 * 2^23
 
 struct TcArgs {
   const int8_t* q_idx;
@@ -55,7 +65,6 @@ struct TcArgs {
   int32_t* scores;
   uint32_t* status;
   int64_t L_max;
-  RowState* rows;       // per-row key range for the top-k
   int B, H_i, D_i, RG, stages, relu;
   uint32_t off_b, off_stage, off_w, off_bar, off_misc, off_prefix;   // shared-memory map
   uint32_t tmem_cols;
@@ -186,34 +195,44 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Four int8 -> four fp16, exactly: bias to unsigned, splice the byte into the
-// mantissa of 1024.0 (0x6400 | u = 1024 + u), subtract 1152 = 1024 + 128.
+// Four int8 -> four fp16 (two half2 words).  XOR 0x80 biases each byte to
+// u = k + 128; splicing u under the exponent of 1024 (0x6400 | u) gives the
+// exact fp16 value 1024 + u = k + 1152.  The exact form then subtracts 1152.
+template <bool BIASED>
 __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t x = w ^ 0x80808080u;
-  const uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
-  const uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-  __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
-  __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
-  lo = *reinterpret_cast<uint32_t*>(&ha);
-  hi = *reinterpret_cast<uint32_t*>(&hb);
+  lo = __byte_perm(x, 0x64646464u, 0x4140);
+  hi = __byte_perm(x, 0x64646464u, 0x4342);
+  if (!BIASED) {
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&lo), bias);
+    __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&hi), bias);
+    lo = *reinterpret_cast<uint32_t*>(&ha);
+    hi = *reinterpret_cast<uint32_t*>(&hb);
+  }
 }
 
-// 16 int8 of row m (K elements 16c..16c+15) -> fp16 in a K-major SW128 operand
-// whose K-blocks (64 elements, 128 bytes per row) are `kblock_bytes` apart.
-__device__ __forceinline__ void convert_chunk(const int4 v, unsigned char* base, int m, int c,
-                                              uint32_t kblock_bytes) {
+// 16 int8 -> 16 fp16 written as two 16-byte chunks at byte offsets d0, d1.
+template <bool BIASED>
+__device__ __forceinline__ void convert16(const int4 v, unsigned char* d0, unsigned char* d1) {
   uint32_t o[8];
-  i8x4_to_f16x4((uint32_t)v.x, o[0], o[1]);
-  i8x4_to_f16x4((uint32_t)v.y, o[2], o[3]);
-  i8x4_to_f16x4((uint32_t)v.z, o[4], o[5]);
-  i8x4_to_f16x4((uint32_t)v.w, o[6], o[7]);
-  const int kb = c >> 2;
-  const int j0 = (c & 3) * 2;
-  unsigned char* row = base + kb * kblock_bytes + m * 128;
-  const int sw = m & 7;
-  *reinterpret_cast<uint4*>(row + ((j0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-  *reinterpret_cast<uint4*>(row + (((j0 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  i8x4_to_f16x4<BIASED>((uint32_t)v.x, o[0], o[1]);
+  i8x4_to_f16x4<BIASED>((uint32_t)v.y, o[2], o[3]);
+  i8x4_to_f16x4<BIASED>((uint32_t)v.z, o[4], o[5]);
+  i8x4_to_f16x4<BIASED>((uint32_t)v.w, o[6], o[7]);
+  *reinterpret_cast<uint4*>(d0) = make_uint4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint4*>(d1) = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Byte offsets, inside a K-major SW128 operand whose 64-element K-blocks are
+// `kblock_bytes` apart, of the two 16-byte chunks holding K elements
+// 16c..16c+15 of row m (the 16-byte unit index is XOR-ed with m mod 8).
+__device__ __forceinline__ void sw128_offsets(int m, int c, uint32_t kblock_bytes, uint32_t& o0,
+                                              uint32_t& o1) {
+  const uint32_t row = (uint32_t)(c >> 2) * kblock_bytes + (uint32_t)m * 128u;
+  const int j0 = (c & 3) * 2, sw = m & 7;
+  o0 = row + ((uint32_t)(j0 ^ sw) << 4);
+  o1 = row + ((uint32_t)((j0 + 1) ^ sw) << 4);
 }
 
 struct TileInfo {
@@ -258,13 +277,15 @@ __device__ __forceinline__ bool tile_step(const TcArgs& a, const int* prefix, in
   return true;
 }
 
-template <int D_I, int S>
+template <int D_I, int S, bool BIASED>
 __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   constexpr int CPR = D_I / 16;                            // 16-byte chunks per int8 key row
   constexpr uint32_t kABytes = kTile * D_I * 2;             // one fp16 A buffer
   constexpr uint32_t kStageBytes = kTile * D_I;             // one int8 tile
   constexpr int kConvThreads = kConvWarps * 32;
   constexpr int kChunksPerThread = kTile * CPR / kConvThreads;
+  constexpr int kRowsPerPass = kConvThreads / CPR;          // rows covered by one chunk sweep
+  static_assert(kRowsPerPass % 8 == 0, "swizzle phase must repeat across sweeps");
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
@@ -272,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   unsigned char* A = smem;                                 // 2 x [D_i/64][128][128 B]
   unsigned char* Bop = smem + a.off_b;                     // [D_i/64][N_max][128 B]
   unsigned char* stage = smem + a.off_stage;               // S x [128][D_i] int8
-  int* w_s = reinterpret_cast<int*>(smem + a.off_w);       // per epilogue warp
+  int2* wc_s = reinterpret_cast<int2*>(smem + a.off_w);    // per epilogue warp: (w, c) per head
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.off_bar);
   volatile int* misc = reinterpret_cast<volatile int*>(smem + a.off_misc);  // [0] tmem, [1] abort
   int* prefix = reinterpret_cast<int*>(smem + a.off_prefix);               // [B+1]
@@ -320,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_afull + 8 * i, kConvWarps);
       mbar_init(bar_accfull + 8 * i, 1);
-      mbar_init(bar_accempty + 8 * i, kEpiWarps);
+      mbar_init(bar_accempty + 8 * i, kEpiWarps / 2);
     }
     misc[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -401,6 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ converters
     const int ct = tid - kConvWarp0 * 32;
+    // This thread always converts chunk c = ct % CPR of rows m0 + kRowsPerPass*it:
+    // the swizzle phase (m mod 8) is the same for all of them.
+    const int m0 = ct / CPR, c = ct % CPR;
+    uint32_t o0, o1;
+    sw128_offsets(m0, c, kTile * 128, o0, o1);
     for (int i = 0; i < n_local; ++i) {
       const int s = i % S, buf = i & 1;
       const bool new_group = tile_step(a, prefix, t_begin + i, ti);
@@ -413,18 +439,21 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
           break;
         const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
         const int nchunks = ti.nrows * a.H_i * CPR;
-        for (int q = ct; q < nchunks; q += kConvThreads)
-          convert_chunk(__ldg(src + q), Bop, q / CPR, q % CPR, (uint32_t)N_max * 128);
+        for (int q = ct; q < nchunks; q += kConvThreads) {
+          uint32_t b0, b1;
+          sw128_offsets(q / CPR, q % CPR, (uint32_t)N_max * 128, b0, b1);
+          convert16<false>(__ldg(src + q), Bop + b0, Bop + b1);   // queries stay exact
+        }
       }
-      const int4* st = reinterpret_cast<const int4*>(stage + s * kStageBytes);
+      const int4* st = reinterpret_cast<const int4*>(stage + s * kStageBytes) + ct;
       unsigned char* abuf = A + buf * kABytes;
       int4 v[kChunksPerThread];
 #pragma unroll
-      for (int it = 0; it < kChunksPerThread; ++it) v[it] = st[ct + it * kConvThreads];
+      for (int it = 0; it < kChunksPerThread; ++it) v[it] = st[it * kConvThreads];
 #pragma unroll
       for (int it = 0; it < kChunksPerThread; ++it) {
-        const int q = ct + it * kConvThreads;
-        convert_chunk(v[it], abuf, q / CPR, q % CPR, kTile * 128);
+        const uint32_t step = (uint32_t)it * kRowsPerPass * 128u;
+        convert16<BIASED>(v[it], abuf + o0 + step, abuf + o1 + step);
       }
       fence_proxy_async();
       __syncwarp();
@@ -435,74 +464,76 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    const int ew = warp - kEpiWarp0;         // 0..7
+    const int grp = ew >> 2;                 // tiles i with i % 2 == grp (= TMEM buffer)
     const int quarter = warp & 3;            // TMEM lanes this warp may read
     const int m = quarter * 32 + lane;       // key row of the tile = TMEM lane
-    const int wstride = (a.RG * a.H_i + 4 * kMaxRG + 3) & ~3;
-    int* w_own = w_s + (warp - kEpiWarp0) * wstride;
-    int* wsum = w_own + a.RG * a.H_i;
-    const float floor_v = a.relu ? 0.f : -3.0e38f;   // max(d, floor) = ReLU or identity
-    int rlen[kMaxRG];
-    uint32_t umax[kMaxRG], uminv[kMaxRG];
-    int cur_r0 = -1, cur_n = 0;
-    for (int i = 0; i < n_local; ++i) {
-      const int buf = i & 1;
+    const int wstride = a.RG * a.H_i + kMaxRG;
+    int2* wc = wc_s + ew * wstride;          // (w_h, bits of M - bias_h) per (row, head)
+    int* wsum = reinterpret_cast<int*>(wc + a.RG * a.H_i);
+    const float floor_v = a.relu ? kMagic : -3.0e38f;   // ReLU folded into the magic offset
+    int rlen0 = 0, rlen1 = 0, rlen2 = 0, rlen3 = 0;
+    for (int i = grp; i < n_local; i += 2) {
       if (tile_step(a, prefix, t_begin + i, ti)) {
-        for (int jr = 0; jr < cur_n; ++jr) row_minmax_flush(a.rows + cur_r0 + jr, umax[jr], uminv[jr]);
         __syncwarp();
-        for (int q = lane; q < ti.nrows * a.H_i; q += 32) w_own[q] = a.w_idx[(int64_t)ti.r0 * a.H_i + q];
+        for (int q = lane; q < ti.nrows * a.H_i; q += 32) {
+          const int w = a.w_idx[(int64_t)ti.r0 * a.H_i + q];
+          int bias = 0;
+          if (BIASED) {
+            const int4* qv = reinterpret_cast<const int4*>(a.q_idx + ((int64_t)ti.r0 * a.H_i + q) * D_I);
+            for (int j = 0; j < D_I / 16; ++j) {
+              const int4 x = __ldg(qv + j);
+              bias = __dp4a(x.x, 0x01010101, bias);
+              bias = __dp4a(x.y, 0x01010101, bias);
+              bias = __dp4a(x.z, 0x01010101, bias);
+              bias = __dp4a(x.w, 0x01010101, bias);
+            }
+            bias *= 1152;
+          }
+          wc[q] = make_int2(w, __float_as_int((float)(12582912 - bias)));
+        }
         __syncwarp();
         if (lane < ti.nrows) {
           uint32_t sacc = 0;
-          for (int h = 0; h < a.H_i; ++h) sacc += (uint32_t)w_own[lane * a.H_i + h];
+          for (int h = 0; h < a.H_i; ++h) sacc += (uint32_t)wc[lane * a.H_i + h].x;
           wsum[lane] = (int)sacc;
         }
         __syncwarp();
-#pragma unroll
-        for (int jr = 0; jr < kMaxRG; ++jr) {
-          rlen[jr] = jr < ti.nrows ? a.row_len[ti.r0 + jr] : 0;
-          umax[jr] = 0u;
-          uminv[jr] = 0u;
-        }
-        cur_r0 = ti.r0;
-        cur_n = ti.nrows;
+        rlen0 = ti.nrows > 0 ? a.row_len[ti.r0] : 0;
+        rlen1 = ti.nrows > 1 ? a.row_len[ti.r0 + 1] : 0;
+        rlen2 = ti.nrows > 2 ? a.row_len[ti.r0 + 2] : 0;
+        rlen3 = ti.nrows > 3 ? a.row_len[ti.r0 + 3] : 0;
       }
-      if (!wait_bar_warp(bar_accfull + 8 * buf, (i >> 1) & 1, abort_flag, a.status)) break;
+      if (!wait_bar_warp(bar_accfull + 8 * grp, (i >> 1) & 1, abort_flag, a.status)) break;
       tc_fence_after();
       const int t = ti.j * kTile + m;
 #pragma unroll
       for (int jr = 0; jr < kMaxRG; ++jr) {
         if (jr >= ti.nrows) break;
         uint32_t acc = 0;  // wraps mod 2^32; the true score fits int32
-        const int4* wr = reinterpret_cast<const int4*>(w_own + jr * a.H_i);
+        const int4* wr = reinterpret_cast<const int4*>(wc + jr * a.H_i);
         for (int h0 = 0; h0 < a.H_i; h0 += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * N_max + jr * a.H_i + h0, v);
+          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + grp * N_max + jr * a.H_i + h0, v);
 #pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
-            const int4 w4 = wr[(h0 >> 2) + h4];
-            const int wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float d = fmaxf(__uint_as_float(v[4 * h4 + e]), floor_v);
-              // d is an exact integer with |d| < 2^22: adding 1.5 * 2^23 puts it in
-              // the low mantissa bits (bit pattern 0x4B400000 + d).
-              acc += (uint32_t)__float_as_int(d + 12582912.f) * (uint32_t)wv[e];
-            }
+          for (int h2 = 0; h2 < 16; ++h2) {
+            const int4 p = wr[(h0 >> 1) + h2];     // (w, c) of heads h0+2*h2 and h0+2*h2+1
+            // x = max(d - bias + M, floor) = M + ReLU(q.k): an exact integer in
+            // [2^23, 2^24), so its bit pattern is 0x4B400000 + score part.
+            const float x0 = fmaxf(__uint_as_float(v[2 * h2]) + __int_as_float(p.y), floor_v);
+            const float x1 = fmaxf(__uint_as_float(v[2 * h2 + 1]) + __int_as_float(p.w), floor_v);
+            acc += (uint32_t)__float_as_int(x0) * (uint32_t)p.x;
+            acc += (uint32_t)__float_as_int(x1) * (uint32_t)p.z;
           }
         }
         acc -= 0x4B400000u * (uint32_t)wsum[jr];
-        if (t < rlen[jr]) {
-          a.scores[(int64_t)(ti.r0 + jr) * a.L_max + t] = (int32_t)acc;
-          const uint32_t u = acc ^ 0x80000000u;
-          umax[jr] = max(umax[jr], u);
-          uminv[jr] = max(uminv[jr], ~u);
-        }
+        const int rl = jr == 0 ? rlen0 : (jr == 1 ? rlen1 : (jr == 2 ? rlen2 : rlen3));
+        if (t < rl) a.scores[(int64_t)(ti.r0 + jr) * a.L_max + t] = (int32_t)acc;
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_accempty + 8 * buf);
+      if (lane == 0) mbar_arrive(bar_accempty + 8 * grp);
     }
-    for (int jr = 0; jr < cur_n; ++jr) row_minmax_flush(a.rows + cur_r0 + jr, umax[jr], uminv[jr]);
   }
 
   tc_fence_before();
@@ -520,19 +551,24 @@ bool indexer_tc_supported(const dsa_problem& p) {
   return (p.D_i == 64 || p.D_i == 128) && (p.H_i == 32 || p.H_i == 64 || p.H_i == 128);
 }
 
-template <int D_I, int S>
+template <int D_I, int S, bool BIASED>
 cudaError_t launch_tc(const TcArgs& a, int sms, size_t smem, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<D_I, S>,
+  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<D_I, S, BIASED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(indexer_tc_kernel<D_I, S>, dim3(sms), dim3(kThreads), smem, st, a);
+  return launch_pdl(indexer_tc_kernel<D_I, S, BIASED>, dim3(sms), dim3(kThreads), smem, st, a);
+}
+
+template <int D_I, bool BIASED>
+cudaError_t launch_tc_s(const TcArgs& a, int sms, size_t smem, cudaStream_t st) {
+  return a.stages == 8 ? launch_tc<D_I, 8, BIASED>(a, sms, smem, st)
+                       : launch_tc<D_I, 4, BIASED>(a, sms, smem, st);
 }
 
 cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                               cudaStream_t st) {
   TcArgs a;
   a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
-  a.rows = reinterpret_cast<RowState*>(ws + pl.off_state);
   a.zero = reinterpret_cast<uint4*>(ws);
   a.n_zero = (int)(pl.zero_end / 16);
   a.q_idx = p.q_idx; a.w_idx = p.w_idx; a.k_idx = p.k_idx;
@@ -550,8 +586,7 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   const uint32_t b_bytes = (uint32_t)N_max * D_i * 2u;
   const uint32_t stage_bytes = 128u * D_i;
   const uint32_t prefix_bytes = ((uint32_t)(p.B + 1) * 4u + 15u) / 16u * 16u;
-  const uint32_t wstride = (uint32_t)((RG * p.H_i + 4 * kMaxRG + 3) & ~3);
-  const uint32_t w_bytes = kEpiWarps * wstride * 4u;
+  const uint32_t w_bytes = kEpiWarps * (uint32_t)(RG * p.H_i + kMaxRG) * 8u;
   const uint32_t budget = 227u * 1024u - 1024u;   // minus the alignment slack
   auto total_for = [&](int s) {
     return a_bytes + b_bytes + s * stage_bytes + w_bytes + (2 * s + 6) * 8 + 16 + prefix_bytes;
@@ -570,11 +605,15 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   a.tmem_cols = cols;
   size_t smem = (size_t)a.off_prefix + prefix_bytes + 1024;
   if (smem < 120u * 1024u) smem = 120u * 1024u;   // one CTA per SM: TMEM is never contended
+  // The biased conversion needs every partial sum |sum_d q_d (k_d + 1152)| < 2^24.
+  const int64_t qk = p.qk_abs_max > 0 ? p.qk_abs_max : 128;
+  const bool biased = (int64_t)D_i * qk * 1279 < (int64_t(1) << 24);
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (D_i == 128) return S == 8 ? launch_tc<128, 8>(a, sms, smem, st) : launch_tc<128, 4>(a, sms, smem, st);
-  return S == 8 ? launch_tc<64, 8>(a, sms, smem, st) : launch_tc<64, 4>(a, sms, smem, st);
+  if (D_i == 128)
+    return biased ? launch_tc_s<128, true>(a, sms, smem, st) : launch_tc_s<128, false>(a, sms, smem, st);
+  return biased ? launch_tc_s<64, true>(a, sms, smem, st) : launch_tc_s<64, false>(a, sms, smem, st);
 }
 
 }  // namespace dsa

@@ -3,27 +3,25 @@
 // "ds4 glm53-m3ultra" (page 1) replaced a selection that sorted and merged
 // ever larger candidate lists with parallel scans that narrow the candidates,
 // a sort of the small surviving list, and the original exact algorithm for the
-// ambiguous cases -- keeping the same positions in the same order.  Here:
+// ambiguous cases -- keeping the same positions in the same order.  Here, with
+// u = s ^ 0x80000000 the order-preserving unsigned key of a score s:
 //
-//   minmax   the range [umin, umax] of the row's order-preserving keys
-//            u = s ^ 0x80000000 (merged by the indexer's epilogue in a decode
-//            step; a separate scan for dsa_topk); the bits above the highest
-//            bit where umin and umax differ are common to every key, so only
-//            D = bitlen(umin ^ umax) bits remain to be searched.
-//   pass x3  radix search for the k-th largest key T, 11 bits per pass, over
-//            the positions still in the candidate bin (shared-memory histogram,
-//            global merge, the row's last CTA picks the bin).  Rows finish in
-//            ceil(D / 11) passes; the remaining launches return at once.
-//   compact  every u > T is selected (unordered slots); positions with u == T
-//            are counted per chunk.
-//   ties     the r = k - #{u > T} lowest-index positions with u == T: each
-//            chunk takes its share from the exclusive prefix of the counts and
-//            writes its ties in index order (the exact fallback: it never
-//            depends on how many positions tie).
-//   rank     the <= k survivors are ordered by (score desc, position asc): the
-//            rank of a survivor is the number of survivors whose 64-bit key
-//            (u << 32 | ~position) is larger; keys are unique, so ranks are a
-//            permutation and the order is exact.
+//   hist    one scan: a histogram of a monotone 13-bit code of each score (the
+//           top bits of its float32 value: sign, exponent, 4 mantissa bits).
+//           The row's last CTA finds the threshold bucket b*: fewer than k
+//           positions lie above it, at least k at or above it.
+//   select  every position whose code is >= b* joins the row's survivor list
+//           (unordered slots): the n_above sure winners plus the bucket's
+//           candidates, a few thousand positions at long context.
+//   rank    each survivor's rank is the number of survivors with a larger
+//           64-bit key (u << 32 | ~position).  Keys are unique, so the ranks
+//           are a permutation and sort by (score desc, position asc); a
+//           survivor with rank < k is selected and written at idx[rank].
+//   exact fallback  when the survivor list would exceed kCapFast (heavy ties
+//           at the threshold), one CTA per row resolves it exactly: the
+//           candidates' key range, radix passes to the exact k-th key T,
+//           every key > T plus the lowest-index positions with key == T in
+//           index order, then a bitonic sort.
 // A row with row_len <= k selects every position; an empty row selects none.
 // Nothing here waits on another CTA: cross-CTA steps use the last-arriving
 // CTA of a row (fence + counter), and kernel boundaries.
@@ -33,8 +31,12 @@ namespace dsa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRankPerBlock = 32;                    // survivors ranked per CTA
-constexpr int kRankLanes = kThreads / kRankPerBlock; // threads per survivor
+constexpr int kRankThreads = 512;
+constexpr int kRankPerBlock = 64;                          // survivors ranked per CTA
+constexpr int kRankLanes = kRankThreads / kRankPerBlock;   // threads per survivor
+constexpr int kRadixBits = 11;
+
+enum Mode : uint32_t { kFast = 0, kAll = 1, kEmpty = 2, kExact = 3 };
 
 struct TopkArgs {
   const int32_t* scores;
@@ -42,9 +44,8 @@ struct TopkArgs {
   int32_t* idx;
   int32_t* nsel;
   RowState* state;
-  uint32_t* hist;      // [R, kHistBins]
-  uint32_t* tiecnt;    // [R, nchunk]
-  uint64_t* sel;       // [R, k]
+  uint32_t* hist;      // [R, kBuckets]
+  uint64_t* surv;      // [R, kCapFast] survivor keys
   int64_t L_max;
   int k, chunk;
 };
@@ -55,42 +56,24 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-__device__ __forceinline__ uint64_t sel_key(uint32_t u, int t) {
+// Monotone (non-decreasing) 13-bit code of a score: its float32 value mapped
+// to an order-preserving unsigned key, top 13 bits.
+__device__ __forceinline__ uint32_t bucket_of(int32_t s) {
+  const uint32_t b = __float_as_uint(__int2float_rn(s));
+  const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return o >> (32 - kBucketBits);
+}
+
+__device__ __forceinline__ uint64_t surv_key(uint32_t u, int t) {
   return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - (uint32_t)t);
+}
+__device__ __forceinline__ int key_pos(uint64_t key) {
+  return (int)(0xFFFFFFFFu - (uint32_t)key);
 }
 
 template <typename T>
 __device__ __forceinline__ T ld_volatile(const T* p) {
   return *reinterpret_cast<const volatile T*>(p);
-}
-
-// Block-wide max of two values (all threads get the result).
-__device__ void block_max2(uint32_t& a, uint32_t& b) {
-  __shared__ uint32_t sa[kThreads / 32], sb[kThreads / 32];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
-    b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
-  }
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  if (lane == 0) { sa[w] = a; sb[w] = b; }
-  __syncthreads();
-  a = 0; b = 0;
-  for (int i = 0; i < kThreads / 32; ++i) { a = max(a, sa[i]); b = max(b, sb[i]); }
-  __syncthreads();
-}
-
-__device__ uint32_t block_sum(uint32_t v) {
-  __shared__ uint32_t s[kThreads / 32];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  if (lane == 0) s[w] = v;
-  __syncthreads();
-  uint32_t t = 0;
-  for (int i = 0; i < kThreads / 32; ++i) t += s[i];
-  __syncthreads();
-  return t;
 }
 
 // True in every thread of the CTA that arrives last at counter `c`.
@@ -104,236 +87,289 @@ __device__ bool last_arrival(uint32_t* c, uint32_t expected) {
   return is_last != 0;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_minmax_kernel(TopkArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int r = blockIdx.y;
-  const int len = a.row_len[r];
-  const int start = blockIdx.x * a.chunk;
-  const int end = min(start + a.chunk, len);
-  const int32_t* s = a.scores + (int64_t)r * a.L_max;
-  uint32_t umax = 0, uminv = 0;
-  for (int t = start + threadIdx.x; t < end; t += kThreads) {
-    const uint32_t u = ordered_key(s[t]);
-    umax = max(umax, u);
-    uminv = max(uminv, ~u);
-  }
-  row_minmax_flush(a.state + r, umax, uminv);
-}
-
-__global__ void __launch_bounds__(kThreads) topk_pass_kernel(TopkArgs a, int phase) {
-  pdl_wait();
-  pdl_trigger();
-  const int r = blockIdx.y;
-  RowState* st = a.state + r;
-  const int len = a.row_len[r];
-  uint32_t mode, shift, prefix, k_rem;
-  if (phase == kPhasePass0) {
-    // Initial state from the row's key range; every CTA derives the same.
-    mode = len <= 0 ? 2u : (len <= a.k ? 1u : 0u);
-    const uint32_t hi = st->umax, lo = ~st->uminv;
-    const uint32_t diff = hi ^ lo;
-    shift = (mode == 0 && diff) ? 32u - __clz(diff) : 0u;
-    prefix = shift >= 32 ? 0u : (hi >> shift);
-    k_rem = (uint32_t)a.k;
-    if (mode != 0 || shift == 0) {
-      // Nothing to search: the last CTA records the state for the next kernels.
-      if (!last_arrival(&st->arrive[phase], gridDim.x) || threadIdx.x != 0) return;
-      st->mode = mode;
-      st->shift = 0;
-      st->prefix = prefix;
-      st->k_rem = k_rem;
-      st->n_take = (uint32_t)min(a.k, max(len, 0));
-      return;
-    }
-  } else {
-    mode = st->mode;
-    if (mode != 0) return;
-    shift = st->shift;
-    if (shift == 0) return;                     // threshold already exact
-    prefix = st->prefix;
-    k_rem = st->k_rem;                          // read before the last CTA rewrites it
-  }
-  const uint32_t bits = min(shift, (uint32_t)kHistBits);
-  const uint32_t ns = shift - bits;
-  const uint32_t mask = (1u << bits) - 1u;
-  const int nbins = 1 << bits;
-
-  __shared__ uint32_t h[kHistBins];
-  for (int i = threadIdx.x; i < nbins; i += kThreads) h[i] = 0;
-  __syncthreads();
-
-  const int start = blockIdx.x * a.chunk;
-  const int end = min(start + a.chunk, len);
-  const int32_t* s = a.scores + (int64_t)r * a.L_max;
-  for (int t = start + threadIdx.x; t < end; t += kThreads) {
-    const uint32_t u = ordered_key(s[t]);
-    if ((static_cast<uint64_t>(u) >> shift) == prefix) atomicAdd(&h[(u >> ns) & mask], 1u);
-  }
-  __syncthreads();
-  uint32_t* gh = a.hist + (size_t)r * kHistBins;
-  for (int i = threadIdx.x; i < nbins; i += kThreads)
-    if (h[i]) atomicAdd(&gh[i], h[i]);
-
-  if (!last_arrival(&st->arrive[phase], gridDim.x)) return;
-
-  // Last CTA of the row: find the bin holding the k_rem-th largest candidate.
-  // Thread i owns bins [i*per, (i+1)*per) counted from the top.
-  constexpr int per = kHistBins / kThreads;
-  uint32_t local[per];
-  uint32_t sum = 0;
-#pragma unroll
-  for (int j = 0; j < per; ++j) {
-    const int bin = nbins - 1 - (threadIdx.x * per + j);
-    local[j] = bin >= 0 ? ld_volatile(&gh[bin]) : 0u;
-    sum += local[j];
-  }
-  // exclusive scan of `sum` over threads (top bins first)
-  __shared__ uint32_t wsum[kThreads / 32];
-  uint32_t v = sum;
+// Block-wide inclusive scan in thread order (NT threads).
+template <int NT>
+__device__ uint32_t block_scan_incl(uint32_t v, uint32_t* warp_tot) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += n;
   }
-  if (lane == 31) wsum[w] = v;
+  if (lane == 31) warp_tot[w] = v;
   __syncthreads();
-  uint32_t above = v - sum;
-  for (int i = 0; i < w; ++i) above += wsum[i];
-  if (above < k_rem && above + sum >= k_rem) {
-    uint32_t acc = above;
+  uint32_t base = 0;
+  for (int i = 0; i < w; ++i) base += warp_tot[i];
+  __syncthreads();
+  return base + v;
+}
+
+template <int NT>
+__device__ uint32_t block_reduce_max(uint32_t v, uint32_t* tmp) {
 #pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) tmp[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint32_t r = 0;
+  for (int i = 0; i < NT / 32; ++i) r = max(r, tmp[i]);
+  __syncthreads();
+  return r;
+}
+
+// Finds, in a histogram of `nbins` counts held in shared memory, the bin b
+// (counting from the top) with above(b) < need <= above(b) + h[b].  Writes
+// (b, above) to out[0..1].  Every thread of the NT-thread block takes part.
+template <int NT>
+__device__ void find_crossing(const uint32_t* h, int nbins, uint32_t need, uint32_t* out) {
+  __shared__ uint32_t wt[NT / 32];
+  const int per = (nbins + NT - 1) / NT;
+  const int top = nbins - 1 - threadIdx.x * per;   // this thread owns bins top, top-1, ...
+  uint32_t sum = 0;
+  for (int j = 0; j < per; ++j)
+    if (top - j >= 0) sum += h[top - j];
+  const uint32_t incl = block_scan_incl<NT>(sum, wt);
+  uint32_t above = incl - sum;
+  if (above < need && incl >= need) {
     for (int j = 0; j < per; ++j) {
-      const int bin = nbins - 1 - (threadIdx.x * per + j);
-      if (acc + local[j] >= k_rem) {
-        st->k_rem = k_rem - acc;
-        st->prefix = (prefix << bits) | (uint32_t)bin;
-        st->shift = ns;
-        if (phase == kPhasePass0) {
-          st->mode = 0;
-          st->n_take = (uint32_t)a.k;
-        }
+      const uint32_t c = h[top - j];
+      if (above + c >= need) {
+        out[0] = (uint32_t)(top - j);
+        out[1] = above;
         break;
       }
-      acc += local[j];
+      above += c;
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < nbins; i += kThreads) gh[i] = 0;  // ready for the next pass
 }
 
-__global__ void __launch_bounds__(kThreads) topk_compact_kernel(TopkArgs a) {
+// ------------------------------------------------------------------ hist
+
+__global__ void __launch_bounds__(kThreads) topk_hist_kernel(TopkArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ uint32_t h[kBuckets];
+  __shared__ uint32_t res[2];
+  const int r = blockIdx.y;
+  const int len = a.row_len[r];
+  for (int i = threadIdx.x; i < kBuckets; i += kThreads) h[i] = 0;
+  __syncthreads();
+  const int start = blockIdx.x * a.chunk;
+  const int end = min(start + a.chunk, len);
+  const int32_t* s = a.scores + (int64_t)r * a.L_max;
+  if (len > a.k)
+    for (int t = start + threadIdx.x; t < end; t += kThreads) atomicAdd(&h[bucket_of(s[t])], 1u);
+  __syncthreads();
+  uint32_t* gh = a.hist + (size_t)r * kBuckets;
+  if (len > a.k)
+    for (int i = threadIdx.x; i < kBuckets; i += kThreads)
+      if (h[i]) atomicAdd(&gh[i], h[i]);
+
+  RowState* st = a.state + r;
+  if (!last_arrival(&st->arrive[0], gridDim.x)) return;
+  // Last CTA of the row: pick the mode and the threshold bucket.
+  if (len <= a.k) {
+    if (threadIdx.x == 0) {
+      st->mode = len <= 0 ? kEmpty : kAll;
+      st->n_take = (uint32_t)max(len, 0);
+      st->bstar = 0;
+    }
+    return;
+  }
+  for (int i = threadIdx.x; i < kBuckets; i += kThreads) h[i] = ld_volatile(&gh[i]);
+  __syncthreads();
+  find_crossing<kThreads>(h, kBuckets, (uint32_t)a.k, res);
+  if (threadIdx.x == 0) {
+    const uint32_t b = res[0], above = res[1];
+    st->bstar = b;
+    st->n_above = above;
+    st->cand = h[b];
+    st->n_take = (uint32_t)a.k;
+    st->mode = (above + h[b] <= (uint32_t)kCapFast) ? kFast : kExact;
+  }
+}
+
+// ------------------------------------------------------------------ select
+
+__global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkArgs a) {
   pdl_wait();
   pdl_trigger();
   const int r = blockIdx.y;
   RowState* st = a.state + r;
   const uint32_t mode = st->mode;
-  if (mode == 2) return;
-  const uint32_t T = st->prefix;       // exact threshold key (shift is 0 here)
+  if (mode != kFast && mode != kAll) return;
+  const uint32_t bstar = st->bstar;
   const int len = a.row_len[r];
   const int start = blockIdx.x * a.chunk;
   const int end = min(start + a.chunk, len);
   const int32_t* s = a.scores + (int64_t)r * a.L_max;
-  uint64_t* sel = a.sel + (size_t)r * a.k;
+  uint64_t* surv = a.surv + (size_t)r * kCapFast;
   const int lane = threadIdx.x & 31;
-  uint32_t ties = 0;
   for (int base = start; base < end; base += kThreads) {
     const int t = base + threadIdx.x;
-    uint32_t u = 0;
+    int32_t v = 0;
     bool take = false;
     if (t < end) {
-      u = ordered_key(s[t]);
-      if (mode == 1 || u > T) take = true;
-      else if (u == T) ++ties;
+      v = s[t];
+      take = mode == kAll || bucket_of(v) >= bstar;
     }
     const uint32_t m = __ballot_sync(0xffffffffu, take);
     if (m) {
       uint32_t slot = 0;
-      if (lane == 0) slot = atomicAdd(&st->n_gt, (uint32_t)__popc(m));
+      if (lane == 0) slot = atomicAdd(&st->n_union, (uint32_t)__popc(m));
       slot = __shfl_sync(0xffffffffu, slot, 0);
-      if (take) sel[slot + __popc(m & lanemask_lt())] = sel_key(u, t);
+      if (take) surv[slot + __popc(m & lanemask_lt())] = surv_key(ordered_key(v), t);
     }
-  }
-  if (mode == 0) {
-    const uint32_t tot = block_sum(ties);
-    if (threadIdx.x == 0) a.tiecnt[(size_t)r * gridDim.x + blockIdx.x] = tot;
   }
 }
 
-__global__ void __launch_bounds__(kThreads) topk_ties_kernel(TopkArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int r = blockIdx.y;
-  RowState* st = a.state + r;
-  if (st->mode != 0) return;
-  const uint32_t k_rem = st->k_rem;
-  const uint32_t* cnt = a.tiecnt + (size_t)r * gridDim.x;
-  if (k_rem == 0 || cnt[blockIdx.x] == 0) return;
-  uint32_t mine = 0;
-  for (int c = threadIdx.x; c < (int)blockIdx.x; c += kThreads) mine += cnt[c];
-  const uint32_t before = block_sum(mine);
-  if (before >= k_rem) return;
-  const uint32_t take = min(k_rem - before, cnt[blockIdx.x]);
-  const uint32_t T = st->prefix;
+// ------------------------------------------------------------------ exact fallback
+
+// One CTA resolves a row exactly: the candidates are the positions in bucket
+// b*; k_rem = k - n_above of them are taken.
+__device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys) {
+  constexpr int NT = kRankThreads;
+  __shared__ uint32_t h[1 << kRadixBits];
+  __shared__ uint32_t tmp[NT / 32];
+  __shared__ uint32_t res[2];
+  __shared__ uint32_t n_list;
   const int len = a.row_len[r];
-  const int start = blockIdx.x * a.chunk;
-  const int end = min(start + a.chunk, len);
   const int32_t* s = a.scores + (int64_t)r * a.L_max;
-  uint64_t* out = a.sel + (size_t)r * a.k + (a.k - k_rem) + before;
+  const uint32_t bstar = st->bstar;
+  uint32_t k_rem = (uint32_t)a.k - st->n_above;
 
-  __shared__ uint32_t wcnt[kThreads / 32];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  uint32_t done = 0;
-  for (int base = start; base < end && done < take; base += kThreads) {
-    const int t = base + threadIdx.x;
-    const bool tie = t < end && ordered_key(s[t]) == T;
-    const uint32_t m = __ballot_sync(0xffffffffu, tie);
-    if (lane == 0) wcnt[w] = __popc(m);
-    __syncthreads();
-    uint32_t pos = done + __popc(m & lanemask_lt());
-    uint32_t total = 0;
-    for (int i = 0; i < kThreads / 32; ++i) {
-      if (i < w) pos += wcnt[i];
-      total += wcnt[i];
+  // Key range of the candidates.
+  uint32_t umax = 0, uminv = 0;
+  for (int t = threadIdx.x; t < len; t += NT) {
+    const int32_t v = s[t];
+    if (bucket_of(v) == bstar) {
+      const uint32_t u = ordered_key(v);
+      umax = max(umax, u);
+      uminv = max(uminv, ~u);
     }
-    if (tie && pos < take) out[pos] = sel_key(T, t);
-    done += total;
+  }
+  umax = block_reduce_max<NT>(umax, tmp);
+  uminv = block_reduce_max<NT>(uminv, tmp);
+  const uint32_t diff = umax ^ ~uminv;
+  uint32_t shift = diff ? 32u - __clz(diff) : 0u;
+  uint32_t prefix = shift >= 32 ? 0u : (umax >> shift);
+
+  // Radix passes down to the exact k_rem-th largest candidate key T.
+  while (shift > 0) {
+    const uint32_t bits = min(shift, (uint32_t)kRadixBits);
+    const uint32_t ns = shift - bits;
+    const int nb = 1 << bits;
+    for (int i = threadIdx.x; i < nb; i += NT) h[i] = 0;
+    __syncthreads();
+    for (int t = threadIdx.x; t < len; t += NT) {
+      const int32_t v = s[t];
+      const uint32_t u = ordered_key(v);
+      if (bucket_of(v) == bstar && (static_cast<uint64_t>(u) >> shift) == prefix)
+        atomicAdd(&h[(u >> ns) & (uint32_t)(nb - 1)], 1u);
+    }
+    __syncthreads();
+    find_crossing<NT>(h, nb, k_rem, res);
+    k_rem -= res[1];
+    prefix = (prefix << bits) | res[0];
+    shift = ns;
     __syncthreads();
   }
+  const uint32_t T = prefix;
+
+  // Winners: every key > T (unordered), then the k_rem lowest-index ties in
+  // index order.  n_gt = k - k_rem keys are strictly greater than T.
+  if (threadIdx.x == 0) n_list = 0;
+  __syncthreads();
+  const uint32_t n_gt = (uint32_t)a.k - k_rem;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint32_t ties_done = 0;
+  for (int base = 0; base < len; base += NT) {
+    const int t = base + threadIdx.x;
+    uint32_t u = 0;
+    bool gt = false, tie = false;
+    if (t < len) {
+      u = ordered_key(s[t]);
+      gt = u > T;
+      tie = u == T;
+    }
+    if (gt) keys[atomicAdd(&n_list, 1u)] = surv_key(u, t);
+    const uint32_t m = __ballot_sync(0xffffffffu, tie);
+    if (lane == 0) tmp[w] = __popc(m);
+    __syncthreads();
+    uint32_t pos = ties_done + __popc(m & lanemask_lt()), tot = 0;
+    for (int i = 0; i < NT / 32; ++i) {
+      if (i < w) pos += tmp[i];
+      tot += tmp[i];
+    }
+    if (tie && pos < k_rem) keys[n_gt + pos] = surv_key(u, t);
+    ties_done += tot;
+    __syncthreads();
+  }
+
+  // Bitonic sort of the k winners, descending (zero keys pad to a power of two).
+  int n = 1;
+  while (n < a.k) n <<= 1;
+  for (int i = a.k + threadIdx.x; i < n; i += NT) keys[i] = 0;
+  __syncthreads();
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (n >> 1); i += NT) {
+        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+        const uint64_t x = keys[lo], y = keys[hi];
+        const bool desc = (lo & size) == 0;
+        if (desc ? (x < y) : (x > y)) {
+          keys[lo] = y;
+          keys[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  int32_t* idx = a.idx + (size_t)r * a.k;
+  for (int j = threadIdx.x; j < a.k; j += NT) idx[j] = key_pos(keys[j]);
 }
 
-__global__ void __launch_bounds__(kThreads) topk_rank_kernel(TopkArgs a) {
+// ------------------------------------------------------------------ rank
+
+__global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(TopkArgs a) {
   pdl_wait();
   pdl_trigger();
+  extern __shared__ uint64_t keys[];   // [max(kCapFast, pow2 >= k)]
   const int r = blockIdx.y;
   RowState* st = a.state + r;
-  const int n = st->mode == 2 ? 0 : (int)st->n_take;
-  extern __shared__ uint64_t keys[];
-  const uint64_t* sel = a.sel + (size_t)r * a.k;
-  for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = sel[i];
-  __syncthreads();
+  const uint32_t mode = st->mode;
+  const int n_take = mode == kEmpty ? 0 : (int)st->n_take;
   int32_t* idx = a.idx + (size_t)r * a.k;
-  const int e = blockIdx.x * kRankPerBlock + threadIdx.x / kRankLanes;
-  const int part = threadIdx.x % kRankLanes;
-  const uint64_t key = e < n ? keys[e] : 0;
-  uint32_t rank = 0;
-  if (e < n)
-    for (int j = part; j < n; j += kRankLanes) rank += keys[j] > key;
-#pragma unroll
-  for (int o = kRankLanes / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-  if (e < n && part == 0) idx[rank] = (int32_t)(0xFFFFFFFFu - (uint32_t)key);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.nsel) a.nsel[r] = n_take;
+  if (mode == kExact) {
+    if (blockIdx.x == 0) exact_row(a, st, r, keys);
+    return;
+  }
   if (threadIdx.x < kRankPerBlock) {
     const int p = blockIdx.x * kRankPerBlock + threadIdx.x;
-    if (p >= n && p < a.k) idx[p] = -1;
+    if (p >= n_take && p < a.k) idx[p] = -1;
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0 && a.nsel) a.nsel[r] = n;
+  if (mode == kEmpty) return;
+  const int U = (int)st->n_union;
+  if (blockIdx.x * kRankPerBlock >= U) return;
+  const uint64_t* surv = a.surv + (size_t)r * kCapFast;
+  for (int i = threadIdx.x; i < U; i += kRankThreads) keys[i] = surv[i];
+  __syncthreads();
+  const int e = blockIdx.x * kRankPerBlock + threadIdx.x / kRankLanes;
+  const int part = threadIdx.x % kRankLanes;
+  const uint64_t key = e < U ? keys[e] : ~0ull;
+  uint32_t rank = 0;
+  if (e < U)
+    for (int j = part; j < U; j += kRankLanes) rank += keys[j] > key;
+#pragma unroll
+  for (int o = kRankLanes / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+  if (e < U && part == 0 && rank < (uint32_t)n_take) idx[rank] = key_pos(key);
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* scores,
-                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st, bool minmax_done) {
+                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st) {
   TopkArgs a;
   a.scores = scores;
   a.row_len = p.row_len;
@@ -341,24 +377,22 @@ cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* sco
   a.nsel = nsel;
   a.state = reinterpret_cast<RowState*>(ws + pl.off_state);
   a.hist = reinterpret_cast<uint32_t*>(ws + pl.off_hist);
-  a.tiecnt = reinterpret_cast<uint32_t*>(ws + pl.off_tiecnt);
-  a.sel = reinterpret_cast<uint64_t*>(ws + pl.off_sel);
+  a.surv = reinterpret_cast<uint64_t*>(ws + pl.off_surv);
   a.L_max = pl.L_max;
   a.k = pl.k;
   a.chunk = pl.chunk;
   const dim3 grid(pl.nchunk, pl.R), block(kThreads);
   cudaError_t e;
-  if (!minmax_done && (e = launch_pdl(topk_minmax_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
-  if ((e = launch_pdl(topk_pass_kernel, grid, block, 0, st, a, (int)kPhasePass0)) != cudaSuccess) return e;
-  if ((e = launch_pdl(topk_pass_kernel, grid, block, 0, st, a, (int)kPhasePass1)) != cudaSuccess) return e;
-  if ((e = launch_pdl(topk_pass_kernel, grid, block, 0, st, a, (int)kPhasePass2)) != cudaSuccess) return e;
-  if ((e = launch_pdl(topk_compact_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
-  if ((e = launch_pdl(topk_ties_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
-  const size_t smem = (size_t)pl.k * 8;
+  if ((e = launch_pdl(topk_hist_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
+  if ((e = launch_pdl(topk_select_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
+  int n = 1;
+  while (n < pl.k) n <<= 1;
+  const size_t smem = (size_t)(n > kCapFast ? n : kCapFast) * 8;
   e = cudaFuncSetAttribute(topk_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const dim3 rgrid((pl.k + kRankPerBlock - 1) / kRankPerBlock, pl.R);
-  return launch_pdl(topk_rank_kernel, rgrid, block, smem, st, a);
+  const int span = (pl.k > kCapFast ? pl.k : kCapFast);
+  const dim3 rgrid((span + kRankPerBlock - 1) / kRankPerBlock, pl.R);
+  return launch_pdl(topk_rank_kernel, rgrid, dim3(kRankThreads), smem, st, a);
 }
 
 }  // namespace dsa

@@ -8,11 +8,19 @@ ATOL = 1e-2      # max |out - oracle| on the bf16 attention output
 RTOL_L2 = 5e-3   # ||out - oracle||_2 / ||oracle||_2
 
 
-def run_ops(x, indexer="auto", relu=True, lse=True, scores_fill=-7):
-    """dsa_index_scores -> dsa_topk -> dsa_sparse_attn; returns host arrays."""
+def value_bound(x):
+    """The caller's declared bound on |q_idx| and |k_idx| (from the data)."""
+    return int(max(np.abs(x.q_idx.astype(np.int32)).max(initial=0),
+                   np.abs(x.k_idx.astype(np.int32)).max(initial=0), 1))
+
+
+def run_ops(x, indexer="auto", relu=True, lse=True, scores_fill=-7, qk="data"):
+    """dsa_index_scores -> dsa_topk -> dsa_sparse_attn; returns host arrays.
+    qk: declared |q|,|k| bound ("data" = the inputs' own maximum, 0 = int8 range)."""
     import torch
     import dsa_sparse_attention_03_gb300 as dsa
-    prob, t = dsa.upload_inputs(x, indexer=indexer, relu=relu)
+    qk = value_bound(x) if qk == "data" else qk
+    prob, t = dsa.upload_inputs(x, indexer=indexer, relu=relu, qk_abs_max=qk)
     ws = dsa.alloc_workspace(prob)
     ws.fill_(0xAB)  # the library must not rely on a clean workspace
     dev = ws.device
@@ -31,10 +39,11 @@ def run_ops(x, indexer="auto", relu=True, lse=True, scores_fill=-7):
                 lse=None if lse_t is None else lse_t.cpu().numpy(), status=status)
 
 
-def run_step(x, indexer="auto"):
+def run_step(x, indexer="auto", qk="data"):
     import torch
     import dsa_sparse_attention_03_gb300 as dsa
-    prob, t = dsa.upload_inputs(x, indexer=indexer)
+    qk = value_bound(x) if qk == "data" else qk
+    prob, t = dsa.upload_inputs(x, indexer=indexer, qk_abs_max=qk)
     ws = dsa.alloc_workspace(prob)
     ws.fill_(0x5A)
     idx = torch.full((x.R, x.k), -5, dtype=torch.int32, device=ws.device)

@@ -7,14 +7,15 @@ import pytest
 
 import dsa_inputs as gen
 import oracle
+from gpu_harness import value_bound
 
 pytestmark = pytest.mark.gpu
 
 
-def _scores(x, indexer, relu=True):
+def _scores(x, indexer, relu=True, qk=0):
     import torch
     import dsa_sparse_attention_03_gb300 as dsa
-    prob, t = dsa.upload_inputs(x, indexer=indexer, relu=relu)
+    prob, t = dsa.upload_inputs(x, indexer=indexer, relu=relu, qk_abs_max=qk)
     assert dsa.indexer_kind(prob) == indexer
     ws = dsa.alloc_workspace(prob)
     s = torch.full((x.R, max(1, x.L_max)), -99, dtype=torch.int32, device="cuda")
@@ -24,7 +25,13 @@ def _scores(x, indexer, relu=True):
 
 
 def _check(x, rows=None, relu=True, vs_dp4a=True):
-    got, status = _scores(x, "tc", relu)
+    """Both conversions: exact (no declared bound) and biased (declared bound)."""
+    for qk in (0, value_bound(x)):
+        _check_one(x, rows, relu, vs_dp4a, qk)
+
+
+def _check_one(x, rows, relu, vs_dp4a, qk):
+    got, status = _scores(x, "tc", relu, qk)
     assert status == 0
     rows = list(range(x.R)) if rows is None else rows
     ref = oracle.indexer_scores(x.q_idx, x.w_idx, x.k_idx, x.offsets, x.row_offsets, x.row_len,
@@ -90,3 +97,14 @@ def test_tc_head_and_dim_variants(H_i, D_i):
                         row_len=[2500, 2400, 2000, 900, 700], H_i=H_i, D_i=D_i, H_q=16,
                         D_k=64, D_v=64, k=256, softmax_scale=0.125)
     _check(x)
+
+
+def test_tc_biased_path_at_its_exactness_limit():
+    # D_i * max|q| * 1279 < 2^24 allows a declared bound of 102 at D_i = 128:
+    # values at +-102 keep every partial sum of the biased MMA exact in fp32.
+    x = gen.l64k(L=2000)
+    rng = np.random.default_rng(7)
+    x.q_idx[:] = rng.choice(np.array([-102, 102, 101, -1], np.int8), x.q_idx.shape)
+    x.k_idx[:] = rng.choice(np.array([-102, 102, 0], np.int8), x.k_idx.shape)
+    x.w_idx[:] = 1
+    _check_one(x, None, True, True, 102)
