@@ -213,6 +213,7 @@ def bench_ours(args):
     step_bytes = n_layers * (L_LONG * x0.D_i + x0.k * x0.D_k * 2 + x0.H_q * x0.D_k * 2)
     step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
 
+    stages = bench_stages(layers, ws, idx, nsel, out, stream) if not args.no_extras else None
     e2e = bench_e2e(args, layers, ws, idx, nsel, out, stream, device) if not args.no_extras else None
 
     # The L = 65536 single-layer point of the metric: 12 independent layers
@@ -242,6 +243,7 @@ def bench_ours(args):
                      "peak_source": peak_src, "traffic": None,
                      "algorithmic_bytes_per_launch": idx_bytes,
                      "avg_launch_us": round(idx_avg_ms * 1000, 3)},
+        "stages_us_per_layer": stages,
         "secondary": sec,
         "e2e": e2e,
         "gpu_launches": args.steps * n_layers * kernels_per_step(),
@@ -251,6 +253,40 @@ def bench_ours(args):
     if not args.no_cpu_baseline and not args.no_extras and world == 1:
         res["cpu_baseline"] = cpu_baseline(layers_for_cpu=[x for x, _, _ in layers[:4]])
     return res
+
+
+def bench_stages(layers, ws, idx, nsel, out, stream):
+    """Per-stage device time (CUDA events around each public call, all layers,
+    no graph): where a decode step's time goes."""
+    import torch
+    import dsa_sparse_attention_03_gb300 as dsa
+    sp = stream.cuda_stream
+    x0 = layers[0][0]
+    scores = torch.empty((1, x0.L_max), dtype=torch.int32, device=ws.device)
+    names = ("index_scores", "topk", "sparse_attn")
+    tot = {n: 0.0 for n in names}
+    reps = 5
+    with torch.cuda.stream(stream):
+        for rep in range(reps + 1):
+            evs = []
+            for i, (_, prob, _) in enumerate(layers):
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                e[0].record(stream)
+                dsa.dsa_index_scores(prob, scores, ws, stream=sp)
+                e[1].record(stream)
+                dsa.dsa_topk(prob, scores, idx[i], nsel[i], ws, stream=sp)
+                e[2].record(stream)
+                dsa.dsa_sparse_attn(prob, idx[i], nsel[i], out[i], None, ws, stream=sp)
+                e[3].record(stream)
+                evs.append(e)
+            torch.cuda.synchronize()
+            if rep == 0:
+                continue
+            for e in evs:
+                for j, n in enumerate(names):
+                    tot[n] += e[j].elapsed_time(e[j + 1]) * 1000.0
+    n = reps * len(layers)
+    return {k: round(v / n, 3) for k, v in tot.items()}
 
 
 def bench_e2e(args, layers, ws, idx, nsel, out, stream, device):

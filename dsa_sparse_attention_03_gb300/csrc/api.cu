@@ -193,7 +193,7 @@ dsa_status dsa_topk(const dsa_problem* p, const int32_t* scores, int32_t* idx, i
   cudaError_t e = cudaMemsetAsync(ws, 0, pl.zero_end, st);
   if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
   if (p->R == 0) return DSA_OK;
-  e = launch_topk(*p, pl, scores, idx, nsel, static_cast<char*>(ws), st);
+  e = launch_topk(*p, pl, scores, idx, nsel, static_cast<char*>(ws), st, false);
   if (e != cudaSuccess) return cuda_fail(e, "top-k");
   return DSA_OK;
 }
@@ -235,7 +235,7 @@ dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* nsel, ui
   }
   int32_t* scores = reinterpret_cast<int32_t*>(w + pl.off_scores);
   if ((s = run_indexer(*p, pl, scores, w, st)) != DSA_OK) return s;
-  e = launch_topk(*p, pl, scores, idx, nsel, w, st);
+  e = launch_topk(*p, pl, scores, idx, nsel, w, st, true);
   if (e != cudaSuccess) return cuda_fail(e, "top-k");
   e = launch_attention(*p, pl, idx, nsel, out, nullptr, w, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention");

@@ -9,7 +9,7 @@
 
 namespace dsa {
 
-constexpr int kBucketBits = 13;               // float-like score code of the top-k histogram
+constexpr int kBucketBits = 11;               // linear bins over the row's key range
 constexpr int kBuckets = 1 << kBucketBits;
 constexpr int kCapFast = 4096;                // survivors ranked directly (else exact fallback)
 constexpr int kAttnRows = 64;                 // selected positions per attention CTA
@@ -20,13 +20,14 @@ constexpr int kMaxK = 4096;
 // Per-row state of the top-k, in the workspace.  Zeroed (with the histograms)
 // by the indexer of a decode step, or by dsa_topk before its first kernel.
 struct RowState {
+  uint32_t umax;       // max ordered key of the row (merged by the indexer)
+  uint32_t uminv;      // max of ~key, i.e. ~min
   uint32_t bstar;      // threshold bucket
   uint32_t n_above;    // positions in buckets above it (all selected)
   uint32_t cand;       // positions in the threshold bucket
   uint32_t n_union;    // survivor slot counter
   uint32_t mode;       // fast / take all / empty / exact fallback
   uint32_t n_take;     // min(k, row_len)
-  uint32_t pad[2];
   uint32_t arrive[8];  // last-CTA counters
 };
 static_assert(sizeof(RowState) == 64, "RowState is 64 bytes");
@@ -77,6 +78,20 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 
+// Per-row running max of the ordered keys and of their complements (= ~min),
+// merged into RowState.umax / uminv by the indexers' epilogues (one warp).
+__device__ __forceinline__ void row_minmax_flush(RowState* st, uint32_t umax, uint32_t uminv) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, o));
+    uminv = max(uminv, __shfl_xor_sync(0xffffffffu, uminv, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    if (umax) atomicMax(&st->umax, umax);
+    if (uminv) atomicMax(&st->uminv, uminv);
+  }
+}
+
 // Launchers (one per translation unit).  Each returns the launch error.
 // Both indexers also clear the workspace's status word, top-k state and
 // histograms ([0, Plan::zero_end)), so a decode step needs no separate memset.
@@ -85,8 +100,9 @@ cudaError_t launch_indexer_dp4a(const dsa_problem& p, const Plan& pl, int32_t* s
 cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                               cudaStream_t st);
 bool indexer_tc_supported(const dsa_problem& p);
+// minmax_done: the indexer already merged each row's key range into RowState.
 cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* scores,
-                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st);
+                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st, bool minmax_done);
 cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t* idx,
                              const int32_t* nsel, uint16_t* out, float* lse, char* ws,
                              cudaStream_t st);

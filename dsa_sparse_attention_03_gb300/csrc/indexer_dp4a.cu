@@ -29,6 +29,7 @@ struct IdxArgs {
   int total_tiles_bound;
   uint4* zero;          // workspace words to clear (status + top-k state)
   int n_zero;
+  RowState* rows;       // per-row key range for the top-k
 };
 
 // Exclusive prefix of per-request tile counts into tile_start[0..B], by one block.
@@ -151,11 +152,18 @@ __global__ void __launch_bounds__(kThreads) indexer_dp4a_kernel(IdxArgs a) {
         for (int kk = 0; kk < KPT; ++kk) acc[kk] += wh * (a.relu ? max(d[kk], 0) : d[kk]);
       }
       int32_t* out = a.scores + (int64_t)r * a.L_max;
+      uint32_t umax = 0, uminv = 0;
 #pragma unroll
       for (int kk = 0; kk < KPT; ++kk) {
         const int t = t0 + kk * kThreads + threadIdx.x;
-        if (t < len) out[t] = acc[kk];
+        if (t < len) {
+          out[t] = acc[kk];
+          const uint32_t u = ordered_key(acc[kk]);
+          umax = max(umax, u);
+          uminv = max(uminv, ~u);
+        }
       }
+      row_minmax_flush(a.rows + r, umax, uminv);
     }
   }
   pdl_trigger();
@@ -171,6 +179,7 @@ cudaError_t launch(const dsa_problem& p, const Plan& pl, int32_t* scores, char* 
   a.relu = (p.flags & DSA_FLAG_NO_RELU) ? 0 : 1;
   a.zero = reinterpret_cast<uint4*>(ws);
   a.n_zero = (int)(pl.zero_end / 16);
+  a.rows = reinterpret_cast<RowState*>(ws + pl.off_state);
   const int64_t bound = p.L_total / TILE + p.B;
   a.total_tiles_bound = (int)bound;
   const size_t ts_bytes = ((size_t)(p.B + 1) * 4 + 15) / 16 * 16;

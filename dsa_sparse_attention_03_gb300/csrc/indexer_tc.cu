@@ -32,7 +32,7 @@
 //   warps 10-17   epilogue, two groups of four taking alternate tiles (one per
 //                 TMEM accumulator buffer): tcgen05.ld of each key's head dots
 //                 (one TMEM lane per key), ReLU, weight, head sum in exact
-//                 int32, store.
+//                 int32, store, and the row's running key range for the top-k.
 // A and the accumulator are double-buffered, so conversion, MMA and epilogue
 // of consecutive tiles overlap the key stream.  Every mbarrier wait is bounded
 // (a few seconds of %globaltimer); on expiry the CTA sets DSA_DEVICE_TIMEOUT,
@@ -64,6 +64,7 @@ struct TcArgs {
   const int32_t* row_len;
   int32_t* scores;
   uint32_t* status;
+  RowState* rows;       // per-row key range for the top-k
   int64_t L_max;
   int B, H_i, D_i, RG, stages, relu;
   uint32_t off_b, off_stage, off_w, off_bar, off_misc, off_prefix;   // shared-memory map
@@ -473,8 +474,17 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
     int* wsum = reinterpret_cast<int*>(wc + a.RG * a.H_i);
     const float floor_v = a.relu ? kMagic : -3.0e38f;   // ReLU folded into the magic offset
     int rlen0 = 0, rlen1 = 0, rlen2 = 0, rlen3 = 0;
+    uint32_t mx0 = 0, mx1 = 0, mx2 = 0, mx3 = 0, mn0 = 0, mn1 = 0, mn2 = 0, mn3 = 0;  // max u, max ~u
+    int cur_r0 = -1, cur_n = 0;
     for (int i = grp; i < n_local; i += 2) {
       if (tile_step(a, prefix, t_begin + i, ti)) {
+        if (cur_n > 0) row_minmax_flush(a.rows + cur_r0, mx0, mn0);
+        if (cur_n > 1) row_minmax_flush(a.rows + cur_r0 + 1, mx1, mn1);
+        if (cur_n > 2) row_minmax_flush(a.rows + cur_r0 + 2, mx2, mn2);
+        if (cur_n > 3) row_minmax_flush(a.rows + cur_r0 + 3, mx3, mn3);
+        mx0 = mx1 = mx2 = mx3 = mn0 = mn1 = mn2 = mn3 = 0;
+        cur_r0 = ti.r0;
+        cur_n = ti.nrows;
         __syncwarp();
         for (int q = lane; q < ti.nrows * a.H_i; q += 32) {
           const int w = a.w_idx[(int64_t)ti.r0 * a.H_i + q];
@@ -528,12 +538,23 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
         }
         acc -= 0x4B400000u * (uint32_t)wsum[jr];
         const int rl = jr == 0 ? rlen0 : (jr == 1 ? rlen1 : (jr == 2 ? rlen2 : rlen3));
-        if (t < rl) a.scores[(int64_t)(ti.r0 + jr) * a.L_max + t] = (int32_t)acc;
+        if (t < rl) {
+          a.scores[(int64_t)(ti.r0 + jr) * a.L_max + t] = (int32_t)acc;
+          const uint32_t u = acc ^ 0x80000000u;
+          if (jr == 0) { mx0 = max(mx0, u); mn0 = max(mn0, ~u); }
+          if (jr == 1) { mx1 = max(mx1, u); mn1 = max(mn1, ~u); }
+          if (jr == 2) { mx2 = max(mx2, u); mn2 = max(mn2, ~u); }
+          if (jr == 3) { mx3 = max(mx3, u); mn3 = max(mn3, ~u); }
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_accempty + 8 * grp);
     }
+    if (cur_n > 0) row_minmax_flush(a.rows + cur_r0, mx0, mn0);
+    if (cur_n > 1) row_minmax_flush(a.rows + cur_r0 + 1, mx1, mn1);
+    if (cur_n > 2) row_minmax_flush(a.rows + cur_r0 + 2, mx2, mn2);
+    if (cur_n > 3) row_minmax_flush(a.rows + cur_r0 + 3, mx3, mn3);
   }
 
   tc_fence_before();
@@ -569,6 +590,7 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
                               cudaStream_t st) {
   TcArgs a;
   a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
+  a.rows = reinterpret_cast<RowState*>(ws + pl.off_state);
   a.zero = reinterpret_cast<uint4*>(ws);
   a.n_zero = (int)(pl.zero_end / 16);
   a.q_idx = p.q_idx; a.w_idx = p.w_idx; a.k_idx = p.k_idx;

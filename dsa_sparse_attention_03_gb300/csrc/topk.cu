@@ -6,10 +6,12 @@
 // ambiguous cases -- keeping the same positions in the same order.  Here, with
 // u = s ^ 0x80000000 the order-preserving unsigned key of a score s:
 //
-//   hist    one scan: a histogram of a monotone 13-bit code of each score (the
-//           top bits of its float32 value: sign, exponent, 4 mantissa bits).
-//           The row's last CTA finds the threshold bucket b*: fewer than k
-//           positions lie above it, at least k at or above it.
+//   hist    one scan: a histogram of 2048 equal-width bins over the row's key
+//           range [umin, umax] (merged by the indexer, or by a min/max scan
+//           for a standalone call); bin(u) = (u - umin) >> shift with the
+//           smallest shift that fits.  The row's last CTA finds the threshold
+//           bin b*: fewer than k positions lie above it, at least k at or
+//           above it.
 //   select  every position whose code is >= b* joins the row's survivor list
 //           (unordered slots): the n_above sure winners plus the bucket's
 //           candidates, a few thousand positions at long context.
@@ -56,12 +58,41 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Monotone (non-decreasing) 13-bit code of a score: its float32 value mapped
-// to an order-preserving unsigned key, top 13 bits.
-__device__ __forceinline__ uint32_t bucket_of(int32_t s) {
-  const uint32_t b = __float_as_uint(__int2float_rn(s));
-  const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return o >> (32 - kBucketBits);
+// Equal-width bins over the row's key range: bin(u) = (u - umin) >> shift,
+// monotone in u and below kBuckets.
+struct Bins {
+  uint32_t umin, shift;
+  __device__ __forceinline__ explicit Bins(const RowState* st) {
+    const uint32_t hi = st->umax, lo = ~st->uminv;
+    const uint32_t range = hi >= lo ? hi - lo : 0u;
+    const int bl = range ? 32 - __clz(range) : 0;
+    umin = lo;
+    shift = (uint32_t)max(0, bl - kBucketBits);
+  }
+  // (The clamp only guards memory: every key of the row lies in [umin, umax].)
+  __device__ __forceinline__ uint32_t operator()(uint32_t u) const {
+    return min((u - umin) >> shift, (uint32_t)(kBuckets - 1));
+  }
+};
+
+// Visits s[t] for t in [begin, end) with `t += NT` striding, eight loads in
+// flight per thread; f(value, t) is called in increasing t for each thread.
+template <int NT, typename F>
+__device__ __forceinline__ void scan_row(const int32_t* s, int begin, int end, F f) {
+  constexpr int U = 8;
+  for (int base = begin + (int)threadIdx.x; base < end; base += U * NT) {
+    int32_t v[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int t = base + j * NT;
+      v[j] = t < end ? s[t] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int t = base + j * NT;
+      if (t < end) f(v[j], t);
+    }
+  }
 }
 
 __device__ __forceinline__ uint64_t surv_key(uint32_t u, int t) {
@@ -143,6 +174,38 @@ __device__ void find_crossing(const uint32_t* h, int nbins, uint32_t need, uint3
   __syncthreads();
 }
 
+// ------------------------------------------------------------------ minmax
+
+// Standalone dsa_topk only: the row's key range (a decode step merges it in
+// the indexer's epilogue).
+__global__ void __launch_bounds__(kThreads) topk_minmax_kernel(TopkArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.y;
+  const int len = a.row_len[r];
+  const int start = blockIdx.x * a.chunk;
+  const int end = min(start + a.chunk, len);
+  uint32_t umax = 0, uminv = 0;
+  scan_row<kThreads>(a.scores + (int64_t)r * a.L_max, start, end, [&](int32_t v, int) {
+    const uint32_t u = ordered_key(v);
+    umax = max(umax, u);
+    uminv = max(uminv, ~u);
+  });
+  __shared__ uint32_t smax[kThreads / 32], sminv[kThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, o));
+    uminv = max(uminv, __shfl_xor_sync(0xffffffffu, uminv, o));
+  }
+  if ((threadIdx.x & 31) == 0) { smax[threadIdx.x >> 5] = umax; sminv[threadIdx.x >> 5] = uminv; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < kThreads / 32; ++i) { umax = max(umax, smax[i]); uminv = max(uminv, sminv[i]); }
+    if (umax) atomicMax(&a.state[r].umax, umax);
+    if (uminv) atomicMax(&a.state[r].uminv, uminv);
+  }
+}
+
 // ------------------------------------------------------------------ hist
 
 __global__ void __launch_bounds__(kThreads) topk_hist_kernel(TopkArgs a) {
@@ -156,16 +219,17 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(TopkArgs a) {
   __syncthreads();
   const int start = blockIdx.x * a.chunk;
   const int end = min(start + a.chunk, len);
-  const int32_t* s = a.scores + (int64_t)r * a.L_max;
+  RowState* st = a.state + r;
+  const Bins bin(st);
   if (len > a.k)
-    for (int t = start + threadIdx.x; t < end; t += kThreads) atomicAdd(&h[bucket_of(s[t])], 1u);
+    scan_row<kThreads>(a.scores + (int64_t)r * a.L_max, start, end,
+                       [&](int32_t v, int) { atomicAdd(&h[bin(ordered_key(v))], 1u); });
   __syncthreads();
   uint32_t* gh = a.hist + (size_t)r * kBuckets;
   if (len > a.k)
     for (int i = threadIdx.x; i < kBuckets; i += kThreads)
       if (h[i]) atomicAdd(&gh[i], h[i]);
 
-  RowState* st = a.state + r;
   if (!last_arrival(&st->arrive[0], gridDim.x)) return;
   // Last CTA of the row: pick the mode and the threshold bucket.
   if (len <= a.k) {
@@ -199,6 +263,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkArgs a) {
   const uint32_t mode = st->mode;
   if (mode != kFast && mode != kAll) return;
   const uint32_t bstar = st->bstar;
+  const Bins bin(st);
   const int len = a.row_len[r];
   const int start = blockIdx.x * a.chunk;
   const int end = min(start + a.chunk, len);
@@ -211,7 +276,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkArgs a) {
     bool take = false;
     if (t < end) {
       v = s[t];
-      take = mode == kAll || bucket_of(v) >= bstar;
+      take = mode == kAll || bin(ordered_key(v)) >= bstar;
     }
     const uint32_t m = __ballot_sync(0xffffffffu, take);
     if (m) {
@@ -236,18 +301,18 @@ __device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys
   const int len = a.row_len[r];
   const int32_t* s = a.scores + (int64_t)r * a.L_max;
   const uint32_t bstar = st->bstar;
+  const Bins bin(st);
   uint32_t k_rem = (uint32_t)a.k - st->n_above;
 
   // Key range of the candidates.
   uint32_t umax = 0, uminv = 0;
-  for (int t = threadIdx.x; t < len; t += NT) {
-    const int32_t v = s[t];
-    if (bucket_of(v) == bstar) {
-      const uint32_t u = ordered_key(v);
+  scan_row<NT>(s, 0, len, [&](int32_t v, int) {
+    const uint32_t u = ordered_key(v);
+    if (bin(u) == bstar) {
       umax = max(umax, u);
       uminv = max(uminv, ~u);
     }
-  }
+  });
   umax = block_reduce_max<NT>(umax, tmp);
   uminv = block_reduce_max<NT>(uminv, tmp);
   const uint32_t diff = umax ^ ~uminv;
@@ -261,12 +326,11 @@ __device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys
     const int nb = 1 << bits;
     for (int i = threadIdx.x; i < nb; i += NT) h[i] = 0;
     __syncthreads();
-    for (int t = threadIdx.x; t < len; t += NT) {
-      const int32_t v = s[t];
+    scan_row<NT>(s, 0, len, [&](int32_t v, int) {
       const uint32_t u = ordered_key(v);
-      if (bucket_of(v) == bstar && (static_cast<uint64_t>(u) >> shift) == prefix)
+      if (bin(u) == bstar && (static_cast<uint64_t>(u) >> shift) == prefix)
         atomicAdd(&h[(u >> ns) & (uint32_t)(nb - 1)], 1u);
-    }
+    });
     __syncthreads();
     find_crossing<NT>(h, nb, k_rem, res);
     k_rem -= res[1];
@@ -283,27 +347,32 @@ __device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys
   const uint32_t n_gt = (uint32_t)a.k - k_rem;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t ties_done = 0;
-  for (int base = 0; base < len; base += NT) {
-    const int t = base + threadIdx.x;
-    uint32_t u = 0;
-    bool gt = false, tie = false;
-    if (t < len) {
-      u = ordered_key(s[t]);
-      gt = u > T;
-      tie = u == T;
+  for (int base0 = 0; base0 < len; base0 += 8 * NT) {
+    int32_t vv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = base0 + j * NT + threadIdx.x;
+      vv[j] = t < len ? s[t] : 0;
     }
-    if (gt) keys[atomicAdd(&n_list, 1u)] = surv_key(u, t);
-    const uint32_t m = __ballot_sync(0xffffffffu, tie);
-    if (lane == 0) tmp[w] = __popc(m);
-    __syncthreads();
-    uint32_t pos = ties_done + __popc(m & lanemask_lt()), tot = 0;
-    for (int i = 0; i < NT / 32; ++i) {
-      if (i < w) pos += tmp[i];
-      tot += tmp[i];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = base0 + j * NT + threadIdx.x;
+      const uint32_t u = ordered_key(vv[j]);
+      const bool gt = t < len && u > T;
+      const bool tie = t < len && u == T;
+      if (gt) keys[atomicAdd(&n_list, 1u)] = surv_key(u, t);
+      const uint32_t m = __ballot_sync(0xffffffffu, tie);
+      if (lane == 0) tmp[w] = __popc(m);
+      __syncthreads();
+      uint32_t pos = ties_done + __popc(m & lanemask_lt()), tot = 0;
+      for (int i = 0; i < NT / 32; ++i) {
+        if (i < w) pos += tmp[i];
+        tot += tmp[i];
+      }
+      if (tie && pos < k_rem) keys[n_gt + pos] = surv_key(u, t);
+      ties_done += tot;
+      __syncthreads();
     }
-    if (tie && pos < k_rem) keys[n_gt + pos] = surv_key(u, t);
-    ties_done += tot;
-    __syncthreads();
   }
 
   // Bitonic sort of the k winners, descending (zero keys pad to a power of two).
@@ -369,7 +438,7 @@ __global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(TopkArgs a) {
 }  // namespace
 
 cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* scores,
-                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st) {
+                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st, bool minmax_done) {
   TopkArgs a;
   a.scores = scores;
   a.row_len = p.row_len;
@@ -383,6 +452,7 @@ cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* sco
   a.chunk = pl.chunk;
   const dim3 grid(pl.nchunk, pl.R), block(kThreads);
   cudaError_t e;
+  if (!minmax_done && (e = launch_pdl(topk_minmax_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
   if ((e = launch_pdl(topk_hist_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
   if ((e = launch_pdl(topk_select_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
   int n = 1;
