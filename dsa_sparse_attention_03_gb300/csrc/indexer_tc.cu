@@ -26,15 +26,15 @@
 //                 also allocates / frees TMEM.
 //   warp 1        MMA issuer (one thread): D[tmem] = A . B^T, K/16 MMAs per
 //                 tile, tcgen05.commit to the accumulator barrier.
-//   warps 2-9     converters: int8 tile -> fp16 A tile in the canonical K-major
+//   warps 2-5     converters: int8 tile -> fp16 A tile in the canonical K-major
 //                 128-byte-swizzled layout; queries -> fp16 B when the row
 //                 group changes.
-//   warps 10-17   epilogue, two groups of four taking alternate tiles (one per
+//   warps 6-13    epilogue, two groups of four taking alternate tiles (one per
 //                 TMEM accumulator buffer): tcgen05.ld of each key's head dots
 //                 (one TMEM lane per key), ReLU, weight, head sum in exact
 //                 int32, store, and the row's running key range for the top-k.
-// A and the accumulator are double-buffered, so conversion, MMA and epilogue
-// of consecutive tiles overlap the key stream.  Every mbarrier wait is bounded
+// A is double-buffered and the accumulator 4-deep in TMEM (2-deep at N = 256),
+// so conversion, MMA and epilogue of consecutive tiles overlap the key stream.  Every mbarrier wait is bounded
 // (a few seconds of %globaltimer); on expiry the CTA sets DSA_DEVICE_TIMEOUT,
 // the other roles stop at their next wait, in-flight copies and MMAs are
 // drained (bounded) and TMEM is freed before exit.
@@ -45,7 +45,7 @@
 namespace dsa {
 namespace {
 
-constexpr int kConvWarps = 8;
+constexpr int kConvWarps = 4;
 constexpr int kEpiWarps = 8;                 // two groups of four
 constexpr int kThreads = (2 + kConvWarps + kEpiWarps) * 32;
 constexpr int kTile = 128;                   // keys per tile (MMA M)
@@ -53,6 +53,7 @@ constexpr uint64_t kWaitNs = 4000000000ull;
 constexpr int kConvWarp0 = 2;
 constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
 constexpr int kMaxRG = 4;                    // query rows per MMA group (N <= 256)
+constexpr int kMaxAcc = 4;                   // TMEM accumulator buffers at most
 constexpr float kMagic = 12582912.f;         // 1.5 * 2^23
 
 struct TcArgs {
@@ -67,6 +68,7 @@ struct TcArgs {
   RowState* rows;       // per-row key range for the top-k
   int64_t L_max;
   int B, H_i, D_i, RG, stages, relu;
+  int nacc;             // TMEM accumulator buffers (4, or 2 when N = 256)
   uint32_t off_b, off_stage, off_w, off_bar, off_misc, off_prefix;   // shared-memory map
   uint32_t tmem_cols;
   uint4* zero;          // workspace words to clear (status + top-k state)
@@ -183,6 +185,11 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (no wait).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
@@ -193,7 +200,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
         "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // Four int8 -> four fp16 (two half2 words).  XOR 0x80 biases each byte to
@@ -302,17 +308,45 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   const uint32_t bar_full = cvta_smem(bars);                // S
   const uint32_t bar_empty = bar_full + 8 * S;              // S
   const uint32_t bar_afull = bar_empty + 8 * S;             // 2
-  const uint32_t bar_accfull = bar_afull + 16;              // 2
-  const uint32_t bar_accempty = bar_accfull + 16;           // 2
+  const uint32_t bar_accfull = bar_afull + 16;              // kMaxAcc
+  const uint32_t bar_accempty = bar_accfull + 8 * kMaxAcc;  // kMaxAcc
+  const int NACC = a.nacc;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // Set-up that touches no global memory overlaps the previous kernel's tail.
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) {
+        mbar_init(bar_full + 8 * s, 1);
+        mbar_init(bar_empty + 8 * s, kConvWarps);
+      }
+      for (int i = 0; i < 2; ++i) mbar_init(bar_afull + 8 * i, kConvWarps);
+      for (int i = 0; i < kMaxAcc; ++i) {
+        mbar_init(bar_accfull + 8 * i, 1);
+        mbar_init(bar_accempty + 8 * i, kEpiWarps / 2);
+      }
+      misc[1] = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     cvta_smem((const void*)misc)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
 
   pdl_wait();
   pdl_trigger();
   for (int i = blockIdx.x * kThreads + tid; i < a.n_zero; i += gridDim.x * kThreads)
     a.zero[i] = make_uint4(0, 0, 0, 0);
 
-  // Per-request tile counts: groups_b * tiles_b; exclusive prefix by one warp.
+  TileInfo ti;
+  ti.lo = ti.hi = 0;
+  int issued = 0;   // producer (warp 0, lane 0): tiles whose copy has been issued
+  // Per-request tile counts: groups_b * tiles_b; exclusive prefix by one warp,
+  // which then issues the first key-tile copies before the block barrier.
   if (warp == 0) {
     int run = 0;
     for (int base = 0; base < a.B; base += 32) {
@@ -333,27 +367,20 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) prefix[a.B] = run;
-  }
-  if (tid == 32) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kConvWarps);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_afull + 8 * i, kConvWarps);
-      mbar_init(bar_accfull + 8 * i, 1);
-      mbar_init(bar_accempty + 8 * i, kEpiWarps / 2);
-    }
-    misc[1] = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 0) {
     __syncwarp();
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     cvta_smem((const void*)misc)),
-                 "r"(a.tmem_cols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (lane == 0) {
+      const int tot = prefix[a.B];
+      const int tb = (int)(((int64_t)blockIdx.x * tot) / gridDim.x);
+      const int te = (int)(((int64_t)(blockIdx.x + 1) * tot) / gridDim.x);
+      for (; issued < S && issued < te - tb; ++issued) {
+        tile_step(a, prefix, tb + issued, ti);
+        const int rows = min(kTile, ti.L_b - ti.j * kTile);
+        const uint32_t bytes = (uint32_t)rows * D_I;
+        mbar_arrive_tx(bar_full + 8 * issued, bytes);
+        tma_load_1d(cvta_smem(stage + issued * kStageBytes),
+                    a.k_idx + (ti.base + (int64_t)ti.j * kTile) * D_I, bytes, bar_full + 8 * issued);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -366,14 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   const int t_end = (int)(((int64_t)(blockIdx.x + 1) * total) / gridDim.x);
   const int n_local = t_end - t_begin;
   const int N_max = a.RG * a.H_i;
-  TileInfo ti;
-  ti.lo = ti.hi = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < n_local; ++i) {
+      for (int i = issued; i < n_local; ++i) {
         const int s = i % S;
         if (i >= S && !wait_bar(bar_empty + 8 * s, ((i / S) - 1) & 1, abort_flag, a.status)) break;
         tile_step(a, prefix, t_begin + i, ti);
@@ -394,29 +418,31 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int issued = 0;
+      issued = 0;
       const uint32_t b_base = cvta_smem(Bop);
       for (int i = 0; i < n_local; ++i) {
-        const int buf = i & 1;
+        const int abuf = i & 1, acc = i % NACC;
         tile_step(a, prefix, t_begin + i, ti);
         const uint32_t idesc = idesc_f16(kTile, ti.nrows * a.H_i);
-        if (i >= 2 && !wait_bar(bar_accempty + 8 * buf, ((i - 2) >> 1) & 1, abort_flag, a.status)) break;
-        if (!wait_bar(bar_afull + 8 * buf, (i >> 1) & 1, abort_flag, a.status)) break;
+        if (i >= NACC &&
+            !wait_bar(bar_accempty + 8 * acc, ((i / NACC) - 1) & 1, abort_flag, a.status))
+          break;
+        if (!wait_bar(bar_afull + 8 * abuf, (i >> 1) & 1, abort_flag, a.status)) break;
         tc_fence_after();
-        const uint32_t a_base = cvta_smem(A + buf * kABytes);
+        const uint32_t a_base = cvta_smem(A + abuf * kABytes);
 #pragma unroll
         for (int kk = 0; kk < D_I / 16; ++kk) {
           const uint32_t ka = a_base + (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
           const uint32_t kb = b_base + (kk >> 2) * (N_max * 128) + (kk & 3) * 32;
-          mma_f16(tmem + buf * N_max, smem_desc_sw128(ka), smem_desc_sw128(kb), idesc, kk > 0);
+          mma_f16(tmem + acc * N_max, smem_desc_sw128(ka), smem_desc_sw128(kb), idesc, kk > 0);
         }
-        mma_commit(bar_accfull + 8 * buf);
+        mma_commit(bar_accfull + 8 * acc);
         issued = i + 1;
       }
       // Drain: the last MMAs must finish before TMEM is freed.
-      for (int i = max(0, issued - 2); i < issued; ++i) {
+      for (int i = max(0, issued - NACC); i < issued; ++i) {
         const uint64_t t0 = globaltimer();
-        while (!mbar_try(bar_accfull + 8 * (i & 1), (i >> 1) & 1) && globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try(bar_accfull + 8 * (i % NACC), (i / NACC) & 1) && globaltimer() - t0 < kWaitNs) {
         }
       }
     }
@@ -432,11 +458,13 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
       const int s = i % S, buf = i & 1;
       const bool new_group = tile_step(a, prefix, t_begin + i, ti);
       if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status)) break;
-      if (i >= 2 && !wait_bar_warp(bar_accfull + 8 * buf, ((i - 2) >> 1) & 1, abort_flag, a.status)) break;
+      if (i >= 2 &&
+          !wait_bar_warp(bar_accfull + 8 * ((i - 2) % NACC), ((i - 2) / NACC) & 1, abort_flag, a.status))
+        break;
       if (new_group) {
         // B may be rewritten once every issued MMA has finished.
         if (i >= 1 &&
-            !wait_bar_warp(bar_accfull + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, a.status))
+            !wait_bar_warp(bar_accfull + 8 * ((i - 1) % NACC), ((i - 1) / NACC) & 1, abort_flag, a.status))
           break;
         const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
         const int nchunks = ti.nrows * a.H_i * CPR;
@@ -466,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - kEpiWarp0;         // 0..7
-    const int grp = ew >> 2;                 // tiles i with i % 2 == grp (= TMEM buffer)
+    const int grp = ew >> 2;                 // tiles i with i % 2 == grp
     const int quarter = warp & 3;            // TMEM lanes this warp may read
     const int m = quarter * 32 + lane;       // key row of the tile = TMEM lane
     const int wstride = a.RG * a.H_i + kMaxRG;
@@ -514,28 +542,45 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
         rlen2 = ti.nrows > 2 ? a.row_len[ti.r0 + 2] : 0;
         rlen3 = ti.nrows > 3 ? a.row_len[ti.r0 + 3] : 0;
       }
-      if (!wait_bar_warp(bar_accfull + 8 * grp, (i >> 1) & 1, abort_flag, a.status)) break;
+      const int accb = i % NACC;
+      if (!wait_bar_warp(bar_accfull + 8 * accb, (i / NACC) & 1, abort_flag, a.status)) break;
       tc_fence_after();
       const int t = ti.j * kTile + m;
+      const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + accb * N_max;
 #pragma unroll
       for (int jr = 0; jr < kMaxRG; ++jr) {
         if (jr >= ti.nrows) break;
-        uint32_t acc = 0;  // wraps mod 2^32; the true score fits int32
+        // Four independent sums (wrapping mod 2^32; the true score fits int32).
+        uint32_t acc4[4] = {0u, 0u, 0u, 0u};
         const int4* wr = reinterpret_cast<const int4*>(wc + jr * a.H_i);
-        for (int h0 = 0; h0 < a.H_i; h0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + grp * N_max + jr * a.H_i + h0, v);
+        for (int h0 = 0; h0 < a.H_i; h0 += 64) {
+          uint32_t va[32], vb[32];
+          const bool two = h0 + 32 < a.H_i;
+          tmem_ld32(trow + jr * a.H_i + h0, va);
+          if (two) tmem_ld32(trow + jr * a.H_i + h0 + 32, vb);
+          tmem_wait_ld();
 #pragma unroll
           for (int h2 = 0; h2 < 16; ++h2) {
             const int4 p = wr[(h0 >> 1) + h2];     // (w, c) of heads h0+2*h2 and h0+2*h2+1
             // x = max(d - bias + M, floor) = M + ReLU(q.k): an exact integer in
             // [2^23, 2^24), so its bit pattern is 0x4B400000 + score part.
-            const float x0 = fmaxf(__uint_as_float(v[2 * h2]) + __int_as_float(p.y), floor_v);
-            const float x1 = fmaxf(__uint_as_float(v[2 * h2 + 1]) + __int_as_float(p.w), floor_v);
-            acc += (uint32_t)__float_as_int(x0) * (uint32_t)p.x;
-            acc += (uint32_t)__float_as_int(x1) * (uint32_t)p.z;
+            const float x0 = fmaxf(__uint_as_float(va[2 * h2]) + __int_as_float(p.y), floor_v);
+            const float x1 = fmaxf(__uint_as_float(va[2 * h2 + 1]) + __int_as_float(p.w), floor_v);
+            acc4[(h2 & 1) * 2] += (uint32_t)__float_as_int(x0) * (uint32_t)p.x;
+            acc4[(h2 & 1) * 2 + 1] += (uint32_t)__float_as_int(x1) * (uint32_t)p.z;
+          }
+          if (two) {
+#pragma unroll
+            for (int h2 = 0; h2 < 16; ++h2) {
+              const int4 p = wr[(h0 >> 1) + 16 + h2];
+              const float x0 = fmaxf(__uint_as_float(vb[2 * h2]) + __int_as_float(p.y), floor_v);
+              const float x1 = fmaxf(__uint_as_float(vb[2 * h2 + 1]) + __int_as_float(p.w), floor_v);
+              acc4[(h2 & 1) * 2] += (uint32_t)__float_as_int(x0) * (uint32_t)p.x;
+              acc4[(h2 & 1) * 2 + 1] += (uint32_t)__float_as_int(x1) * (uint32_t)p.z;
+            }
           }
         }
+        uint32_t acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
         acc -= 0x4B400000u * (uint32_t)wsum[jr];
         const int rl = jr == 0 ? rlen0 : (jr == 1 ? rlen1 : (jr == 2 ? rlen2 : rlen3));
         if (t < rl) {
@@ -549,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_accempty + 8 * grp);
+      if (lane == 0) mbar_arrive(bar_accempty + 8 * accb);
     }
     if (cur_n > 0) row_minmax_flush(a.rows + cur_r0, mx0, mn0);
     if (cur_n > 1) row_minmax_flush(a.rows + cur_r0 + 1, mx1, mn1);
@@ -611,7 +656,8 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   const uint32_t w_bytes = kEpiWarps * (uint32_t)(RG * p.H_i + kMaxRG) * 8u;
   const uint32_t budget = 227u * 1024u - 1024u;   // minus the alignment slack
   auto total_for = [&](int s) {
-    return a_bytes + b_bytes + s * stage_bytes + w_bytes + (2 * s + 6) * 8 + 16 + prefix_bytes;
+    return a_bytes + b_bytes + s * stage_bytes + w_bytes + (2 * s + 2 + 2 * kMaxAcc) * 8 + 16 +
+           prefix_bytes;
   };
   const int S = total_for(8) <= budget ? 8 : 4;
   if (total_for(S) > budget) return cudaErrorInvalidConfiguration;
@@ -620,10 +666,11 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   a.off_stage = a.off_b + b_bytes;
   a.off_w = a.off_stage + S * stage_bytes;
   a.off_bar = a.off_w + w_bytes;
-  a.off_misc = a.off_bar + (2 * S + 6) * 8;
+  a.off_misc = a.off_bar + (2 * S + 2 + 2 * kMaxAcc) * 8;
   a.off_prefix = a.off_misc + 16;
+  a.nacc = N_max <= 128 ? 4 : 2;               // accumulators fill at most 512 TMEM columns
   uint32_t cols = 32;
-  while (cols < 2u * N_max) cols <<= 1;
+  while (cols < (uint32_t)(a.nacc * N_max)) cols <<= 1;
   a.tmem_cols = cols;
   size_t smem = (size_t)a.off_prefix + prefix_bytes + 1024;
   if (smem < 120u * 1024u) smem = 120u * 1024u;   // one CTA per SM: TMEM is never contended
