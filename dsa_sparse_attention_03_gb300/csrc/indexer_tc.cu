@@ -40,7 +40,10 @@
 // drained (bounded) and TMEM is freed before exit.
 #include "common.cuh"
 
+#include <cuda.h>
 #include <cuda_fp16.h>
+
+#include <cstring>
 
 namespace dsa {
 namespace {
@@ -54,6 +57,7 @@ constexpr int kConvWarp0 = 2;
 constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
 constexpr int kMaxRG = 4;                    // query rows per MMA group (N <= 256)
 constexpr int kMaxAcc = 4;                   // TMEM accumulator buffers at most
+constexpr int kMaxA = 4;                     // TMEM A buffers at most (TMEM-operand kernel)
 constexpr float kMagic = 12582912.f;         // 1.5 * 2^23
 
 struct TcArgs {
@@ -73,6 +77,9 @@ struct TcArgs {
   uint32_t tmem_cols;
   uint4* zero;          // workspace words to clear (status + top-k state)
   int n_zero;
+  int na;               // TMEM A buffers (TMEM-operand kernel)
+  uint32_t a_col0;      // first TMEM column of the A buffers
+  CUtensorMap tmap;     // k_idx as [L_total, 128] bytes, 128-byte swizzle
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -149,6 +156,15 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint3
       : "memory");
 }
 
+// 2-D tiled copy through the tensor map (box 128 x 128 bytes, 128-byte swizzle).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -180,6 +196,16 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
+// As mma_f16 with the A operand read from TMEM (row = lane, 2 fp16 per column).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -200,6 +226,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
         "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+      "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+      "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Four int8 -> four fp16 (two half2 words).  XOR 0x80 biases each byte to
@@ -611,6 +652,340 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// D_i = 128 with the A operand in TMEM.  Key tiles arrive through the tensor
+// map with the 128-byte swizzle, so a converter thread reads its own key row
+// without bank conflicts (16-byte unit j of row m sits at unit j ^ (m mod 8));
+// it writes the fp16 row into its TMEM lane with tcgen05.st, and the MMA takes
+// A from TMEM.  Shared memory then carries only the int8 tiles (TMA write +
+// one read) and the small B operand -- a third of the traffic of staging A in
+// shared memory.  Rings: S key stages, NA TMEM A buffers, NACC accumulators.
+// The MMA commits each tile twice: to the accumulator's barrier (epilogue) and
+// to the A buffer's barrier (converters may reuse it).
+template <int S, bool BIASED>
+__global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid_constant__ TcArgs a) {
+  constexpr int D_I = 128;
+  constexpr uint32_t kStageBytes = kTile * D_I;             // one int8 tile (16 KB)
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* stage = smem;                              // S x [128][128 B], swizzled
+  unsigned char* Bop = smem + a.off_b;                      // [2][N_max][128 B]
+  int2* wc_s = reinterpret_cast<int2*>(smem + a.off_w);     // per epilogue warp: (w, c) per head
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.off_bar);
+  volatile int* misc = reinterpret_cast<volatile int*>(smem + a.off_misc);  // [0] tmem, [1] abort
+  int* prefix = reinterpret_cast<int*>(smem + a.off_prefix);               // [B+1]
+
+  const int NA = a.na, NACC = a.nacc;
+  const uint32_t bar_full = cvta_smem(bars);                   // S
+  const uint32_t bar_empty = bar_full + 8 * S;                 // S
+  const uint32_t bar_afull = bar_empty + 8 * S;                // kMaxA
+  const uint32_t bar_afree = bar_afull + 8 * kMaxA;            // kMaxA
+  const uint32_t bar_accfull = bar_afree + 8 * kMaxA;          // kMaxAcc
+  const uint32_t bar_accempty = bar_accfull + 8 * kMaxAcc;     // kMaxAcc
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) {
+        mbar_init(bar_full + 8 * s, 1);
+        mbar_init(bar_empty + 8 * s, kConvWarps);
+      }
+      for (int i = 0; i < kMaxA; ++i) {
+        mbar_init(bar_afull + 8 * i, kConvWarps);
+        mbar_init(bar_afree + 8 * i, 1);
+      }
+      for (int i = 0; i < kMaxAcc; ++i) {
+        mbar_init(bar_accfull + 8 * i, 1);
+        mbar_init(bar_accempty + 8 * i, kEpiWarps / 2);
+      }
+      misc[1] = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tmap)) : "memory");
+    }
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     cvta_smem((const void*)misc)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+
+  pdl_wait();
+  pdl_trigger();
+  for (int i = blockIdx.x * kThreads + tid; i < a.n_zero; i += gridDim.x * kThreads)
+    a.zero[i] = make_uint4(0, 0, 0, 0);
+
+  TileInfo ti;
+  ti.lo = ti.hi = 0;
+  int issued = 0;
+  if (warp == 0) {
+    int run = 0;
+    for (int base = 0; base < a.B; base += 32) {
+      const int b = base + lane;
+      int v = 0;
+      if (b < a.B) {
+        const int L_b = a.offsets[b + 1] - a.offsets[b];
+        const int rows_b = a.row_offsets[b + 1] - a.row_offsets[b];
+        v = ((rows_b + a.RG - 1) / a.RG) * ((L_b + kTile - 1) / kTile);
+      }
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (b < a.B) prefix[b] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) prefix[a.B] = run;
+    __syncwarp();
+    if (lane == 0) {
+      const int tot = prefix[a.B];
+      const int tb = (int)(((int64_t)blockIdx.x * tot) / gridDim.x);
+      const int te = (int)(((int64_t)(blockIdx.x + 1) * tot) / gridDim.x);
+      for (; issued < S && issued < te - tb; ++issued) {
+        tile_step(a, prefix, tb + issued, ti);
+        mbar_arrive_tx(bar_full + 8 * issued, kStageBytes);
+        tma_load_2d(cvta_smem(stage + issued * kStageBytes), &a.tmap, 0,
+                    (int)(ti.base + (int64_t)ti.j * kTile), bar_full + 8 * issued);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = (uint32_t)misc[0];
+  volatile int* abort_flag = misc + 1;
+
+  const int total = prefix[a.B];
+  const int t_begin = (int)(((int64_t)blockIdx.x * total) / gridDim.x);
+  const int t_end = (int)(((int64_t)(blockIdx.x + 1) * total) / gridDim.x);
+  const int n_local = t_end - t_begin;
+  const int N_max = a.RG * a.H_i;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int i = issued; i < n_local; ++i) {
+        const int s = i % S;
+        if (i >= S && !wait_bar(bar_empty + 8 * s, ((i / S) - 1) & 1, abort_flag, a.status)) break;
+        tile_step(a, prefix, t_begin + i, ti);
+        mbar_arrive_tx(bar_full + 8 * s, kStageBytes);
+        tma_load_2d(cvta_smem(stage + s * kStageBytes), &a.tmap, 0,
+                    (int)(ti.base + (int64_t)ti.j * kTile), bar_full + 8 * s);
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - S); i < issued; ++i) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try(bar_full + 8 * (i % S), (i / S) & 1) && globaltimer() - t0 < kWaitNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      issued = 0;
+      const uint32_t b_base = cvta_smem(Bop);
+      for (int i = 0; i < n_local; ++i) {
+        const int acc = i % NACC, ab = i % NA;
+        tile_step(a, prefix, t_begin + i, ti);
+        const uint32_t idesc = idesc_f16(kTile, ti.nrows * a.H_i);
+        if (i >= NACC &&
+            !wait_bar(bar_accempty + 8 * acc, ((i / NACC) - 1) & 1, abort_flag, a.status))
+          break;
+        if (!wait_bar(bar_afull + 8 * ab, (i / NA) & 1, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t a_tm = tmem + a.a_col0 + ab * 64;
+#pragma unroll
+        for (int kk = 0; kk < D_I / 16; ++kk) {
+          const uint32_t kb = b_base + (kk >> 2) * (N_max * 128) + (kk & 3) * 32;
+          mma_f16_ta(tmem + acc * N_max, a_tm + kk * 8, smem_desc_sw128(kb), idesc, kk > 0);
+        }
+        mma_commit(bar_accfull + 8 * acc);
+        mma_commit(bar_afree + 8 * ab);
+        issued = i + 1;
+      }
+      // Drain: both commit arrivals of the last tiles must land before exit.
+      for (int i = max(0, issued - NACC); i < issued; ++i) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try(bar_accfull + 8 * (i % NACC), (i / NACC) & 1) && globaltimer() - t0 < kWaitNs) {
+        }
+      }
+      for (int i = max(0, issued - NA); i < issued; ++i) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try(bar_afree + 8 * (i % NA), (i / NA) & 1) && globaltimer() - t0 < kWaitNs) {
+        }
+      }
+    }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------------------ converters
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;        // key row = TMEM lane this thread writes
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + a.a_col0;
+    const int ct = tid - kConvWarp0 * 32;
+    for (int i = 0; i < n_local; ++i) {
+      const int s = i % S, ab = i % NA;
+      const bool new_group = tile_step(a, prefix, t_begin + i, ti);
+      if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status)) break;
+      if (i >= NA && !wait_bar_warp(bar_afree + 8 * ab, ((i / NA) - 1) & 1, abort_flag, a.status)) break;
+      if (new_group) {
+        // B may be rewritten once every issued MMA has finished.
+        if (i >= 1 &&
+            !wait_bar_warp(bar_afree + 8 * ((i - 1) % NA), ((i - 1) / NA) & 1, abort_flag, a.status))
+          break;
+        const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
+        const int nchunks = ti.nrows * a.H_i * (D_I / 16);
+        for (int q = ct; q < nchunks; q += kConvWarps * 32) {
+          uint32_t b0, b1;
+          sw128_offsets(q / (D_I / 16), q % (D_I / 16), (uint32_t)N_max * 128, b0, b1);
+          convert16<false>(__ldg(src + q), Bop + b0, Bop + b1);   // queries stay exact
+        }
+        fence_proxy_async();                  // B is read by the MMA (async proxy)
+      }
+      const unsigned char* row = stage + s * kStageBytes + m * 128;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        int4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          v[j] = *reinterpret_cast<const int4*>(row + (((half * 4 + j) ^ (m & 7)) << 4));
+        uint32_t o[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          i8x4_to_f16x4<BIASED>((uint32_t)v[j].x, o[8 * j + 0], o[8 * j + 1]);
+          i8x4_to_f16x4<BIASED>((uint32_t)v[j].y, o[8 * j + 2], o[8 * j + 3]);
+          i8x4_to_f16x4<BIASED>((uint32_t)v[j].z, o[8 * j + 4], o[8 * j + 5]);
+          i8x4_to_f16x4<BIASED>((uint32_t)v[j].w, o[8 * j + 6], o[8 * j + 7]);
+        }
+        tmem_st32(lane_base + ab * 64 + half * 32, o);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_afull + 8 * ab);
+        mbar_arrive(bar_empty + 8 * s);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - kEpiWarp0;         // 0..7
+    const int grp = ew >> 2;                 // tiles i with i % 2 == grp
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;
+    const int wstride = a.RG * a.H_i + kMaxRG;
+    int2* wc = wc_s + ew * wstride;
+    int* wsum = reinterpret_cast<int*>(wc + a.RG * a.H_i);
+    const float floor_v = a.relu ? kMagic : -3.0e38f;
+    int rlen0 = 0, rlen1 = 0, rlen2 = 0, rlen3 = 0;
+    uint32_t mx0 = 0, mx1 = 0, mx2 = 0, mx3 = 0, mn0 = 0, mn1 = 0, mn2 = 0, mn3 = 0;
+    int cur_r0 = -1, cur_n = 0;
+    for (int i = grp; i < n_local; i += 2) {
+      if (tile_step(a, prefix, t_begin + i, ti)) {
+        if (cur_n > 0) row_minmax_flush(a.rows + cur_r0, mx0, mn0);
+        if (cur_n > 1) row_minmax_flush(a.rows + cur_r0 + 1, mx1, mn1);
+        if (cur_n > 2) row_minmax_flush(a.rows + cur_r0 + 2, mx2, mn2);
+        if (cur_n > 3) row_minmax_flush(a.rows + cur_r0 + 3, mx3, mn3);
+        mx0 = mx1 = mx2 = mx3 = mn0 = mn1 = mn2 = mn3 = 0;
+        cur_r0 = ti.r0;
+        cur_n = ti.nrows;
+        __syncwarp();
+        for (int q = lane; q < ti.nrows * a.H_i; q += 32) {
+          const int w = a.w_idx[(int64_t)ti.r0 * a.H_i + q];
+          int bias = 0;
+          if (BIASED) {
+            const int4* qv = reinterpret_cast<const int4*>(a.q_idx + ((int64_t)ti.r0 * a.H_i + q) * D_I);
+#pragma unroll
+            for (int j = 0; j < D_I / 16; ++j) {
+              const int4 x = __ldg(qv + j);
+              bias = __dp4a(x.x, 0x01010101, bias);
+              bias = __dp4a(x.y, 0x01010101, bias);
+              bias = __dp4a(x.z, 0x01010101, bias);
+              bias = __dp4a(x.w, 0x01010101, bias);
+            }
+            bias *= 1152;
+          }
+          wc[q] = make_int2(w, __float_as_int((float)(12582912 - bias)));
+        }
+        __syncwarp();
+        if (lane < ti.nrows) {
+          uint32_t sacc = 0;
+          for (int h = 0; h < a.H_i; ++h) sacc += (uint32_t)wc[lane * a.H_i + h].x;
+          wsum[lane] = (int)sacc;
+        }
+        __syncwarp();
+        rlen0 = ti.nrows > 0 ? a.row_len[ti.r0] : 0;
+        rlen1 = ti.nrows > 1 ? a.row_len[ti.r0 + 1] : 0;
+        rlen2 = ti.nrows > 2 ? a.row_len[ti.r0 + 2] : 0;
+        rlen3 = ti.nrows > 3 ? a.row_len[ti.r0 + 3] : 0;
+      }
+      const int accb = i % NACC;
+      if (!wait_bar_warp(bar_accfull + 8 * accb, (i / NACC) & 1, abort_flag, a.status)) break;
+      tc_fence_after();
+      const int t = ti.j * kTile + m;
+      const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + accb * N_max;
+#pragma unroll
+      for (int jr = 0; jr < kMaxRG; ++jr) {
+        if (jr >= ti.nrows) break;
+        uint32_t acc4[4] = {0u, 0u, 0u, 0u};
+        const int4* wr = reinterpret_cast<const int4*>(wc + jr * a.H_i);
+        for (int h0 = 0; h0 < a.H_i; h0 += 64) {
+          uint32_t va[32], vb[32];
+          const bool two = h0 + 32 < a.H_i;
+          tmem_ld32(trow + jr * a.H_i + h0, va);
+          if (two) tmem_ld32(trow + jr * a.H_i + h0 + 32, vb);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h2 = 0; h2 < 16; ++h2) {
+            const int4 p = wr[(h0 >> 1) + h2];
+            const float x0 = fmaxf(__uint_as_float(va[2 * h2]) + __int_as_float(p.y), floor_v);
+            const float x1 = fmaxf(__uint_as_float(va[2 * h2 + 1]) + __int_as_float(p.w), floor_v);
+            acc4[(h2 & 1) * 2] += (uint32_t)__float_as_int(x0) * (uint32_t)p.x;
+            acc4[(h2 & 1) * 2 + 1] += (uint32_t)__float_as_int(x1) * (uint32_t)p.z;
+          }
+          if (two) {
+#pragma unroll
+            for (int h2 = 0; h2 < 16; ++h2) {
+              const int4 p = wr[(h0 >> 1) + 16 + h2];
+              const float x0 = fmaxf(__uint_as_float(vb[2 * h2]) + __int_as_float(p.y), floor_v);
+              const float x1 = fmaxf(__uint_as_float(vb[2 * h2 + 1]) + __int_as_float(p.w), floor_v);
+              acc4[(h2 & 1) * 2] += (uint32_t)__float_as_int(x0) * (uint32_t)p.x;
+              acc4[(h2 & 1) * 2 + 1] += (uint32_t)__float_as_int(x1) * (uint32_t)p.z;
+            }
+          }
+        }
+        uint32_t acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+        acc -= 0x4B400000u * (uint32_t)wsum[jr];
+        const int rl = jr == 0 ? rlen0 : (jr == 1 ? rlen1 : (jr == 2 ? rlen2 : rlen3));
+        if (t < rl) {
+          a.scores[(int64_t)(ti.r0 + jr) * a.L_max + t] = (int32_t)acc;
+          const uint32_t u = acc ^ 0x80000000u;
+          if (jr == 0) { mx0 = max(mx0, u); mn0 = max(mn0, ~u); }
+          if (jr == 1) { mx1 = max(mx1, u); mn1 = max(mn1, ~u); }
+          if (jr == 2) { mx2 = max(mx2, u); mn2 = max(mn2, ~u); }
+          if (jr == 3) { mx3 = max(mx3, u); mn3 = max(mn3, ~u); }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_accempty + 8 * accb);
+    }
+    if (cur_n > 0) row_minmax_flush(a.rows + cur_r0, mx0, mn0);
+    if (cur_n > 1) row_minmax_flush(a.rows + cur_r0 + 1, mx1, mn1);
+    if (cur_n > 2) row_minmax_flush(a.rows + cur_r0 + 2, mx2, mn2);
+    if (cur_n > 3) row_minmax_flush(a.rows + cur_r0 + 3, mx3, mn3);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
+                 : "memory");
+  }
+}
+
 }  // namespace
 
 bool indexer_tc_supported(const dsa_problem& p) {
@@ -631,9 +1006,37 @@ cudaError_t launch_tc_s(const TcArgs& a, int sms, size_t smem, cudaStream_t st) 
                        : launch_tc<D_I, 4, BIASED>(a, sms, smem, st);
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+template <int S, bool BIASED>
+cudaError_t launch_tm(const TcArgs& a, int sms, size_t smem, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(indexer_tc_tm_kernel<S, BIASED>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(indexer_tc_tm_kernel<S, BIASED>, dim3(sms), dim3(kThreads), smem, st, a);
+}
+
 cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                               cudaStream_t st) {
   TcArgs a;
+  std::memset(&a, 0, sizeof a);
   a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
   a.rows = reinterpret_cast<RowState*>(ws + pl.off_state);
   a.zero = reinterpret_cast<uint4*>(ws);
@@ -649,12 +1052,57 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   a.RG = RG;
   const int N_max = RG * p.H_i;
   const int D_i = p.D_i;
-  const uint32_t a_bytes = 2u * 128u * D_i * 2u;
-  const uint32_t b_bytes = (uint32_t)N_max * D_i * 2u;
-  const uint32_t stage_bytes = 128u * D_i;
+  // The biased conversion needs every partial sum |sum_d q_d (k_d + 1152)| < 2^24.
+  const int64_t qk = p.qk_abs_max > 0 ? p.qk_abs_max : 128;
+  const bool biased = (int64_t)D_i * qk * 1279 < (int64_t(1) << 24);
   const uint32_t prefix_bytes = ((uint32_t)(p.B + 1) * 4u + 15u) / 16u * 16u;
   const uint32_t w_bytes = kEpiWarps * (uint32_t)(RG * p.H_i + kMaxRG) * 8u;
   const uint32_t budget = 227u * 1024u - 1024u;   // minus the alignment slack
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+
+  EncodeTiledFn encode = D_i == 128 && p.L_total >= 128 ? encode_tiled_fn() : nullptr;
+  if (encode) {
+    // A operand in TMEM: NA A buffers of 64 columns, NACC accumulators, 512 columns in all.
+    a.na = kMaxA;
+    a.nacc = (512 - kMaxA * 64) / N_max;
+    if (a.nacc > kMaxAcc) a.nacc = kMaxAcc;
+    a.a_col0 = (uint32_t)(a.nacc * N_max);
+    uint32_t cols = 32;
+    while (cols < a.a_col0 + kMaxA * 64u) cols <<= 1;
+    a.tmem_cols = cols;
+    const cuuint64_t gdim[2] = {128u, (cuuint64_t)p.L_total};
+    const cuuint64_t gstride[1] = {128u};
+    const cuuint32_t box[2] = {128u, 128u};
+    const cuuint32_t estride[2] = {1u, 1u};
+    if (encode(&a.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(p.k_idx), gdim, gstride,
+               box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    const uint32_t stage_bytes = 128u * 128u;
+    const uint32_t b_bytes = (uint32_t)N_max * 128u * 2u;
+    auto total_for = [&](int s) {
+      return s * stage_bytes + b_bytes + w_bytes + (2 * s + 2 * kMaxA + 2 * kMaxAcc) * 8 + 16 + prefix_bytes;
+    };
+    const int S = total_for(8) <= budget ? 8 : 4;
+    if (total_for(S) > budget) return cudaErrorInvalidConfiguration;
+    a.stages = S;
+    a.off_b = S * stage_bytes;
+    a.off_w = a.off_b + b_bytes;
+    a.off_bar = a.off_w + w_bytes;
+    a.off_misc = a.off_bar + (2 * S + 2 * kMaxA + 2 * kMaxAcc) * 8;
+    a.off_prefix = a.off_misc + 16;
+    size_t smem = (size_t)a.off_prefix + prefix_bytes + 1024;
+    if (smem < 120u * 1024u) smem = 120u * 1024u;   // one CTA per SM: TMEM is never contended
+    if (S == 8) return biased ? launch_tm<8, true>(a, sms, smem, st) : launch_tm<8, false>(a, sms, smem, st);
+    return biased ? launch_tm<4, true>(a, sms, smem, st) : launch_tm<4, false>(a, sms, smem, st);
+  }
+
+  // A operand staged in shared memory (D_i = 64, or very short caches).
+  const uint32_t a_bytes = 2u * 128u * D_i * 2u;
+  const uint32_t b_bytes = (uint32_t)N_max * D_i * 2u;
+  const uint32_t stage_bytes = 128u * D_i;
   auto total_for = [&](int s) {
     return a_bytes + b_bytes + s * stage_bytes + w_bytes + (2 * s + 2 + 2 * kMaxAcc) * 8 + 16 +
            prefix_bytes;
@@ -674,12 +1122,6 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   a.tmem_cols = cols;
   size_t smem = (size_t)a.off_prefix + prefix_bytes + 1024;
   if (smem < 120u * 1024u) smem = 120u * 1024u;   // one CTA per SM: TMEM is never contended
-  // The biased conversion needs every partial sum |sum_d q_d (k_d + 1152)| < 2^24.
-  const int64_t qk = p.qk_abs_max > 0 ? p.qk_abs_max : 128;
-  const bool biased = (int64_t)D_i * qk * 1279 < (int64_t(1) << 24);
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (D_i == 128)
     return biased ? launch_tc_s<128, true>(a, sms, smem, st) : launch_tc_s<128, false>(a, sms, smem, st);
   return biased ? launch_tc_s<64, true>(a, sms, smem, st) : launch_tc_s<64, false>(a, sms, smem, st);
