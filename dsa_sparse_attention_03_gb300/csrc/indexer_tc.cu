@@ -1062,9 +1062,12 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
 
-  EncodeTiledFn encode = D_i == 128 && p.L_total >= 128 ? encode_tiled_fn() : nullptr;
+  // A operand in TMEM: 4 A buffers of 64 columns and NACC accumulators within 512
+  // columns.  Each epilogue group must own its accumulator buffers (NACC even),
+  // else a group could wait on a barrier two phases ahead: N_max <= 128 only.
+  EncodeTiledFn encode =
+      D_i == 128 && N_max <= 128 && p.L_total >= 128 ? encode_tiled_fn() : nullptr;
   if (encode) {
-    // A operand in TMEM: NA A buffers of 64 columns, NACC accumulators, 512 columns in all.
     a.na = kMaxA;
     a.nacc = (512 - kMaxA * 64) / N_max;
     if (a.nacc > kMaxAcc) a.nacc = kMaxAcc;
