@@ -58,6 +58,7 @@ constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
 constexpr int kMaxRG = 4;                    // query rows per MMA group (N <= 256)
 constexpr int kMaxAcc = 4;                   // TMEM accumulator buffers at most
 constexpr int kMaxA = 4;                     // TMEM A buffers at most (TMEM-operand kernel)
+constexpr int kModeExact = 0, kModeBiased = 1, kModeFp8 = 2;
 constexpr float kMagic = 12582912.f;         // 1.5 * 2^23
 
 struct TcArgs {
@@ -196,6 +197,16 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
+// kind::f8f6f4 (e4m3 x e4m3, fp32 accumulate, K = 32) with A read from TMEM.
+__device__ __forceinline__ void mma_f8_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // As mma_f16 with the A operand read from TMEM (row = lane, 2 fp16 per column).
 __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                            uint32_t idesc, uint32_t accumulate) {
@@ -258,6 +269,17 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     lo = *reinterpret_cast<uint32_t*>(&ha);
     hi = *reinterpret_cast<uint32_t*>(&hb);
   }
+}
+
+// Four int8 -> four e4m3 (one word): exact fp16 first, then cvt to e4m3x2.
+// Exact for |k| <= 16 (every such integer is an e4m3 value).
+__device__ __forceinline__ uint32_t i8x4_to_e4m3x4(uint32_t w) {
+  uint32_t lo, hi;
+  i8x4_to_f16x4<false>(w, lo, hi);
+  uint16_t a, b;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(a) : "r"(lo));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(b) : "r"(hi));
+  return (uint32_t)a | ((uint32_t)b << 16);
 }
 
 // 16 int8 -> 16 fp16 written as two 16-byte chunks at byte offsets d0, d1.
@@ -662,9 +684,13 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
 // shared memory.  Rings: S key stages, NA TMEM A buffers, NACC accumulators.
 // The MMA commits each tile twice: to the accumulator's barrier (epilogue) and
 // to the A buffer's barrier (converters may reuse it).
-template <int S, bool BIASED>
+// MODE: kModeExact (fp16, k exact), kModeBiased (fp16 k + 1152), kModeFp8 (e4m3).
+template <int S, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid_constant__ TcArgs a) {
   constexpr int D_I = 128;
+  constexpr bool BIASED = MODE == kModeBiased;
+  constexpr bool FP8 = MODE == kModeFp8;
+  constexpr int kACols = FP8 ? 32 : 64;                     // TMEM columns per A buffer
   constexpr uint32_t kStageBytes = kTile * D_I;             // one int8 tile (16 KB)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
@@ -796,11 +822,17 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid
           break;
         if (!wait_bar(bar_afull + 8 * ab, (i / NA) & 1, abort_flag, a.status)) break;
         tc_fence_after();
-        const uint32_t a_tm = tmem + a.a_col0 + ab * 64;
+        const uint32_t a_tm = tmem + a.a_col0 + ab * kACols;
+        if (FP8) {
 #pragma unroll
-        for (int kk = 0; kk < D_I / 16; ++kk) {
-          const uint32_t kb = b_base + (kk >> 2) * (N_max * 128) + (kk & 3) * 32;
-          mma_f16_ta(tmem + acc * N_max, a_tm + kk * 8, smem_desc_sw128(kb), idesc, kk > 0);
+          for (int kk = 0; kk < D_I / 32; ++kk)   // one 128-byte K-block, 32 bytes per step
+            mma_f8_ta(tmem + acc * N_max, a_tm + kk * 8, smem_desc_sw128(b_base + kk * 32), idesc, kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D_I / 16; ++kk) {
+            const uint32_t kb = b_base + (kk >> 2) * (N_max * 128) + (kk & 3) * 32;
+            mma_f16_ta(tmem + acc * N_max, a_tm + kk * 8, smem_desc_sw128(kb), idesc, kk > 0);
+          }
         }
         mma_commit(bar_accfull + 8 * acc);
         mma_commit(bar_afree + 8 * ab);
@@ -837,28 +869,52 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid
         const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
         const int nchunks = ti.nrows * a.H_i * (D_I / 16);
         for (int q = ct; q < nchunks; q += kConvWarps * 32) {
-          uint32_t b0, b1;
-          sw128_offsets(q / (D_I / 16), q % (D_I / 16), (uint32_t)N_max * 128, b0, b1);
-          convert16<false>(__ldg(src + q), Bop + b0, Bop + b1);   // queries stay exact
+          const int n = q / (D_I / 16), c = q % (D_I / 16);
+          if (FP8) {
+            // e4m3 rows of 128 bytes: 16-byte unit c of row n at unit c ^ (n mod 8).
+            const int4 v = __ldg(src + q);
+            *reinterpret_cast<uint4*>(Bop + n * 128 + ((c ^ (n & 7)) << 4)) =
+                make_uint4(i8x4_to_e4m3x4((uint32_t)v.x), i8x4_to_e4m3x4((uint32_t)v.y),
+                           i8x4_to_e4m3x4((uint32_t)v.z), i8x4_to_e4m3x4((uint32_t)v.w));
+          } else {
+            uint32_t b0, b1;
+            sw128_offsets(n, c, (uint32_t)N_max * 128, b0, b1);
+            convert16<false>(__ldg(src + q), Bop + b0, Bop + b1);   // queries stay exact
+          }
         }
         fence_proxy_async();                  // B is read by the MMA (async proxy)
       }
       const unsigned char* row = stage + s * kStageBytes + m * 128;
+      if (FP8) {
+        int4 v[8];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        int4 v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          v[j] = *reinterpret_cast<const int4*>(row + (((half * 4 + j) ^ (m & 7)) << 4));
+        for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const int4*>(row + ((j ^ (m & 7)) << 4));
         uint32_t o[32];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          i8x4_to_f16x4<BIASED>((uint32_t)v[j].x, o[8 * j + 0], o[8 * j + 1]);
-          i8x4_to_f16x4<BIASED>((uint32_t)v[j].y, o[8 * j + 2], o[8 * j + 3]);
-          i8x4_to_f16x4<BIASED>((uint32_t)v[j].z, o[8 * j + 4], o[8 * j + 5]);
-          i8x4_to_f16x4<BIASED>((uint32_t)v[j].w, o[8 * j + 6], o[8 * j + 7]);
+        for (int j = 0; j < 8; ++j) {
+          o[4 * j + 0] = i8x4_to_e4m3x4((uint32_t)v[j].x);
+          o[4 * j + 1] = i8x4_to_e4m3x4((uint32_t)v[j].y);
+          o[4 * j + 2] = i8x4_to_e4m3x4((uint32_t)v[j].z);
+          o[4 * j + 3] = i8x4_to_e4m3x4((uint32_t)v[j].w);
         }
-        tmem_st32(lane_base + ab * 64 + half * 32, o);
+        tmem_st32(lane_base + ab * kACols, o);
+      } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          int4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            v[j] = *reinterpret_cast<const int4*>(row + (((half * 4 + j) ^ (m & 7)) << 4));
+          uint32_t o[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            i8x4_to_f16x4<BIASED>((uint32_t)v[j].x, o[8 * j + 0], o[8 * j + 1]);
+            i8x4_to_f16x4<BIASED>((uint32_t)v[j].y, o[8 * j + 2], o[8 * j + 3]);
+            i8x4_to_f16x4<BIASED>((uint32_t)v[j].z, o[8 * j + 4], o[8 * j + 5]);
+            i8x4_to_f16x4<BIASED>((uint32_t)v[j].w, o[8 * j + 6], o[8 * j + 7]);
+          }
+          tmem_st32(lane_base + ab * kACols + half * 32, o);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -1025,12 +1081,17 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-template <int S, bool BIASED>
+template <int S, int MODE>
 cudaError_t launch_tm(const TcArgs& a, int sms, size_t smem, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(indexer_tc_tm_kernel<S, BIASED>,
+  cudaError_t e = cudaFuncSetAttribute(indexer_tc_tm_kernel<S, MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(indexer_tc_tm_kernel<S, BIASED>, dim3(sms), dim3(kThreads), smem, st, a);
+  return launch_pdl(indexer_tc_tm_kernel<S, MODE>, dim3(sms), dim3(kThreads), smem, st, a);
+}
+
+template <int MODE>
+cudaError_t launch_tm_s(const TcArgs& a, int sms, size_t smem, cudaStream_t st) {
+  return a.stages == 8 ? launch_tm<8, MODE>(a, sms, smem, st) : launch_tm<4, MODE>(a, sms, smem, st);
 }
 
 cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
@@ -1068,12 +1129,17 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   EncodeTiledFn encode =
       D_i == 128 && N_max <= 128 && p.L_total >= 128 ? encode_tiled_fn() : nullptr;
   if (encode) {
+    // e4m3 operands (K = 32 per MMA, half the MMAs) when every value is an exact
+    // e4m3 integer and the per-head dots stay below 2^14 (|q|,|k| <= 11 at D_i = 128).
+    const bool fp8 = (int64_t)D_i * qk * qk < (int64_t(1) << 14);
+    const int mode = fp8 ? kModeFp8 : (biased ? kModeBiased : kModeExact);
+    const uint32_t a_cols = fp8 ? 32u : 64u;
     a.na = kMaxA;
-    a.nacc = (512 - kMaxA * 64) / N_max;
+    a.nacc = (int)((512u - kMaxA * a_cols) / (uint32_t)N_max);
     if (a.nacc > kMaxAcc) a.nacc = kMaxAcc;
     a.a_col0 = (uint32_t)(a.nacc * N_max);
     uint32_t cols = 32;
-    while (cols < a.a_col0 + kMaxA * 64u) cols <<= 1;
+    while (cols < a.a_col0 + kMaxA * a_cols) cols <<= 1;
     a.tmem_cols = cols;
     const cuuint64_t gdim[2] = {128u, (cuuint64_t)p.L_total};
     const cuuint64_t gstride[1] = {128u};
@@ -1084,7 +1150,7 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     const uint32_t stage_bytes = 128u * 128u;
-    const uint32_t b_bytes = (uint32_t)N_max * 128u * 2u;
+    const uint32_t b_bytes = (uint32_t)N_max * 128u * (fp8 ? 1u : 2u);
     auto total_for = [&](int s) {
       return s * stage_bytes + b_bytes + w_bytes + (2 * s + 2 * kMaxA + 2 * kMaxAcc) * 8 + 16 + prefix_bytes;
     };
@@ -1098,8 +1164,9 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
     a.off_prefix = a.off_misc + 16;
     size_t smem = (size_t)a.off_prefix + prefix_bytes + 1024;
     if (smem < 120u * 1024u) smem = 120u * 1024u;   // one CTA per SM: TMEM is never contended
-    if (S == 8) return biased ? launch_tm<8, true>(a, sms, smem, st) : launch_tm<8, false>(a, sms, smem, st);
-    return biased ? launch_tm<4, true>(a, sms, smem, st) : launch_tm<4, false>(a, sms, smem, st);
+    if (mode == kModeFp8) return launch_tm_s<kModeFp8>(a, sms, smem, st);
+    if (mode == kModeBiased) return launch_tm_s<kModeBiased>(a, sms, smem, st);
+    return launch_tm_s<kModeExact>(a, sms, smem, st);
   }
 
   // A operand staged in shared memory (D_i = 64, or very short caches).

@@ -108,3 +108,15 @@ def test_tc_biased_path_at_its_exactness_limit():
     x.k_idx[:] = rng.choice(np.array([-102, 102, 0], np.int8), x.k_idx.shape)
     x.w_idx[:] = 1
     _check_one(x, None, True, True, 102)
+
+
+def test_tc_fp8_path_at_its_exactness_limit():
+    # A declared bound of 11 at D_i = 128 selects e4m3 operands (every |v| <= 16 is
+    # an e4m3 integer, and 128 * 11^2 < 2^14 keeps each head's dot small): values
+    # at +-11 everywhere must still give bit-exact scores.
+    x = gen.l64k(L=3000)
+    rng = np.random.default_rng(11)
+    x.q_idx[:] = rng.choice(np.array([-11, 11, 7, -3, 0], np.int8), x.q_idx.shape)
+    x.k_idx[:] = rng.choice(np.array([-11, 11, -10, 9, 1], np.int8), x.k_idx.shape)
+    _check_one(x, None, True, True, 11)
+    _check_one(x, None, False, True, 11)
