@@ -59,6 +59,11 @@ constexpr int kMaxRG = 4;                    // query rows per MMA group (N <= 2
 constexpr int kMaxAcc = 4;                   // TMEM accumulator buffers at most
 constexpr int kMaxA = 4;                     // TMEM A buffers at most (TMEM-operand kernel)
 constexpr int kModeExact = 0, kModeBiased = 1, kModeFp8 = 2;
+// TMEM-operand kernel: producer, MMA, 8 converters (two per TMEM lane quarter,
+// one half of each key row each), 8 epilogue warps (two groups of four).
+constexpr int kTmConvWarps = 8;
+constexpr int kTmEpiWarp0 = 2 + kTmConvWarps;
+constexpr int kTmThreads = (2 + kTmConvWarps + kEpiWarps) * 32;
 constexpr float kMagic = 12582912.f;         // 1.5 * 2^23
 
 struct TcArgs {
@@ -247,6 +252,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
       "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
       "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 
@@ -686,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
 // to the A buffer's barrier (converters may reuse it).
 // MODE: kModeExact (fp16, k exact), kModeBiased (fp16 k + 1152), kModeFp8 (e4m3).
 template <int S, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __grid_constant__ TcArgs a) {
   constexpr int D_I = 128;
   constexpr bool BIASED = MODE == kModeBiased;
   constexpr bool FP8 = MODE == kModeFp8;
@@ -715,10 +729,10 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid
     if (lane == 0) {
       for (int s = 0; s < S; ++s) {
         mbar_init(bar_full + 8 * s, 1);
-        mbar_init(bar_empty + 8 * s, kConvWarps);
+        mbar_init(bar_empty + 8 * s, kTmConvWarps);
       }
       for (int i = 0; i < kMaxA; ++i) {
-        mbar_init(bar_afull + 8 * i, kConvWarps);
+        mbar_init(bar_afull + 8 * i, kTmConvWarps);
         mbar_init(bar_afree + 8 * i, 1);
       }
       for (int i = 0; i < kMaxAcc; ++i) {
@@ -739,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid
 
   pdl_wait();
   pdl_trigger();
-  for (int i = blockIdx.x * kThreads + tid; i < a.n_zero; i += gridDim.x * kThreads)
+  for (int i = blockIdx.x * kTmThreads + tid; i < a.n_zero; i += gridDim.x * kTmThreads)
     a.zero[i] = make_uint4(0, 0, 0, 0);
 
   TileInfo ti;
@@ -850,12 +864,13 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid
         }
       }
     }
-  } else if (warp < kEpiWarp0) {
+  } else if (warp < kTmEpiWarp0) {
     // ------------------------------------------------------------ converters
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;   // which 64 bytes of each key row
     const int m = quarter * 32 + lane;        // key row = TMEM lane this thread writes
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + a.a_col0;
-    const int ct = tid - kConvWarp0 * 32;
+    const int ct = tid - 64;
     for (int i = 0; i < n_local; ++i) {
       const int s = i % S, ab = i % NA;
       const bool new_group = tile_step(a, prefix, t_begin + i, ti);
@@ -868,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid
           break;
         const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
         const int nchunks = ti.nrows * a.H_i * (D_I / 16);
-        for (int q = ct; q < nchunks; q += kConvWarps * 32) {
+        for (int q = ct; q < nchunks; q += kTmConvWarps * 32) {
           const int n = q / (D_I / 16), c = q % (D_I / 16);
           if (FP8) {
             // e4m3 rows of 128 bytes: 16-byte unit c of row n at unit c ^ (n mod 8).
@@ -885,36 +900,30 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid
         fence_proxy_async();                  // B is read by the MMA (async proxy)
       }
       const unsigned char* row = stage + s * kStageBytes + m * 128;
+      int4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        v[j] = *reinterpret_cast<const int4*>(row + (((half * 4 + j) ^ (m & 7)) << 4));
       if (FP8) {
-        int4 v[8];
+        uint32_t o[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const int4*>(row + ((j ^ (m & 7)) << 4));
-        uint32_t o[32];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
           o[4 * j + 0] = i8x4_to_e4m3x4((uint32_t)v[j].x);
           o[4 * j + 1] = i8x4_to_e4m3x4((uint32_t)v[j].y);
           o[4 * j + 2] = i8x4_to_e4m3x4((uint32_t)v[j].z);
           o[4 * j + 3] = i8x4_to_e4m3x4((uint32_t)v[j].w);
         }
-        tmem_st32(lane_base + ab * kACols, o);
+        tmem_st16(lane_base + ab * kACols + half * 16, o);
       } else {
+        uint32_t o[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          int4 v[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            v[j] = *reinterpret_cast<const int4*>(row + (((half * 4 + j) ^ (m & 7)) << 4));
-          uint32_t o[32];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            i8x4_to_f16x4<BIASED>((uint32_t)v[j].x, o[8 * j + 0], o[8 * j + 1]);
-            i8x4_to_f16x4<BIASED>((uint32_t)v[j].y, o[8 * j + 2], o[8 * j + 3]);
-            i8x4_to_f16x4<BIASED>((uint32_t)v[j].z, o[8 * j + 4], o[8 * j + 5]);
-            i8x4_to_f16x4<BIASED>((uint32_t)v[j].w, o[8 * j + 6], o[8 * j + 7]);
-          }
-          tmem_st32(lane_base + ab * kACols + half * 32, o);
+        for (int j = 0; j < 4; ++j) {
+          i8x4_to_f16x4<BIASED>((uint32_t)v[j].x, o[8 * j + 0], o[8 * j + 1]);
+          i8x4_to_f16x4<BIASED>((uint32_t)v[j].y, o[8 * j + 2], o[8 * j + 3]);
+          i8x4_to_f16x4<BIASED>((uint32_t)v[j].z, o[8 * j + 4], o[8 * j + 5]);
+          i8x4_to_f16x4<BIASED>((uint32_t)v[j].w, o[8 * j + 6], o[8 * j + 7]);
         }
+        tmem_st32(lane_base + ab * kACols + half * 32, o);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -926,7 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - kEpiWarp0;         // 0..7
+    const int ew = warp - kTmEpiWarp0;       // 0..7
     const int grp = ew >> 2;                 // tiles i with i % 2 == grp
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;
@@ -986,29 +995,19 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_tm_kernel(const __grid
         if (jr >= ti.nrows) break;
         uint32_t acc4[4] = {0u, 0u, 0u, 0u};
         const int4* wr = reinterpret_cast<const int4*>(wc + jr * a.H_i);
-        for (int h0 = 0; h0 < a.H_i; h0 += 64) {
-          uint32_t va[32], vb[32];
-          const bool two = h0 + 32 < a.H_i;
+        for (int h0 = 0; h0 < a.H_i; h0 += 32) {
+          uint32_t va[32];
           tmem_ld32(trow + jr * a.H_i + h0, va);
-          if (two) tmem_ld32(trow + jr * a.H_i + h0 + 32, vb);
           tmem_wait_ld();
 #pragma unroll
           for (int h2 = 0; h2 < 16; ++h2) {
-            const int4 p = wr[(h0 >> 1) + h2];
+            const int4 p = wr[(h0 >> 1) + h2];     // (w, c) of heads h0+2*h2 and h0+2*h2+1
+            // x = max(d - bias + M, floor) = M + ReLU(q.k): an exact integer in
+            // [2^23, 2^24), so its bit pattern is 0x4B400000 + score part.
             const float x0 = fmaxf(__uint_as_float(va[2 * h2]) + __int_as_float(p.y), floor_v);
             const float x1 = fmaxf(__uint_as_float(va[2 * h2 + 1]) + __int_as_float(p.w), floor_v);
             acc4[(h2 & 1) * 2] += (uint32_t)__float_as_int(x0) * (uint32_t)p.x;
             acc4[(h2 & 1) * 2 + 1] += (uint32_t)__float_as_int(x1) * (uint32_t)p.z;
-          }
-          if (two) {
-#pragma unroll
-            for (int h2 = 0; h2 < 16; ++h2) {
-              const int4 p = wr[(h0 >> 1) + 16 + h2];
-              const float x0 = fmaxf(__uint_as_float(vb[2 * h2]) + __int_as_float(p.y), floor_v);
-              const float x1 = fmaxf(__uint_as_float(vb[2 * h2 + 1]) + __int_as_float(p.w), floor_v);
-              acc4[(h2 & 1) * 2] += (uint32_t)__float_as_int(x0) * (uint32_t)p.x;
-              acc4[(h2 & 1) * 2 + 1] += (uint32_t)__float_as_int(x1) * (uint32_t)p.z;
-            }
           }
         }
         uint32_t acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
@@ -1086,7 +1085,7 @@ cudaError_t launch_tm(const TcArgs& a, int sms, size_t smem, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(indexer_tc_tm_kernel<S, MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(indexer_tc_tm_kernel<S, MODE>, dim3(sms), dim3(kThreads), smem, st, a);
+  return launch_pdl(indexer_tc_tm_kernel<S, MODE>, dim3(sms), dim3(kTmThreads), smem, st, a);
 }
 
 template <int MODE>
