@@ -59,11 +59,19 @@ constexpr int kMaxRG = 4;                    // query rows per MMA group (N <= 2
 constexpr int kMaxAcc = 4;                   // TMEM accumulator buffers at most
 constexpr int kMaxA = 4;                     // TMEM A buffers at most (TMEM-operand kernel)
 constexpr int kModeExact = 0, kModeBiased = 1, kModeFp8 = 2;
-// TMEM-operand kernel: producer, MMA, 8 converters (two per TMEM lane quarter,
-// one half of each key row each), 8 epilogue warps (two groups of four).
-constexpr int kTmConvWarps = 8;
-constexpr int kTmEpiWarp0 = 2 + kTmConvWarps;
-constexpr int kTmThreads = (2 + kTmConvWarps + kEpiWarps) * 32;
+// TMEM-operand kernel warp roles.  Issuing a tcgen05.mma occupies the issuing
+// SM sub-partition for tens of ns, and every TMEM-touching role is tied to a
+// sub-partition (warp w reaches TMEM lanes 32*(w%4)..), so MMA issue is spread
+// over four threads, one per sub-partition, each taking every fourth tile:
+//   warp 0       TMA producer              warps 1-4    MMA issuers (tile % 4)
+//   warps 5-8    converters (lane quarter = warp % 4)
+//   warps 9-16   epilogue, two groups of four (tile % 2)
+constexpr int kTmMmaWarp0 = 1;
+constexpr int kTmMmaWarps = 4;
+constexpr int kTmConvWarp0 = kTmMmaWarp0 + kTmMmaWarps;
+constexpr int kTmConvWarps = 4;
+constexpr int kTmEpiWarp0 = kTmConvWarp0 + kTmConvWarps;
+constexpr int kTmThreads = (kTmEpiWarp0 + kEpiWarps) * 32;
 constexpr float kMagic = 12582912.f;         // 1.5 * 2^23
 
 struct TcArgs {
@@ -114,14 +122,16 @@ __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 
+// The thread sleeps in hardware until the phase completes (or ~20 us pass),
+// rather than re-polling and taking issue slots from the working warps.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(20000)
       : "memory");
   return ok != 0;
 }
@@ -134,7 +144,7 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
   const uint64_t t0 = globaltimer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try(bar, parity)) return true;
-    if ((n & 15) == 0) {
+    {
       if (*abort_flag) return false;
       if (globaltimer() - t0 > kWaitNs) {
         *abort_flag = 1;
@@ -822,12 +832,16 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp < kTmConvWarp0) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer j takes tiles i = j (mod 4): with NA = 4 it always fills A buffer j
+    // and, with NACC = 4, accumulator j.  A tcgen05.commit covers the MMAs of
+    // its own thread, so each tile's two commits come from its issuer.
+    const int j = warp - kTmMmaWarp0;
     if (lane == 0) {
-      issued = 0;
+      int last = -1;
       const uint32_t b_base = cvta_smem(Bop);
-      for (int i = 0; i < n_local; ++i) {
+      for (int i = j; i < n_local; i += kTmMmaWarps) {
         const int acc = i % NACC, ab = i % NA;
         tile_step(a, prefix, t_begin + i, ti);
         const uint32_t idesc = idesc_f16(kTile, ti.nrows * a.H_i);
@@ -850,37 +864,35 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
         }
         mma_commit(bar_accfull + 8 * acc);
         mma_commit(bar_afree + 8 * ab);
-        issued = i + 1;
+        last = i;
       }
-      // Drain: both commit arrivals of the last tiles must land before exit.
-      for (int i = max(0, issued - NACC); i < issued; ++i) {
+      // Drain: both commit arrivals of this issuer's last tile must land.
+      if (last >= 0) {
         const uint64_t t0 = globaltimer();
-        while (!mbar_try(bar_accfull + 8 * (i % NACC), (i / NACC) & 1) && globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try(bar_accfull + 8 * (last % NACC), (last / NACC) & 1) && globaltimer() - t0 < kWaitNs) {
         }
-      }
-      for (int i = max(0, issued - NA); i < issued; ++i) {
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try(bar_afree + 8 * (i % NA), (i / NA) & 1) && globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try(bar_afree + 8 * (last % NA), (last / NA) & 1) && globaltimer() - t0 < kWaitNs) {
         }
       }
     }
   } else if (warp < kTmEpiWarp0) {
     // ------------------------------------------------------------ converters
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;   // which 64 bytes of each key row
     const int m = quarter * 32 + lane;        // key row = TMEM lane this thread writes
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + a.a_col0;
-    const int ct = tid - 64;
+    const int ct = tid - kTmConvWarp0 * 32;
     for (int i = 0; i < n_local; ++i) {
       const int s = i % S, ab = i % NA;
       const bool new_group = tile_step(a, prefix, t_begin + i, ti);
       if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status)) break;
       if (i >= NA && !wait_bar_warp(bar_afree + 8 * ab, ((i / NA) - 1) & 1, abort_flag, a.status)) break;
       if (new_group) {
-        // B may be rewritten once every issued MMA has finished.
-        if (i >= 1 &&
-            !wait_bar_warp(bar_afree + 8 * ((i - 1) % NA), ((i - 1) / NA) & 1, abort_flag, a.status))
-          break;
+        // B may be rewritten once every issued MMA has finished (the last NA
+        // tiles come from different issuers, so wait for each of them).
+        bool ok = true;
+        for (int pr = max(0, i - NA); pr < i && ok; ++pr)
+          ok = wait_bar_warp(bar_afree + 8 * (pr % NA), (pr / NA) & 1, abort_flag, a.status);
+        if (!ok) break;
         const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
         const int nchunks = ti.nrows * a.H_i * (D_I / 16);
         for (int q = ct; q < nchunks; q += kTmConvWarps * 32) {
@@ -900,30 +912,36 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
         fence_proxy_async();                  // B is read by the MMA (async proxy)
       }
       const unsigned char* row = stage + s * kStageBytes + m * 128;
-      int4 v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        v[j] = *reinterpret_cast<const int4*>(row + (((half * 4 + j) ^ (m & 7)) << 4));
       if (FP8) {
-        uint32_t o[16];
+        int4 v[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const int4*>(row + ((j ^ (m & 7)) << 4));
+        uint32_t o[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
           o[4 * j + 0] = i8x4_to_e4m3x4((uint32_t)v[j].x);
           o[4 * j + 1] = i8x4_to_e4m3x4((uint32_t)v[j].y);
           o[4 * j + 2] = i8x4_to_e4m3x4((uint32_t)v[j].z);
           o[4 * j + 3] = i8x4_to_e4m3x4((uint32_t)v[j].w);
         }
-        tmem_st16(lane_base + ab * kACols + half * 16, o);
+        tmem_st32(lane_base + ab * kACols, o);
       } else {
-        uint32_t o[32];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          i8x4_to_f16x4<BIASED>((uint32_t)v[j].x, o[8 * j + 0], o[8 * j + 1]);
-          i8x4_to_f16x4<BIASED>((uint32_t)v[j].y, o[8 * j + 2], o[8 * j + 3]);
-          i8x4_to_f16x4<BIASED>((uint32_t)v[j].z, o[8 * j + 4], o[8 * j + 5]);
-          i8x4_to_f16x4<BIASED>((uint32_t)v[j].w, o[8 * j + 6], o[8 * j + 7]);
+        for (int half = 0; half < 2; ++half) {
+          int4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            v[j] = *reinterpret_cast<const int4*>(row + (((half * 4 + j) ^ (m & 7)) << 4));
+          uint32_t o[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            i8x4_to_f16x4<BIASED>((uint32_t)v[j].x, o[8 * j + 0], o[8 * j + 1]);
+            i8x4_to_f16x4<BIASED>((uint32_t)v[j].y, o[8 * j + 2], o[8 * j + 3]);
+            i8x4_to_f16x4<BIASED>((uint32_t)v[j].z, o[8 * j + 4], o[8 * j + 5]);
+            i8x4_to_f16x4<BIASED>((uint32_t)v[j].w, o[8 * j + 6], o[8 * j + 7]);
+          }
+          tmem_st32(lane_base + ab * kACols + half * 32, o);
         }
-        tmem_st32(lane_base + ab * kACols + half * 32, o);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -1133,7 +1151,7 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
     const bool fp8 = (int64_t)D_i * qk * qk < (int64_t(1) << 14);
     const int mode = fp8 ? kModeFp8 : (biased ? kModeBiased : kModeExact);
     const uint32_t a_cols = fp8 ? 32u : 64u;
-    a.na = kMaxA;
+    a.na = kMaxA;                                  // = kTmMmaWarps: issuer j owns A buffer j
     a.nacc = (int)((512u - kMaxA * a_cols) / (uint32_t)N_max);
     if (a.nacc > kMaxAcc) a.nacc = kMaxAcc;
     a.a_col0 = (uint32_t)(a.nacc * N_max);
