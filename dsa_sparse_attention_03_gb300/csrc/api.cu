@@ -92,6 +92,9 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   while (chunk < 65536 && int64_t(chunk) * 600 < work) chunk <<= 1;
   P.chunk = chunk;
   P.nchunk = p->L_max > 0 ? (p->L_max + chunk - 1) / chunk : 1;
+  // Hundreds of CTAs adding into one row's 2048 bins serialise on the few hot
+  // bins' L2 lines; CTA c adds into copy c % hist_rep instead.
+  P.hist_rep = P.nchunk >= 256 ? 8 : (P.nchunk >= 64 ? 4 : 1);
 
   // Attention: split the k selected positions so that all rows together give
   // a few hundred CTAs, each over whole 64-position tiles.
@@ -105,7 +108,7 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   size_t off = 0;
   P.off_status = off; off += 256;
   P.off_state = off; off = align_up(off + R * sizeof(RowState), 256);
-  P.off_hist = off; off = align_up(off + R * kBuckets * 4, 256);
+  P.off_hist = off; off = align_up(off + R * size_t(P.hist_rep) * kBuckets * 4, 256);
   P.zero_end = off;
   P.off_surv = off; off = align_up(off + R * size_t(kCapFast) * 8, 256);
   P.off_scores = off; off = align_up(off + R * size_t(p->L_max) * 4, 256);

@@ -37,6 +37,7 @@ struct Plan {
   int R, B, H_i, D_i, H_q, D_k, D_v, k, L_max;
   int flags;
   int chunk, nchunk;       // top-k: positions per CTA, CTAs per row
+  int hist_rep;            // top-k: copies of each row's global histogram
   int nsplit;              // attention: CTAs along the selected positions
   size_t off_status, off_state, off_hist, zero_end;
   size_t off_surv, off_scores, off_part, off_ml, total;

@@ -46,10 +46,10 @@ struct TopkArgs {
   int32_t* idx;
   int32_t* nsel;
   RowState* state;
-  uint32_t* hist;      // [R, kBuckets]
+  uint32_t* hist;      // [R, hist_rep, kBuckets]
   uint64_t* surv;      // [R, kCapFast] survivor keys
   int64_t L_max;
-  int k, chunk;
+  int k, chunk, hist_rep;
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -225,10 +225,12 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(TopkArgs a) {
     scan_row<kThreads>(a.scores + (int64_t)r * a.L_max, start, end,
                        [&](int32_t v, int) { atomicAdd(&h[bin(ordered_key(v))], 1u); });
   __syncthreads();
-  uint32_t* gh = a.hist + (size_t)r * kBuckets;
-  if (len > a.k)
+  uint32_t* gh = a.hist + (size_t)r * a.hist_rep * kBuckets;
+  if (len > a.k) {
+    uint32_t* mine = gh + (size_t)(blockIdx.x % a.hist_rep) * kBuckets;
     for (int i = threadIdx.x; i < kBuckets; i += kThreads)
-      if (h[i]) atomicAdd(&gh[i], h[i]);
+      if (h[i]) atomicAdd(&mine[i], h[i]);
+  }
 
   if (!last_arrival(&st->arrive[0], gridDim.x)) return;
   // Last CTA of the row: pick the mode and the threshold bucket.
@@ -240,7 +242,11 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(TopkArgs a) {
     }
     return;
   }
-  for (int i = threadIdx.x; i < kBuckets; i += kThreads) h[i] = ld_volatile(&gh[i]);
+  for (int i = threadIdx.x; i < kBuckets; i += kThreads) {
+    uint32_t c = 0;
+    for (int j = 0; j < a.hist_rep; ++j) c += ld_volatile(&gh[(size_t)j * kBuckets + i]);
+    h[i] = c;
+  }
   __syncthreads();
   find_crossing<kThreads>(h, kBuckets, (uint32_t)a.k, res);
   if (threadIdx.x == 0) {
@@ -269,22 +275,29 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkArgs a) {
   const int end = min(start + a.chunk, len);
   const int32_t* s = a.scores + (int64_t)r * a.L_max;
   uint64_t* surv = a.surv + (size_t)r * kCapFast;
-  const int lane = threadIdx.x & 31;
-  for (int base = start; base < end; base += kThreads) {
-    const int t = base + threadIdx.x;
-    int32_t v = 0;
-    bool take = false;
-    if (t < end) {
-      v = s[t];
-      take = mode == kAll || bin(ordered_key(v)) >= bstar;
+  // Four positions per thread per sweep; the CTA claims its slots with one
+  // atomic (hundreds of per-warp atomics on n_union would serialise).
+  constexpr int U = 4;
+  __shared__ uint32_t wt[kThreads / 32];
+  __shared__ uint32_t slot0;
+  for (int base = start; base < end; base += U * kThreads) {
+    int32_t v[U];
+    uint32_t take = 0;
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int t = base + j * kThreads + (int)threadIdx.x;
+      v[j] = t < end ? s[t] : 0;
+      if (t < end && (mode == kAll || bin(ordered_key(v[j])) >= bstar)) take |= 1u << j;
     }
-    const uint32_t m = __ballot_sync(0xffffffffu, take);
-    if (m) {
-      uint32_t slot = 0;
-      if (lane == 0) slot = atomicAdd(&st->n_union, (uint32_t)__popc(m));
-      slot = __shfl_sync(0xffffffffu, slot, 0);
-      if (take) surv[slot + __popc(m & lanemask_lt())] = surv_key(ordered_key(v), t);
-    }
+    const uint32_t cnt = (uint32_t)__popc(take);
+    const uint32_t incl = block_scan_incl<kThreads>(cnt, wt);
+    if (threadIdx.x == kThreads - 1) slot0 = incl ? atomicAdd(&st->n_union, incl) : 0u;
+    __syncthreads();
+    uint32_t slot = slot0 + incl - cnt;
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+      if (take & (1u << j)) surv[slot++] = surv_key(ordered_key(v[j]), base + j * kThreads + (int)threadIdx.x);
+    __syncthreads();
   }
 }
 
@@ -450,6 +463,7 @@ cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* sco
   a.L_max = pl.L_max;
   a.k = pl.k;
   a.chunk = pl.chunk;
+  a.hist_rep = pl.hist_rep;
   const dim3 grid(pl.nchunk, pl.R), block(kThreads);
   cudaError_t e;
   if (!minmax_done && (e = launch_pdl(topk_minmax_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
