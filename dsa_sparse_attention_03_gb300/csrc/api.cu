@@ -86,14 +86,14 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   P.R = p->R; P.B = p->B; P.H_i = p->H_i; P.D_i = p->D_i; P.H_q = p->H_q;
   P.D_k = p->D_k; P.D_v = p->D_v; P.k = p->k; P.L_max = p->L_max; P.flags = p->flags;
 
-  // Top-k: aim for a few CTAs per SM over all rows, 1K..64K positions each.
+  // Top-k: about one chunk of 1K..64K positions per CTA of the persistent grid.
   const int64_t work = int64_t(p->L_max) * (p->R > 0 ? p->R : 1);
   int chunk = 1024;
-  while (chunk < 65536 && int64_t(chunk) * 600 < work) chunk <<= 1;
+  while (chunk < 65536 && int64_t(chunk) * 160 < work) chunk <<= 1;
   P.chunk = chunk;
   P.nchunk = p->L_max > 0 ? (p->L_max + chunk - 1) / chunk : 1;
-  // Hundreds of CTAs adding into one row's 2048 bins serialise on the few hot
-  // bins' L2 lines; CTA c adds into copy c % hist_rep instead.
+  // Many chunks adding into one row's 2048 bins would serialise on the hot
+  // bins' L2 lines; chunk c adds into copy c % hist_rep instead.
   P.hist_rep = P.nchunk >= 256 ? 8 : (P.nchunk >= 64 ? 4 : 1);
 
   // Attention: split the k selected positions so that all rows together give

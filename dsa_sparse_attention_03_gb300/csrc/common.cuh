@@ -28,7 +28,7 @@ struct RowState {
   uint32_t n_union;    // survivor slot counter
   uint32_t mode;       // fast / take all / empty / exact fallback
   uint32_t n_take;     // min(k, row_len)
-  uint32_t arrive[8];  // last-CTA counters
+  uint32_t spare[8];
 };
 static_assert(sizeof(RowState) == 64, "RowState is 64 bytes");
 
@@ -78,6 +78,30 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// The same with the cooperative attribute as well: every CTA of the grid is
+// resident at once (the launch fails otherwise), so CTAs may wait on one
+// another at grid barriers.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Words of the 256-byte status block: [0] device status bits; from
+// kBarrierWord on, grid barrier counters (zeroed with the block).
+constexpr int kBarrierWord = 16;
 
 // Per-row running max of the ordered keys and of their complements (= ~min),
 // merged into RowState.umax / uminv by the indexers' epilogues (one warp).

@@ -4,39 +4,43 @@
 // ever larger candidate lists with parallel scans that narrow the candidates,
 // a sort of the small surviving list, and the original exact algorithm for the
 // ambiguous cases -- keeping the same positions in the same order.  Here, with
-// u = s ^ 0x80000000 the order-preserving unsigned key of a score s:
+// u = s ^ 0x80000000 the order-preserving unsigned key of a score s, one
+// persistent kernel over a co-resident (cooperatively launched) grid runs the
+// phases, separated by bounded grid barriers:
 //
-//   hist    one scan: a histogram of 2048 equal-width bins over the row's key
-//           range [umin, umax] (merged by the indexer, or by a min/max scan
-//           for a standalone call); bin(u) = (u - umin) >> shift with the
-//           smallest shift that fits.  The row's last CTA finds the threshold
-//           bin b*: fewer than k positions lie above it, at least k at or
-//           above it.
-//   select  every position whose code is >= b* joins the row's survivor list
-//           (unordered slots): the n_above sure winners plus the bucket's
-//           candidates, a few thousand positions at long context.
+//   range   (standalone calls only) the row's key range [umin, umax]; a
+//           decode step has it already, merged by the indexer's epilogue.
+//   hist    a histogram of 2048 equal-width bins over [umin, umax]:
+//           bin(u) = (u - umin) >> shift with the smallest shift that fits.
+//           Each chunk of a row is binned in shared memory and added into
+//           one of the row's hist_rep global copies.
+//   select  each CTA sums the copies of the rows it serves and finds the
+//           threshold bin b*: fewer than k positions lie above it, at least
+//           k at or above it.  Every position whose bin is >= b* joins the
+//           row's survivor list (unordered slots): the n_above sure winners
+//           plus the bin's candidates, a few thousand at long context.
 //   rank    each survivor's rank is the number of survivors with a larger
 //           64-bit key (u << 32 | ~position).  Keys are unique, so the ranks
 //           are a permutation and sort by (score desc, position asc); a
-//           survivor with rank < k is selected and written at idx[rank].
+//           survivor with rank < k is written at idx[rank].
 //   exact fallback  when the survivor list would exceed kCapFast (heavy ties
-//           at the threshold), one CTA per row resolves it exactly: the
+//           at the threshold), one CTA resolves the row exactly: the
 //           candidates' key range, radix passes to the exact k-th key T,
 //           every key > T plus the lowest-index positions with key == T in
 //           index order, then a bitonic sort.
 // A row with row_len <= k selects every position; an empty row selects none.
-// Nothing here waits on another CTA: cross-CTA steps use the last-arriving
-// CTA of a row (fence + counter), and kernel boundaries.
 #include "common.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kRankThreads = 512;
-constexpr int kRankPerBlock = 64;                          // survivors ranked per CTA
-constexpr int kRankLanes = kRankThreads / kRankPerBlock;   // threads per survivor
+constexpr int kThreads = 512;
+constexpr int kRankSlice = 32;                             // survivors ranked per work unit
+constexpr int kRankLanes = kThreads / kRankSlice;          // threads per survivor
+constexpr int kRankSlices = kCapFast / kRankSlice;         // units per row (also covers idx[0, k))
+static_assert(kRankSlices * kRankSlice >= kMaxK, "rank units must cover idx");
 constexpr int kRadixBits = 11;
+constexpr uint64_t kGridWaitNs = 2000000000ull;            // grid barrier limit (2 s)
 
 enum Mode : uint32_t { kFast = 0, kAll = 1, kEmpty = 2, kExact = 3 };
 
@@ -48,8 +52,10 @@ struct TopkArgs {
   RowState* state;
   uint32_t* hist;      // [R, hist_rep, kBuckets]
   uint64_t* surv;      // [R, kCapFast] survivor keys
+  uint32_t* status;    // device status word
+  uint32_t* bar;       // grid barrier counters (zeroed with the status block)
   int64_t L_max;
-  int k, chunk, hist_rep;
+  int R, k, chunk, nchunk, hist_rep, range;
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -105,17 +111,6 @@ __device__ __forceinline__ int key_pos(uint64_t key) {
 template <typename T>
 __device__ __forceinline__ T ld_volatile(const T* p) {
   return *reinterpret_cast<const volatile T*>(p);
-}
-
-// True in every thread of the CTA that arrives last at counter `c`.
-__device__ bool last_arrival(uint32_t* c, uint32_t expected) {
-  __shared__ int is_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(c, 1u) == expected - 1);
-  __syncthreads();
-  if (is_last) __threadfence();
-  return is_last != 0;
 }
 
 // Block-wide inclusive scan in thread order (NT threads).
@@ -174,139 +169,12 @@ __device__ void find_crossing(const uint32_t* h, int nbins, uint32_t need, uint3
   __syncthreads();
 }
 
-// ------------------------------------------------------------------ minmax
-
-// Standalone dsa_topk only: the row's key range (a decode step merges it in
-// the indexer's epilogue).
-__global__ void __launch_bounds__(kThreads) topk_minmax_kernel(TopkArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int r = blockIdx.y;
-  const int len = a.row_len[r];
-  const int start = blockIdx.x * a.chunk;
-  const int end = min(start + a.chunk, len);
-  uint32_t umax = 0, uminv = 0;
-  scan_row<kThreads>(a.scores + (int64_t)r * a.L_max, start, end, [&](int32_t v, int) {
-    const uint32_t u = ordered_key(v);
-    umax = max(umax, u);
-    uminv = max(uminv, ~u);
-  });
-  __shared__ uint32_t smax[kThreads / 32], sminv[kThreads / 32];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, o));
-    uminv = max(uminv, __shfl_xor_sync(0xffffffffu, uminv, o));
-  }
-  if ((threadIdx.x & 31) == 0) { smax[threadIdx.x >> 5] = umax; sminv[threadIdx.x >> 5] = uminv; }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int i = 1; i < kThreads / 32; ++i) { umax = max(umax, smax[i]); uminv = max(uminv, sminv[i]); }
-    if (umax) atomicMax(&a.state[r].umax, umax);
-    if (uminv) atomicMax(&a.state[r].uminv, uminv);
-  }
-}
-
-// ------------------------------------------------------------------ hist
-
-__global__ void __launch_bounds__(kThreads) topk_hist_kernel(TopkArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ uint32_t h[kBuckets];
-  __shared__ uint32_t res[2];
-  const int r = blockIdx.y;
-  const int len = a.row_len[r];
-  for (int i = threadIdx.x; i < kBuckets; i += kThreads) h[i] = 0;
-  __syncthreads();
-  const int start = blockIdx.x * a.chunk;
-  const int end = min(start + a.chunk, len);
-  RowState* st = a.state + r;
-  const Bins bin(st);
-  if (len > a.k)
-    scan_row<kThreads>(a.scores + (int64_t)r * a.L_max, start, end,
-                       [&](int32_t v, int) { atomicAdd(&h[bin(ordered_key(v))], 1u); });
-  __syncthreads();
-  uint32_t* gh = a.hist + (size_t)r * a.hist_rep * kBuckets;
-  if (len > a.k) {
-    uint32_t* mine = gh + (size_t)(blockIdx.x % a.hist_rep) * kBuckets;
-    for (int i = threadIdx.x; i < kBuckets; i += kThreads)
-      if (h[i]) atomicAdd(&mine[i], h[i]);
-  }
-
-  if (!last_arrival(&st->arrive[0], gridDim.x)) return;
-  // Last CTA of the row: pick the mode and the threshold bucket.
-  if (len <= a.k) {
-    if (threadIdx.x == 0) {
-      st->mode = len <= 0 ? kEmpty : kAll;
-      st->n_take = (uint32_t)max(len, 0);
-      st->bstar = 0;
-    }
-    return;
-  }
-  for (int i = threadIdx.x; i < kBuckets; i += kThreads) {
-    uint32_t c = 0;
-    for (int j = 0; j < a.hist_rep; ++j) c += ld_volatile(&gh[(size_t)j * kBuckets + i]);
-    h[i] = c;
-  }
-  __syncthreads();
-  find_crossing<kThreads>(h, kBuckets, (uint32_t)a.k, res);
-  if (threadIdx.x == 0) {
-    const uint32_t b = res[0], above = res[1];
-    st->bstar = b;
-    st->n_above = above;
-    st->cand = h[b];
-    st->n_take = (uint32_t)a.k;
-    st->mode = (above + h[b] <= (uint32_t)kCapFast) ? kFast : kExact;
-  }
-}
-
-// ------------------------------------------------------------------ select
-
-__global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int r = blockIdx.y;
-  RowState* st = a.state + r;
-  const uint32_t mode = st->mode;
-  if (mode != kFast && mode != kAll) return;
-  const uint32_t bstar = st->bstar;
-  const Bins bin(st);
-  const int len = a.row_len[r];
-  const int start = blockIdx.x * a.chunk;
-  const int end = min(start + a.chunk, len);
-  const int32_t* s = a.scores + (int64_t)r * a.L_max;
-  uint64_t* surv = a.surv + (size_t)r * kCapFast;
-  // Four positions per thread per sweep; the CTA claims its slots with one
-  // atomic (hundreds of per-warp atomics on n_union would serialise).
-  constexpr int U = 4;
-  __shared__ uint32_t wt[kThreads / 32];
-  __shared__ uint32_t slot0;
-  for (int base = start; base < end; base += U * kThreads) {
-    int32_t v[U];
-    uint32_t take = 0;
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const int t = base + j * kThreads + (int)threadIdx.x;
-      v[j] = t < end ? s[t] : 0;
-      if (t < end && (mode == kAll || bin(ordered_key(v[j])) >= bstar)) take |= 1u << j;
-    }
-    const uint32_t cnt = (uint32_t)__popc(take);
-    const uint32_t incl = block_scan_incl<kThreads>(cnt, wt);
-    if (threadIdx.x == kThreads - 1) slot0 = incl ? atomicAdd(&st->n_union, incl) : 0u;
-    __syncthreads();
-    uint32_t slot = slot0 + incl - cnt;
-#pragma unroll
-    for (int j = 0; j < U; ++j)
-      if (take & (1u << j)) surv[slot++] = surv_key(ordered_key(v[j]), base + j * kThreads + (int)threadIdx.x);
-    __syncthreads();
-  }
-}
-
 // ------------------------------------------------------------------ exact fallback
 
 // One CTA resolves a row exactly: the candidates are the positions in bucket
 // b*; k_rem = k - n_above of them are taken.
 __device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys) {
-  constexpr int NT = kRankThreads;
+  constexpr int NT = kThreads;
   __shared__ uint32_t h[1 << kRadixBits];
   __shared__ uint32_t tmp[NT / 32];
   __shared__ uint32_t res[2];
@@ -411,41 +279,231 @@ __device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys
   for (int j = threadIdx.x; j < a.k; j += NT) idx[j] = key_pos(keys[j]);
 }
 
-// ------------------------------------------------------------------ rank
+// ------------------------------------------------------------------ the kernel
 
-__global__ void __launch_bounds__(kRankThreads) topk_rank_kernel(TopkArgs a) {
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Barrier over the whole grid (co-resident by the cooperative launch): the
+// CTA's writes are published before it arrives at counter c, and every later
+// read sees the other CTAs' writes.  Bounded: after kGridWaitNs the CTA raises
+// DSA_DEVICE_TIMEOUT and returns false (the caller then exits).
+__device__ bool grid_barrier(uint32_t* c, uint32_t* status) {
+  __shared__ int ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(c, 1u);
+    int good = 1;
+    const uint64_t t0 = gtimer();
+    while (ld_acquire(c) < gridDim.x) {
+      if (gtimer() - t0 > kGridWaitNs) {
+        raise_status(status, DSA_DEVICE_TIMEOUT);
+        good = 0;
+        break;
+      }
+    }
+    __threadfence();
+    ok = good;
+  }
+  __syncthreads();
+  return ok != 0;
+}
+
+// The selection parameters of row r, from its merged histogram (every thread
+// gets the same values).  h: kBuckets words of shared memory.
+struct RowPick {
+  uint32_t mode, bstar, above, cand, n_take;
+};
+__device__ RowPick row_pick(const TopkArgs& a, int r, uint32_t* h, uint32_t* res) {
+  RowPick p;
+  const int len = a.row_len[r];
+  if (len <= a.k) {
+    p.mode = len <= 0 ? kEmpty : kAll;
+    p.n_take = (uint32_t)max(len, 0);
+    p.bstar = p.above = p.cand = 0;
+    return p;
+  }
+  const uint32_t* gh = a.hist + (size_t)r * a.hist_rep * kBuckets;
+  __syncthreads();   // h may still be read by the previous pick
+  for (int i = threadIdx.x; i < kBuckets; i += kThreads) {
+    uint32_t c = 0;
+    for (int j = 0; j < a.hist_rep; ++j) c += gh[(size_t)j * kBuckets + i];
+    h[i] = c;
+  }
+  __syncthreads();
+  find_crossing<kThreads>(h, kBuckets, (uint32_t)a.k, res);
+  p.bstar = res[0];
+  p.above = res[1];
+  p.cand = h[p.bstar];
+  p.n_take = (uint32_t)a.k;
+  p.mode = (p.above + p.cand <= (uint32_t)kCapFast) ? kFast : kExact;
+  return p;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
+  extern __shared__ uint64_t keys[];   // [max(kCapFast, pow2 >= k)]: ranks / exact fallback
+  __shared__ uint32_t h[kBuckets];
+  __shared__ uint32_t res[2];
+  __shared__ uint32_t wt[kThreads / 32];
+  __shared__ uint32_t slot0;
   pdl_wait();
   pdl_trigger();
-  extern __shared__ uint64_t keys[];   // [max(kCapFast, pow2 >= k)]
-  const int r = blockIdx.y;
-  RowState* st = a.state + r;
-  const uint32_t mode = st->mode;
-  const int n_take = mode == kEmpty ? 0 : (int)st->n_take;
-  int32_t* idx = a.idx + (size_t)r * a.k;
-  if (blockIdx.x == 0 && threadIdx.x == 0 && a.nsel) a.nsel[r] = n_take;
-  if (mode == kExact) {
-    if (blockIdx.x == 0) exact_row(a, st, r, keys);
-    return;
+  const int nunits = a.R * a.nchunk;
+  int nb = 0;
+
+  // ---- range (standalone call): the row's max key and max complemented key.
+  if (a.range) {
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+      const int r = u / a.nchunk, c = u % a.nchunk;
+      const int len = a.row_len[r];
+      const int start = c * a.chunk, end = min(start + a.chunk, len);
+      uint32_t umax = 0, uminv = 0;
+      scan_row<kThreads>(a.scores + (int64_t)r * a.L_max, start, end, [&](int32_t v, int) {
+        const uint32_t x = ordered_key(v);
+        umax = max(umax, x);
+        uminv = max(uminv, ~x);
+      });
+      umax = block_reduce_max<kThreads>(umax, wt);
+      uminv = block_reduce_max<kThreads>(uminv, wt);
+      if (threadIdx.x == 0) {
+        if (umax) atomicMax(&a.state[r].umax, umax);
+        if (uminv) atomicMax(&a.state[r].uminv, uminv);
+      }
+    }
+    if (!grid_barrier(a.bar + nb++, a.status)) return;
   }
-  if (threadIdx.x < kRankPerBlock) {
-    const int p = blockIdx.x * kRankPerBlock + threadIdx.x;
-    if (p >= n_take && p < a.k) idx[p] = -1;
+
+  // ---- hist
+  for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+    const int r = u / a.nchunk, c = u % a.nchunk;
+    const int len = a.row_len[r];
+    const int start = c * a.chunk, end = min(start + a.chunk, len);
+    if (len <= a.k || start >= end) continue;
+    for (int i = threadIdx.x; i < kBuckets; i += kThreads) h[i] = 0;
+    __syncthreads();
+    const Bins bin(a.state + r);
+    scan_row<kThreads>(a.scores + (int64_t)r * a.L_max, start, end,
+                       [&](int32_t v, int) { atomicAdd(&h[bin(ordered_key(v))], 1u); });
+    __syncthreads();
+    uint32_t* mine = a.hist + ((size_t)r * a.hist_rep + (size_t)(c % a.hist_rep)) * kBuckets;
+    for (int i = threadIdx.x; i < kBuckets; i += kThreads)
+      if (h[i]) atomicAdd(&mine[i], h[i]);
+    __syncthreads();
   }
-  if (mode == kEmpty) return;
-  const int U = (int)st->n_union;
-  if (blockIdx.x * kRankPerBlock >= U) return;
-  const uint64_t* surv = a.surv + (size_t)r * kCapFast;
-  for (int i = threadIdx.x; i < U; i += kRankThreads) keys[i] = surv[i];
-  __syncthreads();
-  const int e = blockIdx.x * kRankPerBlock + threadIdx.x / kRankLanes;
-  const int part = threadIdx.x % kRankLanes;
-  const uint64_t key = e < U ? keys[e] : ~0ull;
-  uint32_t rank = 0;
-  if (e < U)
-    for (int j = part; j < U; j += kRankLanes) rank += keys[j] > key;
+  if (!grid_barrier(a.bar + nb++, a.status)) return;
+
+  // ---- select
+  {
+    int cur = -1;
+    RowPick pk;
+    pk.mode = kEmpty;
+    pk.bstar = 0;
+    constexpr int U = 4;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+      const int r = u / a.nchunk, c = u % a.nchunk;
+      RowState* st = a.state + r;
+      const int len = a.row_len[r];
+      const int start = c * a.chunk, end = min(start + a.chunk, len);
+      const int32_t* s = a.scores + (int64_t)r * a.L_max;
+      const Bins bin(st);
+      // The first sweep's scores are loaded before the threshold is known.
+      int32_t v[U];
 #pragma unroll
-  for (int o = kRankLanes / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-  if (e < U && part == 0 && rank < (uint32_t)n_take) idx[rank] = key_pos(key);
+      for (int j = 0; j < U; ++j) {
+        const int t = start + j * kThreads + (int)threadIdx.x;
+        v[j] = t < end ? s[t] : 0;
+      }
+      if (r != cur) {
+        pk = row_pick(a, r, h, res);
+        cur = r;
+      }
+      if (c == 0 && threadIdx.x == 0) {
+        st->mode = pk.mode;
+        st->bstar = pk.bstar;
+        st->n_above = pk.above;
+        st->cand = pk.cand;
+        st->n_take = pk.n_take;
+      }
+      if (pk.mode != kFast && pk.mode != kAll) continue;
+      uint64_t* surv = a.surv + (size_t)r * kCapFast;
+      // U positions per thread per sweep; the CTA claims its slots with one
+      // atomic (per-warp atomics on n_union would serialise).
+      for (int base = start; base < end; base += U * kThreads) {
+        uint32_t take = 0;
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const int t = base + j * kThreads + (int)threadIdx.x;
+          if (base != start) v[j] = t < end ? s[t] : 0;
+          if (t < end && (pk.mode == kAll || bin(ordered_key(v[j])) >= pk.bstar)) take |= 1u << j;
+        }
+        const uint32_t cnt = (uint32_t)__popc(take);
+        const uint32_t incl = block_scan_incl<kThreads>(cnt, wt);
+        if (threadIdx.x == kThreads - 1) slot0 = incl ? atomicAdd(&st->n_union, incl) : 0u;
+        __syncthreads();
+        uint32_t slot = slot0 + incl - cnt;
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+          if (take & (1u << j))
+            surv[slot++] = surv_key(ordered_key(v[j]), base + j * kThreads + (int)threadIdx.x);
+        __syncthreads();
+      }
+    }
+  }
+  if (!grid_barrier(a.bar + nb++, a.status)) return;
+
+  // ---- rank: units (row, slice of kRankSlice survivors), contiguous per CTA so
+  // that a CTA loads each row's survivor keys once.
+  const int64_t nr = (int64_t)a.R * kRankSlices;
+  const int u0 = (int)(nr * blockIdx.x / gridDim.x), u1 = (int)(nr * (blockIdx.x + 1) / gridDim.x);
+  int loaded = -1;
+  for (int u = u0; u < u1; ++u) {
+    const int r = u / kRankSlices, sl = u % kRankSlices;
+    RowState* st = a.state + r;
+    const uint32_t mode = st->mode;
+    const int n_take = mode == kEmpty ? 0 : (int)st->n_take;
+    int32_t* idx = a.idx + (size_t)r * a.k;
+    if (sl == 0 && threadIdx.x == 0 && a.nsel) a.nsel[r] = n_take;
+    if (mode == kExact) {
+      if (sl == 0) {
+        exact_row(a, st, r, keys);
+        loaded = -1;
+      }
+      continue;
+    }
+    if (threadIdx.x < kRankSlice) {
+      const int p = sl * kRankSlice + threadIdx.x;
+      if (p >= n_take && p < a.k) idx[p] = -1;
+    }
+    if (mode == kEmpty) continue;
+    const int U = (int)st->n_union;
+    if (sl * kRankSlice >= U) continue;
+    if (loaded != r) {
+      __syncthreads();
+      const uint64_t* surv = a.surv + (size_t)r * kCapFast;
+      for (int i = threadIdx.x; i < U; i += kThreads) keys[i] = surv[i];
+      __syncthreads();
+      loaded = r;
+    }
+    const int e = sl * kRankSlice + (int)threadIdx.x / kRankLanes;
+    const int part = (int)threadIdx.x % kRankLanes;
+    const uint64_t key = e < U ? keys[e] : ~0ull;
+    uint32_t rank = 0;
+    if (e < U)
+      for (int j = part; j < U; j += kRankLanes) rank += keys[j] > key;
+#pragma unroll
+    for (int o = kRankLanes / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (e < U && part == 0 && rank < (uint32_t)n_take) idx[rank] = key_pos(key);
+  }
 }
 
 }  // namespace
@@ -460,23 +518,31 @@ cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* sco
   a.state = reinterpret_cast<RowState*>(ws + pl.off_state);
   a.hist = reinterpret_cast<uint32_t*>(ws + pl.off_hist);
   a.surv = reinterpret_cast<uint64_t*>(ws + pl.off_surv);
+  a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
+  a.bar = a.status + kBarrierWord;
   a.L_max = pl.L_max;
+  a.R = pl.R;
   a.k = pl.k;
   a.chunk = pl.chunk;
+  a.nchunk = pl.nchunk;
   a.hist_rep = pl.hist_rep;
-  const dim3 grid(pl.nchunk, pl.R), block(kThreads);
-  cudaError_t e;
-  if (!minmax_done && (e = launch_pdl(topk_minmax_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
-  if ((e = launch_pdl(topk_hist_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
-  if ((e = launch_pdl(topk_select_kernel, grid, block, 0, st, a)) != cudaSuccess) return e;
+  a.range = minmax_done ? 0 : 1;
   int n = 1;
   while (n < pl.k) n <<= 1;
   const size_t smem = (size_t)(n > kCapFast ? n : kCapFast) * 8;
-  e = cudaFuncSetAttribute(topk_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int span = (pl.k > kCapFast ? pl.k : kCapFast);
-  const dim3 rgrid((span + kRankPerBlock - 1) / kRankPerBlock, pl.R);
-  return launch_pdl(topk_rank_kernel, rgrid, dim3(kRankThreads), smem, st, a);
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel, kThreads, smem)) != cudaSuccess)
+    return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // One CTA per SM: enough for every phase, and always co-resident.
+  int grid = sms;
+  const int most = pl.R * (pl.nchunk > kRankSlices ? pl.nchunk : kRankSlices);
+  if (grid > most) grid = most;
+  return launch_coop(topk_kernel, dim3(grid), dim3(kThreads), smem, st, a);
 }
 
 }  // namespace dsa
