@@ -200,8 +200,8 @@ def upload_inputs(inp, device="cuda", indexer="auto", relu=True, qk_abs_max=0, w
     return prob, t
 
 
-# Kernels one dsa_decode_step enqueues: indexer 1, top-k 1, attention 2.
-KERNELS_PER_DECODE_STEP = 4
+# Kernels one dsa_decode_step enqueues: indexer 1, top-k 1, attention 1.
+KERNELS_PER_DECODE_STEP = 3
 
 
 def dsa_indexer_kind(prob: Problem) -> int:

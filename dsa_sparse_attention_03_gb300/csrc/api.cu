@@ -96,14 +96,6 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   // bins' L2 lines; chunk c adds into copy c % hist_rep instead.
   P.hist_rep = P.nchunk >= 256 ? 8 : (P.nchunk >= 64 ? 4 : 1);
 
-  // Attention: split the k selected positions so that all rows together give
-  // a few hundred CTAs, each over whole 64-position tiles.
-  const int tiles = (p->k + kAttnRows - 1) / kAttnRows;
-  const int hgroups = (p->H_q > 0 ? p->H_q + kAttnHeads - 1 : kAttnHeads) / kAttnHeads;
-  int per = (p->R > 0) ? 600 / (p->R * hgroups) : 1;
-  if (per < 1) per = 1;
-  P.nsplit = per < tiles ? per : tiles;
-
   const size_t R = size_t(p->R);
   size_t off = 0;
   P.off_status = off; off += 256;
@@ -112,10 +104,6 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   P.zero_end = off;
   P.off_surv = off; off = align_up(off + R * size_t(kCapFast) * 8, 256);
   P.off_scores = off; off = align_up(off + R * size_t(p->L_max) * 4, 256);
-  const int hq = p->H_q > 0 ? p->H_q : 0;
-  const int dv = p->D_v > 0 ? p->D_v : 0;
-  P.off_part = off; off = align_up(off + R * size_t(P.nsplit) * hq * dv * 4, 256);
-  P.off_ml = off; off = align_up(off + R * size_t(P.nsplit) * hq * 2 * 4, 256);
   P.total = off;
   return DSA_OK;
 }

@@ -1,20 +1,25 @@
-// Sparse MLA attention over the selected latent rows, split along the selected
-// positions, then a fixed-order log-sum-exp merge of the splits.
+// Sparse MLA attention over the selected latent rows: the positions are split
+// over the CTAs of one thread-block cluster, whose partial results are merged
+// through distributed shared memory.
 //
 // For query row r and head h ("ds4 glm53-m3ultra", page 1: attention over the
 // ~2048 selected positions only; latent cache of "glm53-tensorfold-spark",
 // page 4: key = the whole D_k-wide latent row, value = its first D_v columns):
 //   z_j = scale * q[r,h,:] . kv[idx_j, :],  o[h,:] = sum_j softmax(z)_j kv[idx_j, :D_v]
 //
-// attn_split_kernel  grid (split, head group of 16, row), 4 warps.  Per tile of
-//   64 selected positions: gather the rows (16-byte cp.async, whole rows, as the
-//   front-axis gather of "GLM-5.3-Flash-Alis-MLX-4bit", page 3), S = Q K^T and
-//   O += P V with bf16 mma.sync (fp32 accumulation), online softmax in fp32
-//   (log2 domain).  Writes unnormalised O, the running max m and sum l.
-// attn_combine_kernel  grid (head, row): merges the splits in split order and
-//   rounds to bf16 (nearest even).
+// attn_cluster_kernel  grid (C, head group of 16, row), cluster (C, 1, 1), 4
+//   warps.  CTA x of the cluster takes the tiles x, x + C, ... of 64 selected
+//   positions: it gathers the rows (one bulk copy per whole row, as the
+//   front-axis gather of "GLM-5.3-Flash-Alis-MLX-4bit", page 3; the next tile's
+//   gather overlaps this tile's math), computes S = Q K^T and O += P V with
+//   bf16 mma.sync (fp32 accumulation) and an online softmax in fp32 (log2
+//   domain).  Each CTA leaves its unnormalised O, running max m and sum l in
+//   shared memory; after a cluster barrier CTA x merges columns
+//   [x D_v / C, (x + 1) D_v / C) of all C partials in CTA order and rounds to
+//   bf16 (nearest even).  No partial result goes through global memory.
 #include "common.cuh"
 
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -24,6 +29,8 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kPStride = kAttnRows + 8;  // bf16 elements per P row in shared memory
+constexpr int kMaxTiles = 8;             // tiles per CTA (k <= 4096 over >= 8 CTAs)
+namespace cg = cooperative_groups;
 
 struct AttnArgs {
   const uint16_t* q;
@@ -33,12 +40,10 @@ struct AttnArgs {
   const int32_t* row_len;
   const int32_t* idx;
   const int32_t* nsel;
-  float* part;        // [R, nsplit, H_q, D_v]
-  float* ml;          // [R, nsplit, H_q, 2]
   uint16_t* out;      // [R, H_q, D_v]
   float* lse;         // [R, H_q] or null
   uint32_t* status;
-  int B, H_q, D_k, D_v, k, nsplit, tiles_per_split;
+  int B, H_q, D_k, D_v, k;
   int qs, ks;         // shared-memory row strides (elements)
   float scale_log2;
 };
@@ -68,11 +73,37 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// One contiguous row (16-byte aligned, size a multiple of 16) by the bulk-copy engine.
+__device__ __forceinline__ void bulk_row(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+// Bounded wait for the phase of parity `parity` (2 s; then DSA_DEVICE_TIMEOUT).
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+    if (gtimer() - t0 > 2000000000ull) {
+      raise_status(status, DSA_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -91,22 +122,42 @@ __device__ int row_request(const int32_t* row_offsets, int B, int r) {
 
 // NT: output n-tiles (of 8 columns) per warp; the 4 warps cover 32*NT >= D_v columns.
 template <int NT>
-__global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);                          // [16][qs]
-  uint16_t* Ks = Qs + kAttnHeads * a.qs;                                    // [64][ks]
-  uint16_t* Ps = Ks + kAttnRows * a.ks;                                     // [16][kPStride]
+  uint16_t* Kb = Qs + kAttnHeads * a.qs;                                    // [2][64][ks]
+  uint16_t* Ps = Kb + 2 * kAttnRows * a.ks;                                 // [16][kPStride]
   float* red = reinterpret_cast<float*>(Ps + kAttnHeads * kPStride);        // [2][4][16]
-  int* idx_s = reinterpret_cast<int*>(red + 2 * kWarps * kAttnHeads);       // [64]
+  float* mls = red + 2 * kWarps * kAttnHeads;                               // [16][2]: m, l
+  float* mall = mls + 2 * kAttnHeads;                                       // [C][16][2]: every CTA's
+  float* wts = mall + 16 * kAttnHeads * 2;                                  // [C][16]
+  float* invl = wts + 16 * kAttnHeads;                                      // [16]
+  int* idx_s = reinterpret_cast<int*>(invl + kAttnHeads);                  // [kMaxTiles][64]
+  float* Ob = reinterpret_cast<float*>(Kb);   // [16][D_v] partial O, after the tile loop
   __shared__ int req_s;
+  __shared__ __align__(8) uint64_t bars[3];   // queries, K buffer 0, K buffer 1
 
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int x = (int)cluster.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int r = blockIdx.z, h0 = blockIdx.y * kAttnHeads, split = blockIdx.x;
+  const int r = blockIdx.z, h0 = blockIdx.y * kAttnHeads;
 
+  const uint32_t bar_q = smem_u32(&bars[0]);
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   pdl_wait();
   pdl_trigger();
   if (tid == 0) req_s = row_request(a.row_offsets, a.B, r);
+  // This CTA's selected positions (masked below once n is known).
+  const int32_t* idx_row = a.idx + (int64_t)r * a.k;
+  for (int i = tid; i < kMaxTiles * kAttnRows; i += kThreads) {
+    const int p = (x + (i / kAttnRows) * C) * kAttnRows + (i % kAttnRows);
+    idx_s[i] = p < a.k ? idx_row[p] : -1;
+  }
   __syncthreads();
   const int b = req_s;
   const int64_t base = a.offsets[b];
@@ -114,85 +165,118 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
   int n = a.nsel ? a.nsel[r] : min(a.k, a.row_len[r]);
   n = max(0, min(n, a.k));
   const int ntiles = (n + kAttnRows - 1) / kAttnRows;
-  const int t_begin = split * a.tiles_per_split;
-  const int t_end = min(t_begin + a.tiles_per_split, ntiles);
-
-  // Queries of this head group (zero rows past H_q).
-  const int qchunks = a.D_k / 8;
-  for (int i = tid; i < kAttnHeads * qchunks; i += kThreads) {
-    const int hh = i / qchunks, c8 = i % qchunks;
-    uint16_t* dst = Qs + hh * a.qs + c8 * 8;
-    if (h0 + hh < a.H_q)
-      cp_async16(smem_u32(dst), a.q + ((int64_t)r * a.H_q + h0 + hh) * a.D_k + c8 * 8);
-    else
-      *reinterpret_cast<int4*>(dst) = make_int4(0, 0, 0, 0);
+  const int my_tiles = ntiles > x ? (ntiles - x + C - 1) / C : 0;   // <= kMaxTiles
+  for (int i = tid; i < my_tiles * kAttnRows; i += kThreads) {
+    const int p = (x + (i / kAttnRows) * C) * kAttnRows + (i % kAttnRows);
+    int t = idx_s[i];
+    if (p >= n) {
+      t = -1;
+    } else if (t < 0 || t >= L_b) {
+      raise_status(a.status, DSA_DEVICE_BAD_INDEX);
+      t = -1;
+    }
+    idx_s[i] = t;
   }
+
+  __syncthreads();   // idx_s final
+  // Whole rows by the bulk-copy engine, issued by warp 0: queries of this head
+  // group (zero rows past H_q), then per tile its 64 selected latent rows
+  // (zero rows where masked).  Each buffer's barrier counts the bytes.
+  const uint32_t rowb = (uint32_t)a.D_k * 2;
+  if (warp == 0) {
+    const int nq = min(kAttnHeads, a.H_q - h0);
+    if (lane == 0) mbar_expect_tx(bar_q, (uint32_t)nq * rowb);
+    __syncwarp();
+    if (lane < nq)
+      bulk_row(smem_u32(Qs + lane * a.qs), a.q + ((int64_t)r * a.H_q + h0 + lane) * a.D_k, rowb, bar_q);
+    else if (lane < kAttnHeads)
+      for (int c8 = 0; c8 < a.D_k / 8; ++c8) *reinterpret_cast<int4*>(Qs + lane * a.qs + c8 * 8) = make_int4(0, 0, 0, 0);
+  }
+  auto gather = [&](int i) {   // this CTA's tile i into buffer i & 1 (warp 0)
+    uint16_t* Ks = Kb + (i & 1) * kAttnRows * a.ks;
+    const int* ids = idx_s + i * kAttnRows;
+    const uint32_t bar = smem_u32(&bars[1 + (i & 1)]);
+    const int t0 = ids[lane], t1 = ids[lane + 32];
+    const uint32_t nv = __popc(__ballot_sync(0xffffffffu, t0 >= 0)) + __popc(__ballot_sync(0xffffffffu, t1 >= 0));
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier zero fills of this buffer
+    if (lane == 0) mbar_expect_tx(bar, nv * rowb);
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = lane + 32 * h, t = h ? t1 : t0;
+      if (t >= 0)
+        bulk_row(smem_u32(Ks + j * a.ks), a.kv + (base + t) * a.D_k, rowb, bar);
+      else
+        for (int c8 = 0; c8 < a.D_k / 8; ++c8) *reinterpret_cast<int4*>(Ks + j * a.ks + c8 * 8) = make_int4(0, 0, 0, 0);
+    }
+  };
+  if (warp == 0 && my_tiles > 0) gather(0);
+  mbar_wait(bar_q, 0, a.status);
 
   float acc[NT][4];
 #pragma unroll
   for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
   float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
   float l_run[2] = {0.f, 0.f};
-  const int32_t* idx_row = a.idx + (int64_t)r * a.k;
 
-  for (int tile = t_begin; tile < t_end; ++tile) {
-    const int pos0 = tile * kAttnRows;
-    if (tid < kAttnRows) {
-      const int p = pos0 + tid;
-      int t = -1;
-      if (p < n) {
-        t = idx_row[p];
-        if (t < 0 || t >= L_b) {
-          raise_status(a.status, DSA_DEVICE_BAD_INDEX);
-          t = -1;
-        }
-      }
-      idx_s[tid] = t;
-    }
+  for (int i = 0; i < my_tiles; ++i) {
+    if (warp == 0 && i + 1 < my_tiles) gather(i + 1);
+    mbar_wait(smem_u32(&bars[1 + (i & 1)]), (uint32_t)(i >> 1) & 1u, a.status);
     __syncthreads();
-    for (int i = tid; i < kAttnRows * qchunks; i += kThreads) {
-      const int j = i / qchunks, c8 = i % qchunks;
-      uint16_t* dst = Ks + j * a.ks + c8 * 8;
-      const int t = idx_s[j];
-      if (t >= 0)
-        cp_async16(smem_u32(dst), a.kv + (base + t) * a.D_k + c8 * 8);
-      else
-        *reinterpret_cast<int4*>(dst) = make_int4(0, 0, 0, 0);
-    }
-    cp_async_wait_all();
-    __syncthreads();
+    const uint16_t* Ks = Kb + (i & 1) * kAttnRows * a.ks;
+    const int* ids = idx_s + i * kAttnRows;
 
     // S = Q K^T for kv rows [warp*16, warp*16+16).
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     {
+      // Two accumulator pairs (even and odd k-steps) halve the mma dependency chain.
+      float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
       const int brow = warp * 16 + (lane & 7) + (lane >> 4) * 8, bcol = ((lane >> 3) & 1) * 8;
       const uint32_t aaddr = smem_u32(Qs + arow * a.qs + acol);
       const uint32_t baddr = smem_u32(Ks + brow * a.ks + bcol);
-      for (int kk = 0; kk < a.D_k / 16; ++kk) {
+      const int nk = a.D_k / 16;
+      int kk = 0;
+      for (; kk + 1 < nk; kk += 2) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3, e0, e1, e2, e3, f0, f1, f2, f3;
+        ldsm_x4(aaddr + kk * 32, a0, a1, a2, a3);
+        ldsm_x4(baddr + kk * 32, b0, b1, b2, b3);
+        ldsm_x4(aaddr + kk * 32 + 32, e0, e1, e2, e3);
+        ldsm_x4(baddr + kk * 32 + 32, f0, f1, f2, f3);
+        mma16816(s[0], a0, a1, a2, a3, b0, b1);
+        mma16816(s[1], a0, a1, a2, a3, b2, b3);
+        mma16816(s2[0], e0, e1, e2, e3, f0, f1);
+        mma16816(s2[1], e0, e1, e2, e3, f2, f3);
+      }
+      if (kk < nk) {
         uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
         ldsm_x4(aaddr + kk * 32, a0, a1, a2, a3);
         ldsm_x4(baddr + kk * 32, b0, b1, b2, b3);
         mma16816(s[0], a0, a1, a2, a3, b0, b1);
         mma16816(s[1], a0, a1, a2, a3, b2, b3);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s[0][e] += s2[0][e];
+        s[1][e] += s2[1][e];
+      }
     }
     // Online softmax (rows g and g+8 of the head group; columns of this warp).
-    float x[2][4];
+    float xv[2][4];
     float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int col = warp * 16 + nt * 8 + 2 * c + (e & 1);
-        const float v = idx_s[col] >= 0 ? s[nt][e] * a.scale_log2 : -CUDART_INF_F;
-        x[nt][e] = v;
+        const float v = ids[col] >= 0 ? s[nt][e] * a.scale_log2 : -CUDART_INF_F;
+        xv[nt][e] = v;
         mx[e >> 1] = fmaxf(mx[e >> 1], v);
       }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
-      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+    for (int j = 0; j < 2; ++j) {
+      mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 1));
+      mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 2));
     }
     float* red_max = red;
     float* red_sum = red + kWarps * kAttnHeads;
@@ -203,31 +287,31 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
     __syncthreads();
     float m_new[2], alpha[2];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int j = 0; j < 2; ++j) {
       float tm = -CUDART_INF_F;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) tm = fmaxf(tm, red_max[w * kAttnHeads + g + 8 * i]);
-      m_new[i] = fmaxf(m_run[i], tm);
-      alpha[i] = m_new[i] == -CUDART_INF_F ? 1.f : exp2f(m_run[i] - m_new[i]);
+      for (int w = 0; w < kWarps; ++w) tm = fmaxf(tm, red_max[w * kAttnHeads + g + 8 * j]);
+      m_new[j] = fmaxf(m_run[j], tm);
+      alpha[j] = m_new[j] == -CUDART_INF_F ? 1.f : exp2f(m_run[j] - m_new[j]);
     }
     float ps[2] = {0.f, 0.f};
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      float p[4];
+      float pv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float mm = m_new[e >> 1];
-        p[e] = (x[nt][e] == -CUDART_INF_F) ? 0.f : exp2f(x[nt][e] - mm);
-        ps[e >> 1] += p[e];
+        pv[e] = (xv[nt][e] == -CUDART_INF_F) ? 0.f : exp2f(xv[nt][e] - mm);
+        ps[e >> 1] += pv[e];
       }
       const int col = warp * 16 + nt * 8 + 2 * c;
-      *reinterpret_cast<uint32_t*>(Ps + g * kPStride + col) = pack_bf16(p[0], p[1]);
-      *reinterpret_cast<uint32_t*>(Ps + (g + 8) * kPStride + col) = pack_bf16(p[2], p[3]);
+      *reinterpret_cast<uint32_t*>(Ps + g * kPStride + col) = pack_bf16(pv[0], pv[1]);
+      *reinterpret_cast<uint32_t*>(Ps + (g + 8) * kPStride + col) = pack_bf16(pv[2], pv[3]);
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      ps[i] += __shfl_xor_sync(0xffffffffu, ps[i], 1);
-      ps[i] += __shfl_xor_sync(0xffffffffu, ps[i], 2);
+    for (int j = 0; j < 2; ++j) {
+      ps[j] += __shfl_xor_sync(0xffffffffu, ps[j], 1);
+      ps[j] += __shfl_xor_sync(0xffffffffu, ps[j], 2);
     }
     if (c == 0) {
       red_sum[warp * kAttnHeads + g] = ps[0];
@@ -235,12 +319,12 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int j = 0; j < 2; ++j) {
       float ts = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) ts += red_sum[w * kAttnHeads + g + 8 * i];
-      l_run[i] = l_run[i] * alpha[i] + ts;
-      m_run[i] = m_new[i];
+      for (int w = 0; w < kWarps; ++w) ts += red_sum[w * kAttnHeads + g + 8 * j];
+      l_run[j] = l_run[j] * alpha[j] + ts;
+      m_run[j] = m_new[j];
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -254,111 +338,137 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
       const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8, vcol = warp * 8 * NT + (lane >> 4) * 8;
       const uint32_t vaddr = smem_u32(Ks + vrow * a.ks + vcol);
 #pragma unroll
-      for (int ks = 0; ks < kAttnRows / 16; ++ks) {
+      for (int kq = 0; kq < kAttnRows / 16; ++kq) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(paddr + ks * 32, a0, a1, a2, a3);
+        ldsm_x4(paddr + kq * 32, a0, a1, a2, a3);
 #pragma unroll
         for (int n2 = 0; n2 < NT / 2; ++n2) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vaddr + (ks * 16 * a.ks + n2 * 16) * 2, b0, b1, b2, b3);
+          ldsm_x4_t(vaddr + (kq * 16 * a.ks + n2 * 16) * 2, b0, b1, b2, b3);
           mma16816(acc[2 * n2], a0, a1, a2, a3, b0, b1);
           mma16816(acc[2 * n2 + 1], a0, a1, a2, a3, b2, b3);
         }
       }
     }
-    __syncthreads();  // Ks / Ps / idx_s are rewritten by the next tile
+    __syncthreads();  // buffer i & 1, Ps and red are rewritten next
   }
+  __syncthreads();
 
-  cp_async_wait_all();  // an empty split still issued its query copies
-  // Unnormalised partial output of this split.
-  const int64_t prow = ((int64_t)r * a.nsplit + split) * a.H_q;
+  // This CTA's unnormalised partial O, m and l, for the cluster to read.
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int h = h0 + g + 8 * i;
-    if (h >= a.H_q) continue;
-    float* dst = a.part + (prow + h) * a.D_v;
+  for (int j = 0; j < 2; ++j) {
+    float* dst = Ob + (g + 8 * j) * a.D_v;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int col = warp * 8 * NT + nt * 8 + 2 * c;
-      if (col < a.D_v)
-        *reinterpret_cast<float2*>(dst + col) = make_float2(acc[nt][2 * i], acc[nt][2 * i + 1]);
+      if (col < a.D_v) *reinterpret_cast<float2*>(dst + col) = make_float2(acc[nt][2 * j], acc[nt][2 * j + 1]);
     }
-    if (warp == 0 && c == 0)
-      *reinterpret_cast<float2*>(a.ml + (prow + h) * 2) = make_float2(m_run[i], l_run[i]);
+    if (warp == 0 && c == 0) {
+      mls[(g + 8 * j) * 2] = m_run[j];
+      mls[(g + 8 * j) * 2 + 1] = l_run[j];
+    }
   }
-}
+  cluster.sync();
 
-// One CTA per (head, row): warp 0 derives the split weights exp2(m_s - M) and
-// 1/L in parallel; then every thread merges 4 columns over the splits, in
-// split order, and rounds to bf16.
-__global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int h = blockIdx.x, r = blockIdx.y;
-  extern __shared__ float wts[];  // [nsplit]
-  __shared__ float inv_l_s;
-  const int lane = threadIdx.x & 31;
-  const float2* ml = reinterpret_cast<const float2*>(a.ml) + ((int64_t)r * a.nsplit) * a.H_q + h;
-  if (threadIdx.x < 32) {
-    float M = -CUDART_INF_F;
-    for (int s = lane; s < a.nsplit; s += 32) {
-      const float2 v = ml[(int64_t)s * a.H_q];
-      if (v.y > 0.f) M = fmaxf(M, v.x);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-    for (int s = lane; s < a.nsplit; s += 32) {
-      const float2 v = ml[(int64_t)s * a.H_q];
-      const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
-      wts[s] = w;
-      L += w * v.y;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) {
-      inv_l_s = L > 0.f ? 1.f / L : 0.f;
-      if (a.lse) a.lse[(int64_t)r * a.H_q + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
-    }
+  // Merge: weights exp2(m_c - M) per (CTA c, head), then columns of slice x.
+  for (int e = tid; e < C * kAttnHeads; e += kThreads) {   // every CTA's (m, l), one round trip
+    const float2 v = *reinterpret_cast<const float2*>(cluster.map_shared_rank(mls, e / kAttnHeads) +
+                                                      (e % kAttnHeads) * 2);
+    mall[2 * e] = v.x;
+    mall[2 * e + 1] = v.y;
   }
   __syncthreads();
-  const float inv_l = inv_l_s;
-  uint16_t* o = a.out + ((int64_t)r * a.H_q + h) * a.D_v;
-  const float* part = a.part + (((int64_t)r * a.nsplit) * a.H_q + h) * a.D_v;
-  const int64_t sstride = (int64_t)a.H_q * a.D_v;
-  for (int col = threadIdx.x * 4; col < a.D_v; col += blockDim.x * 4) {
-    // Every split wrote its partial (zeros when it saw no position), so the
-    // loads are unconditional and eight of them are kept in flight.
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = 0;
-    for (; s + 8 <= a.nsplit; s += 8) {
-      float4 v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const float4*>(part + (s + j) * sstride + col);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float w = wts[s + j];
-        x.x += w * v[j].x; x.y += w * v[j].y; x.z += w * v[j].z; x.w += w * v[j].w;
-      }
+  if (tid < kAttnHeads) {
+    const int hh = tid;
+    float M = -CUDART_INF_F;
+    for (int cc = 0; cc < C; ++cc)
+      if (mall[2 * (cc * kAttnHeads + hh) + 1] > 0.f) M = fmaxf(M, mall[2 * (cc * kAttnHeads + hh)]);
+    float L = 0.f;
+    for (int cc = 0; cc < C; ++cc) {
+      const float m = mall[2 * (cc * kAttnHeads + hh)], l = mall[2 * (cc * kAttnHeads + hh) + 1];
+      const float w = l > 0.f ? exp2f(m - M) : 0.f;
+      wts[cc * kAttnHeads + hh] = w;
+      L += w * l;
     }
-    for (; s < a.nsplit; ++s) {
-      const float w = wts[s];
-      const float4 v = *reinterpret_cast<const float4*>(part + s * sstride + col);
-      x.x += w * v.x; x.y += w * v.y; x.z += w * v.z; x.w += w * v.w;
-    }
-    uint2 pk;
-    pk.x = pack_bf16(x.x * inv_l, x.y * inv_l);
-    pk.y = pack_bf16(x.z * inv_l, x.w * inv_l);
-    *reinterpret_cast<uint2*>(o + col) = pk;
+    invl[hh] = L > 0.f ? 1.f / L : 0.f;
+    if (a.lse && x == 0 && h0 + hh < a.H_q)
+      a.lse[(int64_t)r * a.H_q + h0 + hh] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
   }
+  __syncthreads();
+  const int cs = a.D_v / C;            // columns of this CTA's slice (even: D_v % 32 == 0, C <= 16)
+  const int npairs = kAttnHeads * (cs / 2);
+  for (int e = tid; e < npairs; e += kThreads) {
+    const int hh = e / (cs / 2), col = x * cs + 2 * (e % (cs / 2));
+    // All C remote loads are issued before the (CTA-ordered) accumulation.
+    float2 v[16];
+#pragma unroll
+    for (int cc = 0; cc < 16; ++cc)
+      if (cc < C)
+        v[cc] = *reinterpret_cast<const float2*>(cluster.map_shared_rank(Ob, cc) + hh * a.D_v + col);
+    float2 o = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int cc = 0; cc < 16; ++cc)
+      if (cc < C) {
+        const float w = wts[cc * kAttnHeads + hh];
+        o.x += w * v[cc].x;
+        o.y += w * v[cc].y;
+      }
+    if (h0 + hh < a.H_q)
+      *reinterpret_cast<uint32_t*>(a.out + ((int64_t)r * a.H_q + h0 + hh) * a.D_v + col) =
+          pack_bf16(o.x * invl[hh], o.y * invl[hh]);
+  }
+  cluster.sync();   // peers may still be reading this CTA's shared memory
 }
 
 template <int NT>
-cudaError_t launch_split(const AttnArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<NT>,
+cudaError_t launch_cluster(const AttnArgs& a, dim3 grid, int C, size_t smem, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<NT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_split_kernel<NT>, grid, dim3(kThreads), smem, st, a);
+  if (C > 8 && (e = cudaFuncSetAttribute(attn_cluster_kernel<NT>,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+    return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<NT>, a);
+}
+
+template <int NT>
+int max_cluster(int smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(16, 1, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 16;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaFuncSetAttribute(attn_cluster_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(attn_cluster_kernel<NT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess)
+    return 8;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<NT>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    return 8;
+  }
+  return 16;
 }
 
 }  // namespace
@@ -369,14 +479,9 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
   AttnArgs a;
   a.q = p.q; a.kv = p.kv; a.offsets = p.offsets; a.row_offsets = p.row_offsets;
   a.row_len = p.row_len; a.idx = idx; a.nsel = nsel;
-  a.part = reinterpret_cast<float*>(ws + pl.off_part);
-  a.ml = reinterpret_cast<float*>(ws + pl.off_ml);
   a.out = out; a.lse = lse;
   a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
   a.B = p.B; a.H_q = p.H_q; a.D_k = p.D_k; a.D_v = p.D_v; a.k = p.k;
-  a.nsplit = pl.nsplit;
-  const int tiles = (p.k + kAttnRows - 1) / kAttnRows;
-  a.tiles_per_split = (tiles + pl.nsplit - 1) / pl.nsplit;
   a.scale_log2 = p.softmax_scale * 1.4426950408889634f;
 
   int NT = 2;
@@ -384,19 +489,33 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
   const int cols = NT * 32;
   a.qs = p.D_k + 8;
   a.ks = (p.D_k > cols ? p.D_k : cols) + 8;
-  const size_t smem = (size_t)kAttnHeads * a.qs * 2 + (size_t)kAttnRows * a.ks * 2 +
+  const size_t kbytes = (size_t)2 * kAttnRows * a.ks * 2;
+  const size_t obytes = (size_t)kAttnHeads * p.D_v * 4;   // partial O, aliased on the K buffers
+  const size_t smem = (size_t)kAttnHeads * a.qs * 2 + (kbytes > obytes ? kbytes : obytes) +
                       (size_t)kAttnHeads * kPStride * 2 + 2 * kWarps * kAttnHeads * 4 +
-                      kAttnRows * 4;
-  const dim3 grid(pl.nsplit, (p.H_q + kAttnHeads - 1) / kAttnHeads, p.R);
-  cudaError_t e;
-  switch (NT) {
-    case 2: e = launch_split<2>(a, grid, smem, st); break;
-    case 4: e = launch_split<4>(a, grid, smem, st); break;
-    case 8: e = launch_split<8>(a, grid, smem, st); break;
-    default: e = launch_split<16>(a, grid, smem, st); break;
+                      2 * kAttnHeads * 4 + 16 * kAttnHeads * 8 + 16 * kAttnHeads * 4 + kAttnHeads * 4 +
+                      (size_t)kMaxTiles * kAttnRows * 4;
+  // Cluster size: enough CTAs that each takes at most kMaxTiles tiles.
+  const int tiles = (p.k + kAttnRows - 1) / kAttnRows;
+  static int cmax[4] = {0, 0, 0, 0};
+  const int nti = NT == 2 ? 0 : NT == 4 ? 1 : NT == 8 ? 2 : 3;
+  int C = 1;
+  while (C < tiles && C < 16) C <<= 1;
+  if (C > 8) {
+    if (!cmax[nti])
+      cmax[nti] = NT == 2 ? max_cluster<2>((int)smem) : NT == 4 ? max_cluster<4>((int)smem)
+                : NT == 8 ? max_cluster<8>((int)smem) : max_cluster<16>((int)smem);
+    if (C > cmax[nti]) C = cmax[nti];
   }
-  if (e != cudaSuccess) return e;
-  return launch_pdl(attn_combine_kernel, dim3(p.H_q, p.R), dim3(128), (size_t)pl.nsplit * 4, st, a);
+  if ((tiles + C - 1) / C > kMaxTiles) return cudaErrorInvalidConfiguration;
+  // a.D_v / C must be even: D_v is a multiple of 32 and C <= 16.
+  const dim3 grid(C, (p.H_q + kAttnHeads - 1) / kAttnHeads, p.R);
+  switch (NT) {
+    case 2: return launch_cluster<2>(a, grid, C, smem, st);
+    case 4: return launch_cluster<4>(a, grid, C, smem, st);
+    case 8: return launch_cluster<8>(a, grid, C, smem, st);
+    default: return launch_cluster<16>(a, grid, C, smem, st);
+  }
 }
 
 }  // namespace dsa

@@ -12,7 +12,7 @@ namespace dsa {
 constexpr int kBucketBits = 11;               // linear bins over the row's key range
 constexpr int kBuckets = 1 << kBucketBits;
 constexpr int kCapFast = 4096;                // survivors ranked directly (else exact fallback)
-constexpr int kAttnRows = 64;                 // selected positions per attention CTA
+constexpr int kAttnRows = 64;                 // selected positions per attention tile
 constexpr int kAttnHeads = 16;                // query heads per attention CTA (mma M)
 constexpr int kMaxB = 4096;
 constexpr int kMaxK = 4096;
@@ -38,9 +38,8 @@ struct Plan {
   int flags;
   int chunk, nchunk;       // top-k: positions per CTA, CTAs per row
   int hist_rep;            // top-k: copies of each row's global histogram
-  int nsplit;              // attention: CTAs along the selected positions
   size_t off_status, off_state, off_hist, zero_end;
-  size_t off_surv, off_scores, off_part, off_ml, total;
+  size_t off_surv, off_scores, total;
 };
 
 // Order-preserving map of int32 onto uint32.
