@@ -46,7 +46,8 @@ INDEXERS = {"auto": DSA_INDEXER_AUTO, "dp4a": DSA_INDEXER_DP4A, "tc": DSA_INDEXE
 # Symbols the header declares (checked by the ABI test).
 EXPORTS = ("dsa_version", "dsa_last_error_string", "dsa_indexer_kind", "dsa_workspace_size",
            "dsa_index_scores",
-           "dsa_topk", "dsa_sparse_attn", "dsa_decode_step", "dsa_read_device_status")
+           "dsa_topk", "dsa_topk_static", "dsa_sparse_attn", "dsa_decode_step",
+           "dsa_read_device_status")
 
 
 class dsa_problem(ctypes.Structure):
@@ -84,6 +85,7 @@ def _load() -> ctypes.CDLL:
     for name, args in (
         ("dsa_index_scores", [P, vp, vp, sz, vp]),
         ("dsa_topk", [P, vp, vp, vp, vp, sz, vp]),
+        ("dsa_topk_static", [P, vp, vp, vp, vp]),
         ("dsa_sparse_attn", [P, vp, vp, vp, vp, vp, sz, vp]),
         ("dsa_decode_step", [P, vp, vp, vp, vp, sz, vp]),
         ("dsa_read_device_status", [vp, vp, ctypes.POINTER(ctypes.c_int32)]),
@@ -236,6 +238,13 @@ def dsa_index_scores(prob: Problem, scores, ws, stream=None) -> None:
 def dsa_topk(prob: Problem, scores, idx, nsel, ws, stream=None) -> None:
     _check(_lib.dsa_topk(ctypes.byref(prob.c), _ptr(scores), _ptr(idx), _ptr(nsel), _ptr(ws),
                          ws.numel(), _stream(stream)))
+
+
+def dsa_topk_static(prob: Problem, scores, idx, nsel, stream=None) -> None:
+    """dsa_topk with the library's fixed 4 MiB scratch instead of a workspace
+    (see include/dsa.h: calls must not overlap)."""
+    _check(_lib.dsa_topk_static(ctypes.byref(prob.c), _ptr(scores), _ptr(idx), _ptr(nsel),
+                                _stream(stream)))
 
 
 def dsa_sparse_attn(prob: Problem, idx, nsel, out, lse, ws, stream=None) -> None:

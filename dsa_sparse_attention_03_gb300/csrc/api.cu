@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -127,7 +128,17 @@ dsa_status run_indexer(const dsa_problem& p, const Plan& pl, int32_t* scores, ch
   return DSA_OK;
 }
 
+// Scratch of dsa_topk_static: the top-k's status block, row state, histograms
+// and survivor lists, for problems whose top-k scratch fits in 4 MiB.
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
 }  // namespace
+
+__device__ __align__(256) unsigned char g_topk_scratch[kStaticScratchBytes];
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -185,6 +196,48 @@ dsa_status dsa_topk(const dsa_problem* p, const int32_t* scores, int32_t* idx, i
   if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
   if (p->R == 0) return DSA_OK;
   e = launch_topk(*p, pl, scores, idx, nsel, static_cast<char*>(ws), st, false);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k");
+  return DSA_OK;
+}
+
+dsa_status dsa_topk_static(const dsa_problem* p, const int32_t* scores, int32_t* idx,
+                           int32_t* nsel, void* stream) {
+  g_err.clear();
+  Plan pl;
+  dsa_status s = make_plan(p, kNeedTopk, &pl);
+  if (s != DSA_OK) return s;
+  const size_t need = pl.off_scores;   // status block, row state, histograms, survivors
+  if (need > kStaticScratchBytes)
+    return fail(DSA_ERR_UNSUPPORTED,
+                "dsa_topk_static: this problem needs %zu bytes of scratch; the static scratch "
+                "holds %zu (use dsa_topk with a workspace)",
+                need, kStaticScratchBytes);
+  if (p->R > 0 && (!idx || (p->L_max > 0 && !scores)))
+    return fail(DSA_ERR_INVALID_ARG, "scores/idx is NULL");
+  if (!aligned(scores, 16)) return fail(DSA_ERR_INVALID_ARG, "scores must be 16-byte aligned");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "current device");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  void* base = nullptr;
+  {
+    // First call on a device: look the scratch up once (no allocation).
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+      e = cudaGetSymbolAddress(&g_static_ptr[dev], g_topk_scratch);
+      if (e != cudaSuccess) {
+        g_static_ptr[dev] = nullptr;
+        return cuda_fail(e, "static scratch address");
+      }
+    }
+    base = g_static_ptr[dev];
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The status block, row state and histograms must start at zero.
+  e = cudaMemsetAsync(base, 0, pl.zero_end, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear static scratch");
+  if (p->R == 0) return DSA_OK;
+  e = launch_topk(*p, pl, scores, idx, nsel, static_cast<char*>(base), st, false);
   if (e != cudaSuccess) return cuda_fail(e, "top-k");
   return DSA_OK;
 }

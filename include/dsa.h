@@ -171,6 +171,36 @@ DSA_API dsa_status dsa_topk(const dsa_problem* p, const int32_t* scores, int32_t
                     int32_t* nsel, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Step 2 without a caller workspace.  The pages have no counterpart: this is
+ * an interface for callers that hold no device allocator where they call the
+ * top-k (a host plugin interface that passes only input and output buffers),
+ * or on a latency-critical path where a cudaMalloc, which may synchronise the
+ * device, is not acceptable.
+ *
+ * Same inputs, outputs and results as dsa_topk.  Its scratch is a 4 MiB array
+ * in the library's own device memory, fixed at load time; nothing is allocated
+ * or freed.  A problem whose top-k scratch (status block, 64 B of row state,
+ * the row histograms and 32 KB of survivor keys per row) exceeds 4 MiB is
+ * rejected with DSA_ERR_UNSUPPORTED and a message giving both sizes; use
+ * dsa_topk with a workspace then.  A row takes 40 KB to 96 KB (1 to 8
+ * histogram copies, more for long rows split over many CTAs), so roughly 40
+ * to 100 rows fit.
+ *
+ * - The first call on each device looks the array's address up
+ *   (cudaGetSymbolAddress) and caches it; make that first call before any
+ *   stream capture begins.
+ * - Every call first clears the scratch's status block, row state and
+ *   histograms (cudaMemsetAsync on `stream`); the rest needs no clearing.
+ * - All calls share the one array: two calls whose executions overlap (on
+ *   different streams, or on different host threads without ordering) race
+ *   and give wrong results.  Order them on one stream.
+ * - Device status bits land in the shared array, not in a caller workspace,
+ *   so dsa_read_device_status cannot report them.
+ */
+DSA_API dsa_status dsa_topk_static(const dsa_problem* p, const int32_t* scores, int32_t* idx,
+                                   int32_t* nsel, void* stream);
+
+/*
  * Step 3, sparse MLA attention over the selected rows only ("ds4
  * glm53-m3ultra", page 1; latent cache of "glm53-tensorfold-spark", page 4).
  * Reads q, kv, offsets, row_offsets, row_len, idx [R, k] and nsel [R] (NULL
