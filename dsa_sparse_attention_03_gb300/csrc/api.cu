@@ -102,9 +102,20 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   P.off_status = off; off += 256;
   P.off_state = off; off = align_up(off + R * sizeof(RowState), 256);
   P.off_hist = off; off = align_up(off + R * size_t(P.hist_rep) * kBuckets * 4, 256);
+  // Attention: clusters of up to 8 CTAs take one 64-position tile per CTA; a
+  // (row, head group) with more tiles uses several clusters, merged through
+  // per-slice partials and arrival counters.
+  const int hgroups = p->H_q > 0 ? (p->H_q + kAttnHeads - 1) / kAttnHeads : 0;
+  const int tiles = (p->k + kAttnRows - 1) / kAttnRows;
+  P.attn_kc_max = (tiles + 7) / 8;
+  P.off_acnt = off; off = align_up(off + R * size_t(hgroups) * 16 * 4, 256);
   P.zero_end = off;
   P.off_surv = off; off = align_up(off + R * size_t(kCapFast) * 8, 256);
   P.off_scores = off; off = align_up(off + R * size_t(p->L_max) * 4, 256);
+  const size_t dv = p->D_v > 0 ? size_t(p->D_v) : 0;
+  P.off_apart = off;
+  if (P.attn_kc_max > 1)
+    off = align_up(off + R * size_t(hgroups) * P.attn_kc_max * (16 * dv + 32 * 16) * 4, 256);
   P.total = off;
   return DSA_OK;
 }
@@ -252,8 +263,8 @@ dsa_status dsa_sparse_attn(const dsa_problem* p, const int32_t* idx, const int32
   if (p->R > 0 && (!idx || !out)) return fail(DSA_ERR_INVALID_ARG, "idx/out is NULL");
   if (!aligned(out, 8)) return fail(DSA_ERR_INVALID_ARG, "out must be 8-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
-  if (e != cudaSuccess) return cuda_fail(e, "clear status");
+  cudaError_t e = cudaMemsetAsync(ws, 0, pl.zero_end, st);   // status word and merge counters
+  if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
   if (p->R == 0) return DSA_OK;
   e = launch_attention(*p, pl, idx, nsel, out, lse, static_cast<char*>(ws), st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention");

@@ -1,22 +1,25 @@
 // Sparse MLA attention over the selected latent rows: the positions are split
-// over the CTAs of one thread-block cluster, whose partial results are merged
-// through distributed shared memory.
+// over the CTAs of thread-block clusters, whose partial results are merged
+// through distributed shared memory, then across clusters.
 //
 // For query row r and head h ("ds4 glm53-m3ultra", page 1: attention over the
 // ~2048 selected positions only; latent cache of "glm53-tensorfold-spark",
 // page 4: key = the whole D_k-wide latent row, value = its first D_v columns):
 //   z_j = scale * q[r,h,:] . kv[idx_j, :],  o[h,:] = sum_j softmax(z)_j kv[idx_j, :D_v]
 //
-// attn_cluster_kernel  grid (C, head group of 16, row), cluster (C, 1, 1), 4
-//   warps.  CTA x of the cluster takes the tiles x, x + C, ... of 64 selected
-//   positions: it gathers the rows (one bulk copy per whole row, as the
-//   front-axis gather of "GLM-5.3-Flash-Alis-MLX-4bit", page 3; the next tile's
-//   gather overlaps this tile's math), computes S = Q K^T and O += P V with
-//   bf16 mma.sync (fp32 accumulation) and an online softmax in fp32 (log2
-//   domain).  Each CTA leaves its unnormalised O, running max m and sum l in
-//   shared memory; after a cluster barrier CTA x merges columns
-//   [x D_v / C, (x + 1) D_v / C) of all C partials in CTA order and rounds to
-//   bf16 (nearest even).  No partial result goes through global memory.
+// attn_cluster_kernel  grid (C * Kc, head group of 16, row), cluster (C, 1, 1)
+//   with C <= 8, 4 warps.  The S = C * Kc CTAs of a (row, head group) split
+//   the selected positions: CTA sp takes the tiles sp, sp + S, ... of 64
+//   positions (one tile at k = 2048).  It gathers the rows (one bulk copy per
+//   whole row, as the front-axis gather of "GLM-5.3-Flash-Alis-MLX-4bit",
+//   page 3), computes S = Q K^T and O += P V with bf16 mma.sync (fp32
+//   accumulation) and an online softmax in fp32 (log2 domain), and leaves its
+//   unnormalised O, running max m and sum l in shared memory.  After a cluster
+//   barrier CTA x merges columns [x D_v / C, (x + 1) D_v / C) of the C partials
+//   in CTA order.  With one cluster that is the bf16 output (round to nearest
+//   even); with Kc > 1 each CTA writes its merged slice with (M, L) to the
+//   workspace, and the last of the Kc CTAs of slice x to arrive (an atomic
+//   counter, no waiting) merges the Kc slices in cluster order.
 #include "common.cuh"
 
 #include <cooperative_groups.h>
@@ -28,6 +31,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
+static_assert(kThreads == kAttnHeads * 8, "merge: eight lanes per head");
 constexpr int kPStride = kAttnRows + 8;  // bf16 elements per P row in shared memory
 constexpr int kMaxTiles = 8;             // tiles per CTA (k <= 4096 over >= 8 CTAs)
 namespace cg = cooperative_groups;
@@ -43,6 +47,9 @@ struct AttnArgs {
   uint16_t* out;      // [R, H_q, D_v]
   float* lse;         // [R, H_q] or null
   uint32_t* status;
+  float* apart;       // [R, head group, Kc, C] x (M[16], L[16], O[16][D_v / C]) when Kc > 1
+  uint32_t* acnt;     // [R, head group, 16] arrivals per column slice (zeroed)
+  int Kc;             // clusters per (row, head group)
   int B, H_q, D_k, D_v, k;
   int qs, ks;         // shared-memory row strides (elements)
   float scale_log2;
@@ -125,28 +132,32 @@ template <int NT>
 __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);                          // [16][qs]
-  uint16_t* Kb = Qs + kAttnHeads * a.qs;                                    // [2][64][ks]
-  uint16_t* Ps = Kb + 2 * kAttnRows * a.ks;                                 // [16][kPStride]
+  uint16_t* Kb = Qs + kAttnHeads * a.qs;                                    // [64][ks]
+  uint16_t* Ps = Kb + kAttnRows * a.ks;                                     // [16][kPStride]
   float* red = reinterpret_cast<float*>(Ps + kAttnHeads * kPStride);        // [2][4][16]
   float* mls = red + 2 * kWarps * kAttnHeads;                               // [16][2]: m, l
   float* mall = mls + 2 * kAttnHeads;                                       // [C][16][2]: every CTA's
   float* wts = mall + 16 * kAttnHeads * 2;                                  // [C][16]
   float* invl = wts + 16 * kAttnHeads;                                      // [16]
-  int* idx_s = reinterpret_cast<int*>(invl + kAttnHeads);                  // [kMaxTiles][64]
+  float* mlc = invl + kAttnHeads;                                           // [2][16]: cluster M, L
+  int* idx_s = reinterpret_cast<int*>(mlc + 2 * kAttnHeads);               // [kMaxTiles][64]
   float* Ob = reinterpret_cast<float*>(Kb);   // [16][D_v] partial O, after the tile loop
-  __shared__ int req_s;
-  __shared__ __align__(8) uint64_t bars[3];   // queries, K buffer 0, K buffer 1
+  __shared__ int req_s, last_s;
+  __shared__ __align__(8) uint64_t bars[2];   // queries, K buffer
 
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int x = (int)cluster.block_rank();
+  const int kc = (int)blockIdx.x / C;        // cluster within (row, head group)
+  const int S = a.Kc * C;                    // position splits of the row
+  const int sp = kc * C + x;                 // this CTA's split: tiles sp, sp + S, ...
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int r = blockIdx.z, h0 = blockIdx.y * kAttnHeads;
 
   const uint32_t bar_q = smem_u32(&bars[0]);
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars[i]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   pdl_wait();
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   // This CTA's selected positions (masked below once n is known).
   const int32_t* idx_row = a.idx + (int64_t)r * a.k;
   for (int i = tid; i < kMaxTiles * kAttnRows; i += kThreads) {
-    const int p = (x + (i / kAttnRows) * C) * kAttnRows + (i % kAttnRows);
+    const int p = (sp + (i / kAttnRows) * S) * kAttnRows + (i % kAttnRows);
     idx_s[i] = p < a.k ? idx_row[p] : -1;
   }
   __syncthreads();
@@ -165,9 +176,9 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   int n = a.nsel ? a.nsel[r] : min(a.k, a.row_len[r]);
   n = max(0, min(n, a.k));
   const int ntiles = (n + kAttnRows - 1) / kAttnRows;
-  const int my_tiles = ntiles > x ? (ntiles - x + C - 1) / C : 0;   // <= kMaxTiles
+  const int my_tiles = ntiles > sp ? (ntiles - sp + S - 1) / S : 0;   // <= kMaxTiles
   for (int i = tid; i < my_tiles * kAttnRows; i += kThreads) {
-    const int p = (x + (i / kAttnRows) * C) * kAttnRows + (i % kAttnRows);
+    const int p = (sp + (i / kAttnRows) * S) * kAttnRows + (i % kAttnRows);
     int t = idx_s[i];
     if (p >= n) {
       t = -1;
@@ -192,10 +203,10 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
     else if (lane < kAttnHeads)
       for (int c8 = 0; c8 < a.D_k / 8; ++c8) *reinterpret_cast<int4*>(Qs + lane * a.qs + c8 * 8) = make_int4(0, 0, 0, 0);
   }
-  auto gather = [&](int i) {   // this CTA's tile i into buffer i & 1 (warp 0)
-    uint16_t* Ks = Kb + (i & 1) * kAttnRows * a.ks;
+  auto gather = [&](int i) {   // this CTA's tile i into the K buffer (warp 0)
+    uint16_t* Ks = Kb;
     const int* ids = idx_s + i * kAttnRows;
-    const uint32_t bar = smem_u32(&bars[1 + (i & 1)]);
+    const uint32_t bar = smem_u32(&bars[1]);
     const int t0 = ids[lane], t1 = ids[lane + 32];
     const uint32_t nv = __popc(__ballot_sync(0xffffffffu, t0 >= 0)) + __popc(__ballot_sync(0xffffffffu, t1 >= 0));
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier zero fills of this buffer
@@ -220,10 +231,10 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   float l_run[2] = {0.f, 0.f};
 
   for (int i = 0; i < my_tiles; ++i) {
-    if (warp == 0 && i + 1 < my_tiles) gather(i + 1);
-    mbar_wait(smem_u32(&bars[1 + (i & 1)]), (uint32_t)(i >> 1) & 1u, a.status);
+    if (warp == 0 && i > 0) gather(i);   // the previous tile's math is done (barrier below)
+    mbar_wait(smem_u32(&bars[1]), (uint32_t)i & 1u, a.status);
     __syncthreads();
-    const uint16_t* Ks = Kb + (i & 1) * kAttnRows * a.ks;
+    const uint16_t* Ks = Kb;
     const int* ids = idx_s + i * kAttnRows;
 
     // S = Q K^T for kv rows [warp*16, warp*16+16).
@@ -350,7 +361,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
         }
       }
     }
-    __syncthreads();  // buffer i & 1, Ps and red are rewritten next
+    __syncthreads();  // the K buffer, Ps and red are rewritten next
   }
   __syncthreads();
 
@@ -371,53 +382,136 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   cluster.sync();
 
   // Merge: weights exp2(m_c - M) per (CTA c, head), then columns of slice x.
-  for (int e = tid; e < C * kAttnHeads; e += kThreads) {   // every CTA's (m, l), one round trip
-    const float2 v = *reinterpret_cast<const float2*>(cluster.map_shared_rank(mls, e / kAttnHeads) +
-                                                      (e % kAttnHeads) * 2);
-    mall[2 * e] = v.x;
-    mall[2 * e + 1] = v.y;
-  }
-  __syncthreads();
-  if (tid < kAttnHeads) {
-    const int hh = tid;
-    float M = -CUDART_INF_F;
-    for (int cc = 0; cc < C; ++cc)
-      if (mall[2 * (cc * kAttnHeads + hh) + 1] > 0.f) M = fmaxf(M, mall[2 * (cc * kAttnHeads + hh)]);
-    float L = 0.f;
-    for (int cc = 0; cc < C; ++cc) {
-      const float m = mall[2 * (cc * kAttnHeads + hh)], l = mall[2 * (cc * kAttnHeads + hh) + 1];
-      const float w = l > 0.f ? exp2f(m - M) : 0.f;
-      wts[cc * kAttnHeads + hh] = w;
-      L += w * l;
+  // Thread (head hh, CTA cc) reads that CTA's (m, l); eight lanes per head
+  // reduce M and L with shuffles (C <= 8).
+  {
+    const int hh = tid >> 3, cc = tid & 7;
+    float m = -CUDART_INF_F, l = 0.f;
+    if (cc < C) {
+      const float2 v = *reinterpret_cast<const float2*>(cluster.map_shared_rank(mls, cc) + hh * 2);
+      m = v.x;
+      l = v.y;
     }
-    invl[hh] = L > 0.f ? 1.f / L : 0.f;
-    if (a.lse && x == 0 && h0 + hh < a.H_q)
-      a.lse[(int64_t)r * a.H_q + h0 + hh] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
+    float M = l > 0.f ? m : -CUDART_INF_F;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = l > 0.f ? exp2f(m - M) : 0.f;
+    float L = w * l;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (cc < C) wts[cc * kAttnHeads + hh] = w;
+    if (cc == 0) {
+      invl[hh] = L > 0.f ? 1.f / L : 0.f;
+      mlc[hh] = M;
+      mlc[kAttnHeads + hh] = L;
+      if (a.Kc == 1 && a.lse && x == 0 && h0 + hh < a.H_q)
+        a.lse[(int64_t)r * a.H_q + h0 + hh] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
+    }
   }
   __syncthreads();
-  const int cs = a.D_v / C;            // columns of this CTA's slice (even: D_v % 32 == 0, C <= 16)
-  const int npairs = kAttnHeads * (cs / 2);
-  for (int e = tid; e < npairs; e += kThreads) {
-    const int hh = e / (cs / 2), col = x * cs + 2 * (e % (cs / 2));
-    // All C remote loads are issued before the (CTA-ordered) accumulation.
-    float2 v[16];
+  const int cs = a.D_v / C;            // columns of this CTA's slice (even: D_v % 32 == 0, C <= 8)
+  const int nq = kAttnHeads * (cs / 4);   // column quads of this slice (cs % 4 == 0)
+  const size_t pstride = 2 * kAttnHeads + (size_t)kAttnHeads * cs;
+  const size_t slot0 = (((size_t)r * gridDim.y + blockIdx.y) * a.Kc) * C + x;   // (kc' = 0, slice x)
+  float* mypart = a.Kc > 1 ? a.apart + (slot0 + (size_t)kc * C) * pstride : nullptr;
+  // Two quads per thread per sweep, all 2 x C remote loads issued before the
+  // (CTA-ordered) accumulation.
+  for (int e0 = tid; e0 < nq; e0 += 2 * kThreads) {
+    float4 v[2][8];
 #pragma unroll
-    for (int cc = 0; cc < 16; ++cc)
-      if (cc < C)
-        v[cc] = *reinterpret_cast<const float2*>(cluster.map_shared_rank(Ob, cc) + hh * a.D_v + col);
-    float2 o = make_float2(0.f, 0.f);
+    for (int u = 0; u < 2; ++u) {
+      const int e = e0 + u * kThreads;
+      const int hh = e / (cs / 4), col = x * cs + 4 * (e % (cs / 4));
 #pragma unroll
-    for (int cc = 0; cc < 16; ++cc)
-      if (cc < C) {
-        const float w = wts[cc * kAttnHeads + hh];
-        o.x += w * v[cc].x;
-        o.y += w * v[cc].y;
+      for (int cc = 0; cc < 8; ++cc)
+        if (cc < C && e < nq)
+          v[u][cc] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(Ob, cc) + hh * a.D_v + col);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = e0 + u * kThreads;
+      if (e >= nq) continue;
+      const int hh = e / (cs / 4), col = x * cs + 4 * (e % (cs / 4));
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        if (cc < C) {
+          const float w = wts[cc * kAttnHeads + hh];
+          o.x += w * v[u][cc].x;
+          o.y += w * v[u][cc].y;
+          o.z += w * v[u][cc].z;
+          o.w += w * v[u][cc].w;
+        }
+      if (a.Kc > 1) {
+        *reinterpret_cast<float4*>(mypart + 2 * kAttnHeads + hh * cs + (col - x * cs)) = o;
+      } else if (h0 + hh < a.H_q) {
+        const float il = invl[hh];
+        *reinterpret_cast<uint2*>(a.out + ((int64_t)r * a.H_q + h0 + hh) * a.D_v + col) =
+            make_uint2(pack_bf16(o.x * il, o.y * il), pack_bf16(o.z * il, o.w * il));
       }
-    if (h0 + hh < a.H_q)
-      *reinterpret_cast<uint32_t*>(a.out + ((int64_t)r * a.H_q + h0 + hh) * a.D_v + col) =
-          pack_bf16(o.x * invl[hh], o.y * invl[hh]);
+    }
   }
+  if (a.Kc > 1 && tid < 2 * kAttnHeads) mypart[tid] = mlc[tid];
   cluster.sync();   // peers may still be reading this CTA's shared memory
+  if (a.Kc == 1) return;
+
+  // Several clusters share (row, head group): the last to finish slice x merges
+  // the Kc cluster partials of that slice, in cluster order.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0)
+    last_s = atomicAdd(a.acnt + ((size_t)r * gridDim.y + blockIdx.y) * 16 + x, 1u) == (uint32_t)(a.Kc - 1);
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  float* fw = mall;                    // [Kc][16] weights of the cluster partials
+  {
+    const int hh = tid >> 3, q = tid & 7;   // Kc <= 8
+    float m = -CUDART_INF_F, l = 0.f;
+    if (q < a.Kc) {
+      const float* pp = a.apart + (slot0 + (size_t)q * C) * pstride;
+      m = __ldcg(pp + hh);
+      l = __ldcg(pp + kAttnHeads + hh);
+    }
+    float M = l > 0.f ? m : -CUDART_INF_F;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = l > 0.f ? exp2f(m - M) : 0.f;
+    float L = w * l;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (q < a.Kc) fw[q * kAttnHeads + hh] = w;
+    if (q == 0) {
+      invl[hh] = L > 0.f ? 1.f / L : 0.f;
+      if (a.lse && x == 0 && h0 + hh < a.H_q)
+        a.lse[(int64_t)r * a.H_q + h0 + hh] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < nq; e += kThreads) {
+    const int hh = e / (cs / 4), cl = 4 * (e % (cs / 4));
+    float4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < a.Kc)
+        v[q] = __ldcg(reinterpret_cast<const float4*>(
+            a.apart + (slot0 + (size_t)q * C) * pstride + 2 * kAttnHeads + hh * cs + cl));
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < a.Kc) {
+        const float w = fw[q * kAttnHeads + hh];
+        o.x += w * v[q].x;
+        o.y += w * v[q].y;
+        o.z += w * v[q].z;
+        o.w += w * v[q].w;
+      }
+    if (h0 + hh < a.H_q) {
+      const float il = invl[hh];
+      *reinterpret_cast<uint2*>(a.out + ((int64_t)r * a.H_q + h0 + hh) * a.D_v + x * cs + cl) =
+          make_uint2(pack_bf16(o.x * il, o.y * il), pack_bf16(o.z * il, o.w * il));
+    }
+  }
 }
 
 template <int NT>
@@ -425,9 +519,6 @@ cudaError_t launch_cluster(const AttnArgs& a, dim3 grid, int C, size_t smem, cud
   cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<NT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (C > 8 && (e = cudaFuncSetAttribute(attn_cluster_kernel<NT>,
-                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
@@ -445,32 +536,6 @@ cudaError_t launch_cluster(const AttnArgs& a, dim3 grid, int C, size_t smem, cud
   return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<NT>, a);
 }
 
-template <int NT>
-int max_cluster(int smem) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(16, 1, 1);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 16;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaFuncSetAttribute(attn_cluster_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(attn_cluster_kernel<NT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-          cudaSuccess)
-    return 8;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<NT>, &cfg) != cudaSuccess || n < 1) {
-    cudaGetLastError();
-    return 8;
-  }
-  return 16;
-}
-
 }  // namespace
 
 cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t* idx,
@@ -481,6 +546,8 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
   a.row_len = p.row_len; a.idx = idx; a.nsel = nsel;
   a.out = out; a.lse = lse;
   a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
+  a.apart = reinterpret_cast<float*>(ws + pl.off_apart);
+  a.acnt = reinterpret_cast<uint32_t*>(ws + pl.off_acnt);
   a.B = p.B; a.H_q = p.H_q; a.D_k = p.D_k; a.D_v = p.D_v; a.k = p.k;
   a.scale_log2 = p.softmax_scale * 1.4426950408889634f;
 
@@ -489,27 +556,23 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
   const int cols = NT * 32;
   a.qs = p.D_k + 8;
   a.ks = (p.D_k > cols ? p.D_k : cols) + 8;
-  const size_t kbytes = (size_t)2 * kAttnRows * a.ks * 2;
+  const size_t kbytes = (size_t)kAttnRows * a.ks * 2;    // one tile per CTA: one K buffer
   const size_t obytes = (size_t)kAttnHeads * p.D_v * 4;   // partial O, aliased on the K buffers
-  const size_t smem = (size_t)kAttnHeads * a.qs * 2 + (kbytes > obytes ? kbytes : obytes) +
+  size_t smem = (size_t)kAttnHeads * a.qs * 2 + (kbytes > obytes ? kbytes : obytes) +
                       (size_t)kAttnHeads * kPStride * 2 + 2 * kWarps * kAttnHeads * 4 +
                       2 * kAttnHeads * 4 + 16 * kAttnHeads * 8 + 16 * kAttnHeads * 4 + kAttnHeads * 4 +
+                      2 * kAttnHeads * 4 +
                       (size_t)kMaxTiles * kAttnRows * 4;
-  // Cluster size: enough CTAs that each takes at most kMaxTiles tiles.
+  // Clusters of C <= 8 CTAs (two fit in every GPC, so all clusters of a step
+  // run in one wave), one 64-position tile per CTA; Kc clusters per (row, head
+  // group) cover the k positions.
   const int tiles = (p.k + kAttnRows - 1) / kAttnRows;
-  static int cmax[4] = {0, 0, 0, 0};
-  const int nti = NT == 2 ? 0 : NT == 4 ? 1 : NT == 8 ? 2 : 3;
   int C = 1;
-  while (C < tiles && C < 16) C <<= 1;
-  if (C > 8) {
-    if (!cmax[nti])
-      cmax[nti] = NT == 2 ? max_cluster<2>((int)smem) : NT == 4 ? max_cluster<4>((int)smem)
-                : NT == 8 ? max_cluster<8>((int)smem) : max_cluster<16>((int)smem);
-    if (C > cmax[nti]) C = cmax[nti];
-  }
-  if ((tiles + C - 1) / C > kMaxTiles) return cudaErrorInvalidConfiguration;
-  // a.D_v / C must be even: D_v is a multiple of 32 and C <= 16.
-  const dim3 grid(C, (p.H_q + kAttnHeads - 1) / kAttnHeads, p.R);
+  while (C < tiles && C < 8) C <<= 1;
+  a.Kc = (tiles + C - 1) / C;
+  if (a.Kc > pl.attn_kc_max || a.Kc > 8) return cudaErrorInvalidConfiguration;   // the merge holds <= 8
+  // a.D_v / C must be even: D_v is a multiple of 32 and C <= 8.
+  const dim3 grid(C * a.Kc, (p.H_q + kAttnHeads - 1) / kAttnHeads, p.R);
   switch (NT) {
     case 2: return launch_cluster<2>(a, grid, C, smem, st);
     case 4: return launch_cluster<4>(a, grid, C, smem, st);

@@ -38,8 +38,9 @@ struct Plan {
   int flags;
   int chunk, nchunk;       // top-k: positions per CTA, CTAs per row
   int hist_rep;            // top-k: copies of each row's global histogram
-  size_t off_status, off_state, off_hist, zero_end;
-  size_t off_surv, off_scores, total;
+  int attn_kc_max;          // attention: clusters per (row, head group), at most
+  size_t off_status, off_state, off_hist, off_acnt, zero_end;
+  size_t off_surv, off_scores, off_apart, total;
 };
 
 // Order-preserving map of int32 onto uint32.

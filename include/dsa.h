@@ -34,7 +34,7 @@
  * - Each entry point clears the status word before its own kernels run.
  * - dsa_topk and dsa_decode_step launch one cooperative kernel (at most one CTA
  *   per SM, all resident at once); dsa_sparse_attn and dsa_decode_step launch
- *   thread-block clusters of up to 16 CTAs.  A launch the device cannot place
+ *   thread-block clusters of up to 8 CTAs.  A launch the device cannot place
  *   returns DSA_ERR_CUDA and enqueues nothing further.
  *
  * Layouts (row-major, no padding unless stated)
