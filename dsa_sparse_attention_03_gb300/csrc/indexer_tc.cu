@@ -62,14 +62,17 @@ constexpr int kModeExact = 0, kModeBiased = 1, kModeFp8 = 2;
 // TMEM-operand kernel warp roles.  Issuing a tcgen05.mma occupies the issuing
 // SM sub-partition for tens of ns, and every TMEM-touching role is tied to a
 // sub-partition (warp w reaches TMEM lanes 32*(w%4)..), so MMA issue is spread
-// over four threads, one per sub-partition, each taking every fourth tile:
+// over four threads, one per sub-partition, each taking every fourth tile.
+// Conversion is latency-bound within a warp, so two converter warps share
+// each sub-partition, taking alternate tiles:
 //   warp 0       TMA producer              warps 1-4    MMA issuers (tile % 4)
-//   warps 5-8    converters (lane quarter = warp % 4)
-//   warps 9-16   epilogue, two groups of four (tile % 2)
+//   warps 5-12   converters, lane quarter = warp % 4, tile parity = (warp - 5) / 4
+//   warps 13-20  epilogue, two groups of four (tile % 2)
 constexpr int kTmMmaWarp0 = 1;
 constexpr int kTmMmaWarps = 4;
 constexpr int kTmConvWarp0 = kTmMmaWarp0 + kTmMmaWarps;
-constexpr int kTmConvWarps = 4;
+constexpr int kTmConvWarps = 8;
+constexpr int kTmConvPerTile = 4;            // converter warps (arrivals) per tile
 constexpr int kTmEpiWarp0 = kTmConvWarp0 + kTmConvWarps;
 constexpr int kTmThreads = (kTmEpiWarp0 + kEpiWarps) * 32;
 constexpr float kMagic = 12582912.f;         // 1.5 * 2^23
@@ -92,6 +95,7 @@ struct TcArgs {
   uint4* zero;          // workspace words to clear (status + top-k state)
   int n_zero;
   int na;               // TMEM A buffers (TMEM-operand kernel)
+  uint32_t b_stride;    // bytes between the two B buffers (TMEM-operand kernel)
   uint32_t a_col0;      // first TMEM column of the A buffers
   CUtensorMap tmap;     // k_idx as [L_total, 128] bytes, 128-byte swizzle
 };
@@ -251,6 +255,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
         "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
         "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (no wait).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
 }
 
@@ -739,10 +754,10 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
     if (lane == 0) {
       for (int s = 0; s < S; ++s) {
         mbar_init(bar_full + 8 * s, 1);
-        mbar_init(bar_empty + 8 * s, kTmConvWarps);
+        mbar_init(bar_empty + 8 * s, kTmConvPerTile);
       }
       for (int i = 0; i < kMaxA; ++i) {
-        mbar_init(bar_afull + 8 * i, kTmConvWarps);
+        mbar_init(bar_afull + 8 * i, kTmConvPerTile);
         mbar_init(bar_afree + 8 * i, 1);
       }
       for (int i = 0; i < kMaxAcc; ++i) {
@@ -840,7 +855,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
     const int j = warp - kTmMmaWarp0;
     if (lane == 0) {
       int last = -1;
-      const uint32_t b_base = cvta_smem(Bop);
+      const uint32_t b_base = cvta_smem(Bop) + (uint32_t)(j & 1) * a.b_stride;   // B of this tile parity
       for (int i = j; i < n_local; i += kTmMmaWarps) {
         const int acc = i % NACC, ab = i % NA;
         tile_step(a, prefix, t_begin + i, ti);
@@ -878,53 +893,59 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
   } else if (warp < kTmEpiWarp0) {
     // ------------------------------------------------------------ converters
     const int quarter = warp & 3;
+    const int par = (warp - kTmConvWarp0) >> 2;  // tiles i with i % 2 == par
     const int m = quarter * 32 + lane;        // key row = TMEM lane this thread writes
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + a.a_col0;
-    const int ct = tid - kTmConvWarp0 * 32;
-    for (int i = 0; i < n_local; ++i) {
+    const int ct = ((warp - kTmConvWarp0) & 3) * 32 + lane;   // thread among this parity's four warps
+    unsigned char* Bp = Bop + par * a.b_stride;                // B of this parity
+    for (int i = par; i < n_local; i += 2) {
       const int s = i % S, ab = i % NA;
       const bool new_group = tile_step(a, prefix, t_begin + i, ti);
       if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status)) break;
       if (i >= NA && !wait_bar_warp(bar_afree + 8 * ab, ((i / NA) - 1) & 1, abort_flag, a.status)) break;
       if (new_group) {
-        // B may be rewritten once every issued MMA has finished (the last NA
-        // tiles come from different issuers, so wait for each of them).
-        bool ok = true;
-        for (int pr = max(0, i - NA); pr < i && ok; ++pr)
-          ok = wait_bar_warp(bar_afree + 8 * (pr % NA), (pr / NA) & 1, abort_flag, a.status);
-        if (!ok) break;
+        // This parity's B is read by the MMAs of tiles i-2, i-4, ...; issuers
+        // (i-2) % 4 and i % 4 complete theirs in order, and tile i-4 (buffer
+        // ab) was waited for above, so tile i-2 is the one left.
+        if (i >= 2 &&
+            !wait_bar_warp(bar_afree + 8 * ((i - 2) % NA), ((i - 2) / NA) & 1, abort_flag, a.status))
+          break;
         const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
         const int nchunks = ti.nrows * a.H_i * (D_I / 16);
-        for (int q = ct; q < nchunks; q += kTmConvWarps * 32) {
+        for (int q = ct; q < nchunks; q += kTmConvPerTile * 32) {
           const int n = q / (D_I / 16), c = q % (D_I / 16);
           if (FP8) {
             // e4m3 rows of 128 bytes: 16-byte unit c of row n at unit c ^ (n mod 8).
             const int4 v = __ldg(src + q);
-            *reinterpret_cast<uint4*>(Bop + n * 128 + ((c ^ (n & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(Bp + n * 128 + ((c ^ (n & 7)) << 4)) =
                 make_uint4(i8x4_to_e4m3x4((uint32_t)v.x), i8x4_to_e4m3x4((uint32_t)v.y),
                            i8x4_to_e4m3x4((uint32_t)v.z), i8x4_to_e4m3x4((uint32_t)v.w));
           } else {
             uint32_t b0, b1;
             sw128_offsets(n, c, (uint32_t)N_max * 128, b0, b1);
-            convert16<false>(__ldg(src + q), Bop + b0, Bop + b1);   // queries stay exact
+            convert16<false>(__ldg(src + q), Bp + b0, Bp + b1);   // queries stay exact
           }
         }
         fence_proxy_async();                  // B is read by the MMA (async proxy)
       }
       const unsigned char* row = stage + s * kStageBytes + m * 128;
       if (FP8) {
-        int4 v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const int4*>(row + ((j ^ (m & 7)) << 4));
-        uint32_t o[32];
+        for (int half = 0; half < 2; ++half) {
+          int4 v[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          o[4 * j + 0] = i8x4_to_e4m3x4((uint32_t)v[j].x);
-          o[4 * j + 1] = i8x4_to_e4m3x4((uint32_t)v[j].y);
-          o[4 * j + 2] = i8x4_to_e4m3x4((uint32_t)v[j].z);
-          o[4 * j + 3] = i8x4_to_e4m3x4((uint32_t)v[j].w);
+          for (int j = 0; j < 4; ++j)
+            v[j] = *reinterpret_cast<const int4*>(row + (((half * 4 + j) ^ (m & 7)) << 4));
+          uint32_t o[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            o[4 * j + 0] = i8x4_to_e4m3x4((uint32_t)v[j].x);
+            o[4 * j + 1] = i8x4_to_e4m3x4((uint32_t)v[j].y);
+            o[4 * j + 2] = i8x4_to_e4m3x4((uint32_t)v[j].z);
+            o[4 * j + 3] = i8x4_to_e4m3x4((uint32_t)v[j].w);
+          }
+          tmem_st16(lane_base + ab * kACols + half * 16, o);
         }
-        tmem_st32(lane_base + ab * kACols, o);
       } else {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -1013,12 +1034,12 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
         if (jr >= ti.nrows) break;
         uint32_t acc4[4] = {0u, 0u, 0u, 0u};
         const int4* wr = reinterpret_cast<const int4*>(wc + jr * a.H_i);
-        for (int h0 = 0; h0 < a.H_i; h0 += 32) {
-          uint32_t va[32];
-          tmem_ld32(trow + jr * a.H_i + h0, va);
+        for (int h0 = 0; h0 < a.H_i; h0 += 16) {
+          uint32_t va[16];
+          tmem_ld16(trow + jr * a.H_i + h0, va);
           tmem_wait_ld();
 #pragma unroll
-          for (int h2 = 0; h2 < 16; ++h2) {
+          for (int h2 = 0; h2 < 8; ++h2) {
             const int4 p = wr[(h0 >> 1) + h2];     // (w, c) of heads h0+2*h2 and h0+2*h2+1
             // x = max(d - bias + M, floor) = M + ReLU(q.k): an exact integer in
             // [2^23, 2^24), so its bit pattern is 0x4B400000 + score part.
@@ -1154,6 +1175,7 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
     a.na = kMaxA;                                  // = kTmMmaWarps: issuer j owns A buffer j
     a.nacc = (int)((512u - kMaxA * a_cols) / (uint32_t)N_max);
     if (a.nacc > kMaxAcc) a.nacc = kMaxAcc;
+    a.nacc &= ~1;                                  // each tile parity owns its accumulators
     a.a_col0 = (uint32_t)(a.nacc * N_max);
     uint32_t cols = 32;
     while (cols < a.a_col0 + kMaxA * a_cols) cols <<= 1;
@@ -1167,7 +1189,8 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     const uint32_t stage_bytes = 128u * 128u;
-    const uint32_t b_bytes = (uint32_t)N_max * 128u * (fp8 ? 1u : 2u);
+    a.b_stride = (uint32_t)N_max * 128u * (fp8 ? 1u : 2u);
+    const uint32_t b_bytes = 2u * a.b_stride;                  // one B per tile parity
     auto total_for = [&](int s) {
       return s * stage_bytes + b_bytes + w_bytes + (2 * s + 2 * kMaxA + 2 * kMaxAcc) * 8 + 16 + prefix_bytes;
     };

@@ -120,3 +120,14 @@ def test_tc_fp8_path_at_its_exactness_limit():
     x.k_idx[:] = rng.choice(np.array([-11, 11, -10, 9, 1], np.int8), x.k_idx.shape)
     _check_one(x, None, True, True, 11)
     _check_one(x, None, False, True, 11)
+
+
+def test_tc_fp8_with_128_column_accumulators():
+    # 32 heads x 4 rows per request fill 128 accumulator columns per tile in the
+    # e4m3 mode; the two tile parities must still own separate accumulators.
+    x = gen.make_inputs("f4", seed=21, lengths=[3000, 1500], rows_per_request=[4, 4],
+                        row_len=[3000, 2990, 2500, 100, 1500, 1400, 1499, 7], H_i=32, D_i=128,
+                        H_q=16, D_k=64, D_v=64, k=256, softmax_scale=0.125)
+    qk = value_bound(x)
+    assert qk <= 11
+    _check_one(x, None, True, True, qk)
