@@ -91,6 +91,7 @@ struct TcArgs {
   int B, H_i, D_i, RG, stages, relu;
   int nacc;             // TMEM accumulator buffers (4, or 2 when N = 256)
   uint32_t off_b, off_stage, off_w, off_bar, off_misc, off_prefix;   // shared-memory map
+  int pstride;          // ints between the prefix, offsets and row-offset copies in shared memory
   uint32_t tmem_cols;
   uint4* zero;          // workspace words to clear (status + top-k state)
   int n_zero;
@@ -358,18 +359,21 @@ __device__ __noinline__ TileInfo tile_lookup(const TcArgs& a, const int* prefix,
     const int mid = (lo + hi + 1) >> 1;
     if (prefix[mid] <= gt) lo = mid; else hi = mid - 1;
   }
+  // Shared-memory copies of offsets and row_offsets follow the prefix.
+  const int* offs = prefix + a.pstride;
+  const int* roffs = prefix + 2 * a.pstride;
   TileInfo ti;
   ti.b = lo;
-  ti.base = a.offsets[lo];
-  ti.L_b = a.offsets[lo + 1] - a.offsets[lo];
+  ti.base = offs[lo];
+  ti.L_b = offs[lo + 1] - offs[lo];
   const int tiles_b = (ti.L_b + kTile - 1) / kTile;
   const int local = gt - prefix[lo];
   ti.g = local / tiles_b;
   ti.j = local - ti.g * tiles_b;
   ti.lo = prefix[lo] + ti.g * tiles_b;
   ti.hi = ti.lo + tiles_b;
-  const int rb = a.row_offsets[lo];
-  const int rows_b = a.row_offsets[lo + 1] - rb;
+  const int rb = roffs[lo];
+  const int rows_b = roffs[lo + 1] - rb;
   ti.r0 = rb + ti.g * a.RG;
   ti.nrows = min(a.RG, rows_b - ti.g * a.RG);
   return ti;
@@ -455,9 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
       const int b = base + lane;
       int v = 0;
       if (b < a.B) {
-        const int L_b = a.offsets[b + 1] - a.offsets[b];
-        const int rows_b = a.row_offsets[b + 1] - a.row_offsets[b];
-        v = ((rows_b + a.RG - 1) / a.RG) * ((L_b + kTile - 1) / kTile);
+        const int o0 = a.offsets[b], o1 = a.offsets[b + 1];
+        const int r0 = a.row_offsets[b], r1 = a.row_offsets[b + 1];
+        prefix[a.pstride + b] = o0;
+        prefix[2 * a.pstride + b] = r0;
+        if (b == a.B - 1) {
+          prefix[a.pstride + b + 1] = o1;
+          prefix[2 * a.pstride + b + 1] = r1;
+        }
+        v = ((r1 - r0 + a.RG - 1) / a.RG) * ((o1 - o0 + kTile - 1) / kTile);
       }
       int incl = v;
 #pragma unroll
@@ -790,9 +800,15 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
       const int b = base + lane;
       int v = 0;
       if (b < a.B) {
-        const int L_b = a.offsets[b + 1] - a.offsets[b];
-        const int rows_b = a.row_offsets[b + 1] - a.row_offsets[b];
-        v = ((rows_b + a.RG - 1) / a.RG) * ((L_b + kTile - 1) / kTile);
+        const int o0 = a.offsets[b], o1 = a.offsets[b + 1];
+        const int r0 = a.row_offsets[b], r1 = a.row_offsets[b + 1];
+        prefix[a.pstride + b] = o0;
+        prefix[2 * a.pstride + b] = r0;
+        if (b == a.B - 1) {
+          prefix[a.pstride + b + 1] = o1;
+          prefix[2 * a.pstride + b + 1] = r1;
+        }
+        v = ((r1 - r0 + a.RG - 1) / a.RG) * ((o1 - o0 + kTile - 1) / kTile);
       }
       int incl = v;
 #pragma unroll
@@ -901,9 +917,8 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
     for (int i = par; i < n_local; i += 2) {
       const int s = i % S, ab = i % NA;
       const bool new_group = tile_step(a, prefix, t_begin + i, ti);
-      if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status)) break;
       if (i >= NA && !wait_bar_warp(bar_afree + 8 * ab, ((i / NA) - 1) & 1, abort_flag, a.status)) break;
-      if (new_group) {
+      if (new_group) {   // (B does not depend on the key tile: written before waiting for it)
         // This parity's B is read by the MMAs of tiles i-2, i-4, ...; issuers
         // (i-2) % 4 and i % 4 complete theirs in order, and tile i-4 (buffer
         // ab) was waited for above, so tile i-2 is the one left.
@@ -928,6 +943,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
         }
         fence_proxy_async();                  // B is read by the MMA (async proxy)
       }
+      if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status)) break;
       const unsigned char* row = stage + s * kStageBytes + m * 128;
       if (FP8) {
 #pragma unroll
@@ -1154,7 +1170,9 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   // The biased conversion needs every partial sum |sum_d q_d (k_d + 1152)| < 2^24.
   const int64_t qk = p.qk_abs_max > 0 ? p.qk_abs_max : 128;
   const bool biased = (int64_t)D_i * qk * 1279 < (int64_t(1) << 24);
-  const uint32_t prefix_bytes = ((uint32_t)(p.B + 1) * 4u + 15u) / 16u * 16u;
+  // Prefix over requests, then copies of offsets and row_offsets: 3 x (B + 1) ints.
+  a.pstride = (p.B + 1 + 3) / 4 * 4;
+  const uint32_t prefix_bytes = 3u * (uint32_t)a.pstride * 4u;
   const uint32_t w_bytes = kEpiWarps * (uint32_t)(RG * p.H_i + kMaxRG) * 8u;
   const uint32_t budget = 227u * 1024u - 1024u;   // minus the alignment slack
   int dev = 0, sms = 0;
@@ -1194,7 +1212,10 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
     auto total_for = [&](int s) {
       return s * stage_bytes + b_bytes + w_bytes + (2 * s + 2 * kMaxA + 2 * kMaxAcc) * 8 + 16 + prefix_bytes;
     };
-    const int S = total_for(8) <= budget ? 8 : 4;
+    // Four key stages: a smaller first wave of loads gets the first tile to
+    // the converters sooner, and four tiles of look-ahead outrun the per-tile
+    // work at HBM speed.
+    const int S = 4;
     if (total_for(S) > budget) return cudaErrorInvalidConfiguration;
     a.stages = S;
     a.off_b = S * stage_bytes;
