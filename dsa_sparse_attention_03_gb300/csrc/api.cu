@@ -102,12 +102,12 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   P.off_status = off; off += 256;
   P.off_state = off; off = align_up(off + R * sizeof(RowState), 256);
   P.off_hist = off; off = align_up(off + R * size_t(P.hist_rep) * kBuckets * 4, 256);
-  // Attention: clusters of up to 8 CTAs take one 64-position tile per CTA; a
-  // (row, head group) with more tiles uses several clusters, merged through
-  // per-slice partials and arrival counters.
+  // Attention: clusters of 4 or 8 CTAs take one 64-position tile per CTA; a
+  // (row, head group) with more tiles uses several clusters (at most 8),
+  // merged through per-slice partials and arrival counters.
   const int hgroups = p->H_q > 0 ? (p->H_q + kAttnHeads - 1) / kAttnHeads : 0;
   const int tiles = (p->k + kAttnRows - 1) / kAttnRows;
-  P.attn_kc_max = (tiles + 7) / 8;
+  P.attn_kc_max = (tiles + attn_cluster_size(p->k) - 1) / attn_cluster_size(p->k);
   P.off_acnt = off; off = align_up(off + R * size_t(hgroups) * 16 * 4, 256);
   P.zero_end = off;
   P.off_surv = off; off = align_up(off + R * size_t(kCapFast) * 8, 256);

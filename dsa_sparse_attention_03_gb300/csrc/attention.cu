@@ -8,7 +8,7 @@
 //   z_j = scale * q[r,h,:] . kv[idx_j, :],  o[h,:] = sum_j softmax(z)_j kv[idx_j, :D_v]
 //
 // attn_cluster_kernel  grid (C * Kc, head group of 16, row), cluster (C, 1, 1)
-//   with C <= 8, 4 warps.  The S = C * Kc CTAs of a (row, head group) split
+//   with C = 4 (k <= 2048) or 8, 4 warps.  The S = C * Kc CTAs of a (row, head group) split
 //   the selected positions: CTA sp takes the tiles sp, sp + S, ... of 64
 //   positions (one tile at k = 2048).  It gathers the rows (one bulk copy per
 //   whole row, as the front-axis gather of "GLM-5.3-Flash-Alis-MLX-4bit",
@@ -563,14 +563,16 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
                       2 * kAttnHeads * 4 + 16 * kAttnHeads * 8 + 16 * kAttnHeads * 4 + kAttnHeads * 4 +
                       2 * kAttnHeads * 4 +
                       (size_t)kMaxTiles * kAttnRows * 4;
-  // Clusters of C <= 8 CTAs (two fit in every GPC, so all clusters of a step
-  // run in one wave), one 64-position tile per CTA; Kc clusters per (row, head
-  // group) cover the k positions.
+  // Clusters of C CTAs, one 64-position tile per CTA; Kc clusters per (row,
+  // head group) cover the k positions.  Clusters of 4 are placed one CTA per
+  // SM (at least 116 KB of shared memory): two CTAs on an SM would share its
+  // bandwidth for scattered rows (about 40 GB/s), and the gather is the
+  // critical path.  Clusters of 8 so padded would not all fit in one wave.
   const int tiles = (p.k + kAttnRows - 1) / kAttnRows;
-  int C = 1;
-  while (C < tiles && C < 8) C <<= 1;
+  const int C = attn_cluster_size(p.k);
   a.Kc = (tiles + C - 1) / C;
   if (a.Kc > pl.attn_kc_max || a.Kc > 8) return cudaErrorInvalidConfiguration;   // the merge holds <= 8
+  if (C <= 4 && smem < 116u * 1024u) smem = 116u * 1024u;
   // a.D_v / C must be even: D_v is a multiple of 32 and C <= 8.
   const dim3 grid(C * a.Kc, (p.H_q + kAttnHeads - 1) / kAttnHeads, p.R);
   switch (NT) {

@@ -43,6 +43,17 @@ struct Plan {
   size_t off_surv, off_scores, off_apart, total;
 };
 
+// Attention cluster size for k selected positions: one 64-position tile per
+// CTA, clusters of 4 (one CTA per SM) up to 32 tiles, else of 8, so that at
+// most 8 clusters share a (row, head group).
+__host__ __device__ inline int attn_cluster_size(int k) {
+  const int tiles = (k + kAttnRows - 1) / kAttnRows;
+  const int cmax = tiles <= 32 ? 4 : 8;
+  int c = 1;
+  while (c < tiles && c < cmax) c <<= 1;
+  return c;
+}
+
 // Order-preserving map of int32 onto uint32.
 __host__ __device__ __forceinline__ uint32_t ordered_key(int32_t s) {
   return static_cast<uint32_t>(s) ^ 0x80000000u;
