@@ -35,7 +35,7 @@ namespace dsa {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kRankSlice = 32;                             // survivors ranked per work unit
+constexpr int kRankSlice = 16;                             // survivors ranked per work unit
 constexpr int kRankLanes = kThreads / kRankSlice;          // threads per survivor
 constexpr int kRankSlices = kCapFast / kRankSlice;         // units per row (also covers idx[0, k))
 static_assert(kRankSlices * kRankSlice >= kMaxK, "rank units must cover idx");
@@ -461,12 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
   }
   if (!grid_barrier(a.bar + nb++, a.status)) return;
 
-  // ---- rank: units (row, slice of kRankSlice survivors), contiguous per CTA so
-  // that a CTA loads each row's survivor keys once.
-  const int64_t nr = (int64_t)a.R * kRankSlices;
-  const int u0 = (int)(nr * blockIdx.x / gridDim.x), u1 = (int)(nr * (blockIdx.x + 1) / gridDim.x);
+  // ---- rank: units (row, slice of kRankSlice survivors), one warp per
+  // survivor.  Units go out in runs of `run` consecutive units, run c to CTA
+  // c % grid: with one row the few active slices land on different CTAs; with
+  // many rows a CTA's runs stay within a row, which it loads once per run.
+  const int nr = a.R * kRankSlices;
+  const int run = max(1, nr / (4 * (int)gridDim.x));
   int loaded = -1;
-  for (int u = u0; u < u1; ++u) {
+  for (int c = (int)blockIdx.x; (int64_t)c * run < nr; c += (int)gridDim.x)
+  for (int u = c * run; u < min(nr, (c + 1) * run); ++u) {
     const int r = u / kRankSlices, sl = u % kRankSlices;
     RowState* st = a.state + r;
     const uint32_t mode = st->mode;
