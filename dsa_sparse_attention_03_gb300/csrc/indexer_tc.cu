@@ -89,6 +89,7 @@ struct TcArgs {
   RowState* rows;       // per-row key range for the top-k
   int64_t L_max;
   int B, H_i, D_i, RG, stages, relu;
+  int L1, R1;           // B == 1: the request's length (L_total) and rows (R), known on the host
   int nacc;             // TMEM accumulator buffers (4, or 2 when N = 256)
   uint32_t off_b, off_stage, off_w, off_bar, off_misc, off_prefix;   // shared-memory map
   int pstride;          // ints between the prefix, offsets and row-offset copies in shared memory
@@ -459,8 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
       const int b = base + lane;
       int v = 0;
       if (b < a.B) {
-        const int o0 = a.offsets[b], o1 = a.offsets[b + 1];
-        const int r0 = a.row_offsets[b], r1 = a.row_offsets[b + 1];
+        // One request: offsets {0, L_total}, row_offsets {0, R} need no loads.
+        const int o0 = a.B == 1 ? 0 : a.offsets[b], o1 = a.B == 1 ? a.L1 : a.offsets[b + 1];
+        const int r0 = a.B == 1 ? 0 : a.row_offsets[b], r1 = a.B == 1 ? a.R1 : a.row_offsets[b + 1];
         prefix[a.pstride + b] = o0;
         prefix[2 * a.pstride + b] = r0;
         if (b == a.B - 1) {
@@ -800,8 +802,9 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
       const int b = base + lane;
       int v = 0;
       if (b < a.B) {
-        const int o0 = a.offsets[b], o1 = a.offsets[b + 1];
-        const int r0 = a.row_offsets[b], r1 = a.row_offsets[b + 1];
+        // One request: offsets {0, L_total}, row_offsets {0, R} need no loads.
+        const int o0 = a.B == 1 ? 0 : a.offsets[b], o1 = a.B == 1 ? a.L1 : a.offsets[b + 1];
+        const int r0 = a.B == 1 ? 0 : a.row_offsets[b], r1 = a.B == 1 ? a.R1 : a.row_offsets[b + 1];
         prefix[a.pstride + b] = o0;
         prefix[2 * a.pstride + b] = r0;
         if (b == a.B - 1) {
@@ -1160,6 +1163,7 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   a.offsets = p.offsets; a.row_offsets = p.row_offsets; a.row_len = p.row_len;
   a.scores = scores; a.L_max = p.L_max;
   a.B = p.B; a.H_i = p.H_i; a.D_i = p.D_i; a.relu = (p.flags & DSA_FLAG_NO_RELU) ? 0 : 1;
+  a.L1 = (int)p.L_total; a.R1 = p.R;
   const int per_req = (p.R + p.B - 1) / p.B;
   int RG = 256 / p.H_i;
   if (RG > kMaxRG) RG = kMaxRG;

@@ -45,8 +45,10 @@
  *                                 all indexer heads; 16-byte aligned base
  *   q       bf16  [R, H_q, D_k]   attention queries (uint16 bit patterns)
  *   kv      bf16  [L_total, D_k]  latent cache rows; 16-byte aligned base
- *   offsets     int32 [B+1]  cache rows of request b: offsets[b] .. offsets[b+1]-1
- *   row_offsets int32 [B+1]  query rows of request b: row_offsets[b] .. row_offsets[b+1]-1
+ *   offsets     int32 [B+1]  cache rows of request b: offsets[b] .. offsets[b+1]-1;
+ *                            offsets[0] = 0 and offsets[B] = L_total
+ *   row_offsets int32 [B+1]  query rows of request b: row_offsets[b] .. row_offsets[b+1]-1;
+ *                            row_offsets[0] = 0 and row_offsets[B] = R
  *   row_len     int32 [R]    row r sees request-local positions 0 .. row_len[r]-1
  *                            (row_len[r] <= its request's length).  Validity comes
  *                            from each row's own length, never from padding
