@@ -98,18 +98,43 @@ class ClockSampler:
 
 
 def make_layers(n_layers, L, device):
+    """n_layers independent layers whose inputs sit in one device tensor per
+    kind (layer i is slice i), so a step can move every layer's inputs with
+    one copy per kind."""
     import torch
     import dsa_sparse_attention_03_gb300 as dsa
+    xs = [gen.l300k(layer=layer, L=L) if L == L_LONG else gen.l64k(layer=layer, L=L)
+          for layer in range(n_layers)]
+    x0 = xs[0]
+
+    def stack(name, arr_of, dtype):
+        host = np.stack([np.ascontiguousarray(arr_of(x)) for x in xs])
+        return torch.from_numpy(host).to(device=device, dtype=dtype)
+
+    packed = {
+        "q_idx": stack("q_idx", lambda x: x.q_idx, torch.int8),
+        "w_idx": stack("w_idx", lambda x: x.w_idx, torch.int32),
+        "k_idx": stack("k_idx", lambda x: x.k_idx, torch.int8),
+        "q": stack("q", lambda x: np.asarray(x.q).view(np.int16), torch.int16),
+        "kv": stack("kv", lambda x: np.asarray(x.kv).view(np.int16), torch.int16),
+    }
+    offsets = torch.from_numpy(x0.offsets).to(device)
+    row_offsets = torch.from_numpy(x0.row_offsets).to(device)
+    row_len = torch.from_numpy(x0.row_len).to(device)
     layers = []
-    for layer in range(n_layers):
-        x = gen.l300k(layer=layer, L=L) if L == L_LONG else gen.l64k(layer=layer, L=L)
+    for i, x in enumerate(xs):
         # The caller declares its int8 value range (here the data's own bound).
         qk = int(max(np.abs(x.q_idx.astype(np.int32)).max(), np.abs(x.k_idx.astype(np.int32)).max()))
-        prob, t = dsa.upload_inputs(x, device=device, qk_abs_max=qk)
+        t = {k: v[i] for k, v in packed.items()}
+        prob = dsa.Problem.from_tensors(k=x.k, D_v=x.D_v, softmax_scale=x.softmax_scale,
+                                        L_max=int(np.max(x.row_len)), L_total=int(x.offsets[-1]),
+                                        qk_abs_max=qk, offsets=offsets, row_offsets=row_offsets,
+                                        row_len=row_len, **t)
         layers.append((x, prob, t))
+    layers[0][2]["_packed"] = packed
     ws = dsa.alloc_workspace(layers[0][1], device=device)   # same sizes for every layer
-    k = layers[0][0].k
-    H_q, D_v = layers[0][0].H_q, layers[0][0].D_v
+    k = x0.k
+    H_q, D_v = x0.H_q, x0.D_v
     idx = torch.empty((n_layers, 1, k), dtype=torch.int32, device=device)
     nsel = torch.empty((n_layers, 1), dtype=torch.int32, device=device)
     out = torch.empty((n_layers, 1, H_q, D_v), dtype=torch.int16, device=device)
@@ -337,49 +362,65 @@ def bench_e2e(args, layers, ws, idx, nsel, out, stream, device):
     import torch
     import dsa_sparse_attention_03_gb300 as dsa
     sp = stream.cuda_stream
-    host_in, host_out = [], []
-    h2d = d2h = 0
-    for x, prob, t in layers:
-        hi = {
-            "q_idx": torch.from_numpy(x.q_idx).pin_memory(),
-            "w_idx": torch.from_numpy(x.w_idx).pin_memory(),
-            "q": torch.from_numpy(x.q.view(np.int16)).pin_memory(),
-            "k_row": torch.from_numpy(x.k_idx[-1:]).pin_memory(),
-            "kv_row": torch.from_numpy(x.kv[-1:].view(np.int16)).pin_memory(),
-        }
-        host_in.append(hi)
-        host_out.append({"out": torch.empty((1, x.H_q, x.D_v), dtype=torch.int16).pin_memory(),
-                         "idx": torch.empty((1, x.k), dtype=torch.int32).pin_memory()})
-    h2d = sum(v.numel() * v.element_size() for v in host_in[0].values()) * len(layers)
-    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values()) * len(layers)
+    packed = layers[0][2]["_packed"]
+    xs = [x for x, _, _ in layers]
+    # Pinned host inputs of every layer: the query side and the new token's
+    # cache rows (indexer key and latent row, appended at the last position).
+    host_in = {
+        "q_idx": torch.from_numpy(np.stack([x.q_idx for x in xs])).pin_memory(),
+        "w_idx": torch.from_numpy(np.stack([x.w_idx for x in xs])).pin_memory(),
+        "q": torch.from_numpy(np.stack([np.asarray(x.q).view(np.int16) for x in xs])).pin_memory(),
+        "k_row": torch.from_numpy(np.stack([x.k_idx[-1] for x in xs])).pin_memory(),
+        "kv_row": torch.from_numpy(np.stack([np.asarray(x.kv[-1]).view(np.int16) for x in xs])).pin_memory(),
+    }
+    host_out = {"out": torch.empty(tuple(out.shape), dtype=torch.int16).pin_memory(),
+                "idx": torch.empty(tuple(idx.shape), dtype=torch.int32).pin_memory()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
     def step():
+        packed["q_idx"].copy_(host_in["q_idx"], non_blocking=True)
+        packed["w_idx"].copy_(host_in["w_idx"], non_blocking=True)
+        packed["q"].copy_(host_in["q"], non_blocking=True)
+        packed["k_idx"][:, -1].copy_(host_in["k_row"], non_blocking=True)
+        packed["kv"][:, -1].copy_(host_in["kv_row"], non_blocking=True)
         for i, (x, prob, t) in enumerate(layers):
-            hi, ho = host_in[i], host_out[i]
-            t["q_idx"].copy_(hi["q_idx"], non_blocking=True)
-            t["w_idx"].copy_(hi["w_idx"], non_blocking=True)
-            t["q"].copy_(hi["q"], non_blocking=True)
-            t["k_idx"][-1:].copy_(hi["k_row"], non_blocking=True)
-            t["kv"][-1:].copy_(hi["kv_row"], non_blocking=True)
             dsa.dsa_decode_step(prob, idx[i], nsel[i], out[i], ws, stream=sp)
-            ho["out"].copy_(out[i], non_blocking=True)
-            ho["idx"].copy_(idx[i], non_blocking=True)
+        host_out["out"].copy_(out, non_blocking=True)
+        host_out["idx"].copy_(idx, non_blocking=True)
+
+    def timed(run, steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                run()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
 
     with torch.cuda.stream(stream):
         for _ in range(max(1, args.warmup)):
             step()
-        torch.cuda.synchronize()
-        steps = max(3, args.steps // 2)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    steps = max(3, args.steps // 2)
+    eager_ms = timed(step, steps)
+    # The same step as a user would run a decode loop: captured once in a CUDA
+    # graph whose memcpy nodes copy from / to the pinned host buffers on every
+    # replay.
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+    ms = timed(graph.replay, steps) if graph is not None else eager_ms
     return {"value": round(ms * 1000.0 / len(layers), 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": steps, "cuda_graph": False}
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "cuda_graph": graph is not None,
+            "eager_value": round(eager_ms * 1000.0 / len(layers), 3)}
 
 
 def bench_l64k(args, stream, device):
@@ -393,25 +434,36 @@ def bench_l64k(args, stream, device):
         _, prob, _ = layers[i % n]
         dsa.dsa_decode_step(prob, idx[i % n], nsel[i % n], out[i % n], ws, stream=sp)
 
-    with torch.cuda.stream(stream):
+    def all_layers():
         for i in range(n):
             step(i)
-        torch.cuda.synchronize()
-        reps = max(2, args.steps) * n
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
+
+    with torch.cuda.stream(stream):
+        all_layers()
+    torch.cuda.synchronize()
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            all_layers()
+    run = graph.replay if graph is not None else all_layers
+    reps = max(2, min(args.steps, 500))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        run()
         e0.record(stream)
-        for i in range(reps):
-            step(i)
+        for _ in range(reps):
+            run()
         e1.record(stream)
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1000.0 / reps
+    us = e0.elapsed_time(e1) * 1000.0 / (reps * n)
     x0 = layers[0][0]
     nbytes = 65536 * x0.D_i + x0.k * x0.D_k * 2 + x0.H_q * x0.D_k * 2
     del layers, ws
     return {"workload": "l64k: 1 query, L=65536, 1 layer (12 rotated layer buffers, 1.0 GB)",
             "us_per_layer": round(us, 3), "step_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
-            "cuda_graph": False}
+            "cuda_graph": graph is not None}
 
 
 def cpu_baseline(layers_for_cpu):
