@@ -1,0 +1,106 @@
+"""dsa_topk on crafted score rows, against the oracle's full stable sort: the
+sampled-threshold path, rows whose sample over- or under-counts (which must
+take the histogram path), heavy ties (the exact path), and rows of every kind
+in one call.  Scores are given directly, so each path is reached on purpose."""
+import numpy as np
+import pytest
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+K = 2048
+
+
+def _topk(rows, k=K, standalone=True):
+    """rows: list of int32 arrays (one query row per request).  Runs dsa_topk
+    (twice on the same workspace, to check that no state leaks between calls)
+    and returns (idx [R, k], nsel [R])."""
+    import torch
+    import dsa_sparse_attention_03_gb300 as dsa
+    R = len(rows)
+    L_max = max(1, max(len(r) for r in rows))
+    lens = np.array([len(r) for r in rows], dtype=np.int32)
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    dev = "cuda"
+    scores = np.full((R, L_max), -123, dtype=np.int32)
+    for i, r in enumerate(rows):
+        scores[i, :len(r)] = r
+    t = dict(offsets=torch.from_numpy(offsets).to(dev),
+             row_offsets=torch.arange(R + 1, dtype=torch.int32, device=dev),
+             row_len=torch.from_numpy(lens).to(dev))
+    prob = dsa.Problem(R=R, B=R, H_i=64, D_i=128, H_q=64, D_k=576, D_v=512, k=k, L_max=L_max,
+                       L_total=int(offsets[-1]), softmax_scale=1.0, **t)
+    ws = dsa.alloc_workspace(prob)
+    ws.fill_(0xCD)
+    s_dev = torch.from_numpy(scores).to(dev)
+    outs = []
+    for _ in range(2):
+        idx = torch.full((R, k), -9, dtype=torch.int32, device=dev)
+        nsel = torch.full((R,), -9, dtype=torch.int32, device=dev)
+        dsa.dsa_topk(prob, s_dev, idx, nsel, ws)
+        assert dsa.dsa_read_device_status(ws) == 0
+        outs.append((idx.cpu().numpy().astype(np.int64), nsel.cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    return outs[0]
+
+
+def _check(rows, k=K):
+    idx, nsel = _topk(rows, k)
+    for i, r in enumerate(rows):
+        ref = oracle.topk_indices(r, k)
+        assert nsel[i] == min(k, len(r))
+        assert np.array_equal(idx[i], ref), f"row {i}"
+
+
+def test_random_long_row_sampled_path():
+    rng = np.random.default_rng(3)
+    _check([rng.integers(-10**6, 10**6, 300000, dtype=np.int64).astype(np.int32)])
+
+
+def test_sample_positions_hold_the_top_scores():
+    # Positions on the sampling stride carry the largest scores, so the sample
+    # overestimates the threshold and too few positions survive.
+    L = 300000
+    stride = -(-L // 8192)
+    rng = np.random.default_rng(4)
+    s = rng.integers(0, 1000, L).astype(np.int32)
+    s[::stride] = 10**6 + np.arange(len(s[::stride]), dtype=np.int32)
+    _check([s])
+
+
+def test_top_scores_avoid_the_sample_positions():
+    # The sample sees only ordinary scores, so far more than 4096 survive.
+    L = 300000
+    stride = -(-L // 8192)
+    rng = np.random.default_rng(5)
+    s = rng.integers(0, 1000, L).astype(np.int32)
+    hot = np.arange(L)
+    hot = hot[hot % stride != 0][:20000]
+    s[hot] = 5000 + rng.integers(0, 10, len(hot))
+    _check([s])
+
+
+def test_all_equal_long_row_exact_path():
+    _check([np.full(100000, 42, dtype=np.int32)])
+
+
+def test_rows_of_every_kind_in_one_call():
+    rng = np.random.default_rng(6)
+    L = 150000
+    stride = -(-L // 8192)
+    hit = rng.integers(0, 50, L).astype(np.int32)
+    hit[::stride] = 10**5
+    rows = [rng.integers(-5000, 5000, L).astype(np.int32),   # sampled
+            hit,                                            # retried, heavy ties at the top
+            np.array([], dtype=np.int32),                   # empty
+            rng.integers(0, 3, 1500).astype(np.int32),      # shorter than k
+            rng.integers(-7, 7, 6000).astype(np.int32),     # whole row sampled: exact T, ties
+            np.full(9000, -1, dtype=np.int32)]              # ties beyond the survivor cap
+    _check(rows)
+
+
+def test_small_k_and_lengths_around_the_sample_size():
+    rng = np.random.default_rng(7)
+    rows = [rng.integers(-100, 100, n).astype(np.int32) for n in (8191, 8192, 8193, 20000)]
+    _check(rows, k=300)
