@@ -44,6 +44,24 @@ def _dist_env():
     return ws, rank, local
 
 
+def job_ms(ms, world, device):
+    """The job's time: the slowest rank's (max over ranks), seen by every rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_us_per_layer(ms_per_step, n_layers, world):
+    """Whole-job time per layer: `world` independent replicas each run a step
+    of n_layers in ms_per_step, so the job finishes world x n_layers layers."""
+    return ms_per_step * 1000.0 / n_layers / world
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle sampling during the timed region."""
 
@@ -203,13 +221,9 @@ def bench_ours(args):
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        dist.barrier()
+    ms = job_ms(ms, world, device)
     ms_per_step = ms / args.steps
-    us_per_layer = ms_per_step * 1000.0 / n_layers / world   # whole-job: N replicas in parallel
+    us_per_layer = job_us_per_layer(ms_per_step, n_layers, world)
     status = dsa.dsa_read_device_status(ws, stream=sp)
 
     # Dominant kernel: the indexer alone, back to back over the layers (a CUDA
