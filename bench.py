@@ -503,6 +503,62 @@ def _prefix(x, n):
                                row_len=np.array([n], dtype=np.int32))
 
 
+def bench_workload(args):
+    """One decode step of another workload (tiny, l64k, batch32, causal64),
+    replayed from a CUDA graph; reported per step (all rows of the step)."""
+    import torch
+    import dsa_sparse_attention_03_gb300 as dsa
+    world, rank, local = _dist_env()
+    if rank != 0:
+        return None
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    x = {"tiny": gen.tiny, "l64k": gen.l64k, "batch32": gen.batch32, "causal64": gen.causal64}[args.workload]()
+    qk = int(max(np.abs(x.q_idx.astype(np.int32)).max(), np.abs(x.k_idx.astype(np.int32)).max()))
+    prob, t = dsa.upload_inputs(x, device=device, qk_abs_max=qk)
+    ws = dsa.alloc_workspace(prob, device=device)
+    idx = torch.empty((x.R, x.k), dtype=torch.int32, device=device)
+    nsel = torch.empty((x.R,), dtype=torch.int32, device=device)
+    out = torch.empty((x.R, x.H_q, x.D_v), dtype=torch.int16, device=device)
+    stream = torch.cuda.Stream(device=device)
+    sp = stream.cuda_stream
+
+    def step():
+        dsa.dsa_decode_step(prob, idx, nsel, out, ws, stream=sp)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    reps = max(10, min(args.steps, 300))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / reps
+    status = dsa.dsa_read_device_status(ws, stream=sp)
+    n = nsel.cpu().numpy().astype(np.int64)
+    nbytes = int(x.L_total) * x.D_i + int(n.sum()) * x.D_k * 2 + x.R * x.H_q * x.D_k * 2
+    in_bytes = int(x.L_total) * (x.D_i + x.D_k * 2)
+    return {"metric": f"DSA decode-step us per step, {args.workload}", "value": round(us, 3),
+            "unit": "us/step", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
+            "higher_is_better": False, "dtype": "int8+bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "R": x.R, "B": x.B, "L_total": int(x.L_total),
+                       "k": x.k, "H_i": x.H_i, "D_i": x.D_i, "H_q": x.H_q, "D_k": x.D_k,
+                       "indexer": dsa.indexer_kind(prob), "cuda_graph": True,
+                       "l2": f"inputs {in_bytes / 1e6:.1f} MB ({'>' if in_bytes > 129e6 else '<'} L2, 129 MB); not flushed"},
+            "step_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "gpu_launches": reps * kernels_per_step(), "device_status": status}
+
+
 def bench_reference(args):
     """The oracle, as it stands, on the host cores.  One timed step is a decode
     step of one L=307200 layer, or -- when --steps is large -- of its first L'
@@ -552,6 +608,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--workload", default="l300k", choices=["l300k", "l64k", "tiny", "batch32", "causal64"],
+                    help="l300k: the metric's 11-layer long-context step (default); the others time one "
+                         "decode step of that workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers per token (the headline workload runs 11)")
@@ -560,7 +619,12 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    res = bench_reference(args) if args.impl == "reference" else bench_ours(args)
+    if args.impl == "reference":
+        res = bench_reference(args)
+    elif args.workload != "l300k":
+        res = bench_workload(args)
+    else:
+        res = bench_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 
