@@ -179,6 +179,7 @@ __device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys
   __shared__ uint32_t tmp[NT / 32];
   __shared__ uint32_t res[2];
   __shared__ uint32_t n_list;
+  __shared__ uint32_t tie8[8 * (NT / 32)];
   const int len = a.row_len[r];
   const int32_t* s = a.scores + (int64_t)r * a.L_max;
   const uint32_t bstar = st->bstar;
@@ -235,25 +236,36 @@ __device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys
       const int t = base0 + j * NT + threadIdx.x;
       vv[j] = t < len ? s[t] : 0;
     }
+    // Ties are numbered in index order: position t = base0 + j * NT + thread,
+    // so (j, warp, lane) order.  All eight ballots first, one barrier.
+    uint32_t tm[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int t = base0 + j * NT + threadIdx.x;
       const uint32_t u = ordered_key(vv[j]);
-      const bool gt = t < len && u > T;
-      const bool tie = t < len && u == T;
-      if (gt) keys[atomicAdd(&n_list, 1u)] = surv_key(u, t);
-      const uint32_t m = __ballot_sync(0xffffffffu, tie);
-      if (lane == 0) tmp[w] = __popc(m);
-      __syncthreads();
-      uint32_t pos = ties_done + __popc(m & lanemask_lt()), tot = 0;
-      for (int i = 0; i < NT / 32; ++i) {
-        if (i < w) pos += tmp[i];
-        tot += tmp[i];
-      }
-      if (tie && pos < k_rem) keys[n_gt + pos] = surv_key(u, t);
-      ties_done += tot;
-      __syncthreads();
+      if (t < len && u > T) keys[atomicAdd(&n_list, 1u)] = surv_key(u, t);
+      tm[j] = __ballot_sync(0xffffffffu, t < len && u == T);
+      if (lane == 0) tie8[j * (NT / 32) + w] = __popc(tm[j]);
     }
+    __syncthreads();
+    uint32_t before = ties_done;   // ties ahead of (j, warp w) in index order
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t tot = 0, mine = 0;
+      for (int i = 0; i < NT / 32; ++i) {
+        const uint32_t c = tie8[j * (NT / 32) + i];
+        if (i < w) mine += c;
+        tot += c;
+      }
+      const int t = base0 + j * NT + threadIdx.x;
+      if (tm[j] & (1u << lane)) {
+        const uint32_t pos = before + mine + __popc(tm[j] & lanemask_lt());
+        if (pos < k_rem) keys[n_gt + pos] = surv_key(ordered_key(vv[j]), t);
+      }
+      before += tot;
+    }
+    ties_done = before;
+    __syncthreads();   // tie8 is rewritten next
   }
 
   // Bitonic sort of the k winners, descending (zero keys pad to a power of two).
