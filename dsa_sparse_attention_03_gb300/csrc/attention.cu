@@ -51,6 +51,7 @@ struct AttnArgs {
   uint32_t* acnt;     // [R, head group, 16] arrivals per column slice (zeroed)
   int Kc;             // clusters per (row, head group)
   int B, H_q, D_k, D_v, k;
+  int L1;             // B == 1: the request's length (L_total), known on the host
   int qs, ks;         // shared-memory row strides (elements)
   float scale_log2;
 };
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   }
   pdl_wait();
   pdl_trigger();
-  if (tid == 0) req_s = row_request(a.row_offsets, a.B, r);
+  if (tid == 0 && a.B > 1) req_s = row_request(a.row_offsets, a.B, r);
   // This CTA's selected positions (masked below once n is known).
   const int32_t* idx_row = a.idx + (int64_t)r * a.k;
   for (int i = tid; i < kMaxTiles * kAttnRows; i += kThreads) {
@@ -170,9 +171,10 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
     idx_s[i] = p < a.k ? idx_row[p] : -1;
   }
   __syncthreads();
-  const int b = req_s;
-  const int64_t base = a.offsets[b];
-  const int L_b = a.offsets[b + 1] - a.offsets[b];
+  // One request: offsets = {0, L_total} (documented), no lookups.
+  const int b = a.B > 1 ? req_s : 0;
+  const int64_t base = a.B > 1 ? a.offsets[b] : 0;
+  const int L_b = a.B > 1 ? a.offsets[b + 1] - a.offsets[b] : a.L1;
   int n = a.nsel ? a.nsel[r] : min(a.k, a.row_len[r]);
   n = max(0, min(n, a.k));
   const int ntiles = (n + kAttnRows - 1) / kAttnRows;
@@ -549,6 +551,7 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
   a.apart = reinterpret_cast<float*>(ws + pl.off_apart);
   a.acnt = reinterpret_cast<uint32_t*>(ws + pl.off_acnt);
   a.B = p.B; a.H_q = p.H_q; a.D_k = p.D_k; a.D_v = p.D_v; a.k = p.k;
+  a.L1 = (int)p.L_total;
   a.scale_log2 = p.softmax_scale * 1.4426950408889634f;
 
   int NT = 2;
