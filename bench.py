@@ -7,6 +7,10 @@ heads over a 576-wide bf16 latent (512 value columns).  A step is one token:
 the fused decode step of all 11 layers.  The metric is microseconds per layer.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--kv bf16|fp8]
+
+"--kv fp8" runs the same workload over an FP8 E4M3 latent cache (one fp32
+scale per row), written from the same bf16 rows.
 
 One JSON line on stdout (rank 0).  The 11 layers hold 4.3 GB of inputs, far
 above the 129 MB L2, so every layer's keys and latent rows come from HBM.
@@ -115,7 +119,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make_layers(n_layers, L, device):
+def kv_row_bytes(x):
+    """Bytes of one cached latent row as stored (FP8: codes plus the row's scale)."""
+    return x.D_k + 4 if x.kv_format == "e4m3" else x.D_k * 2
+
+
+def make_layers(n_layers, L, device, kv="bf16"):
     """n_layers independent layers whose inputs sit in one device tensor per
     kind (layer i is slice i), so a step can move every layer's inputs with
     one copy per kind."""
@@ -123,7 +132,10 @@ def make_layers(n_layers, L, device):
     import dsa_sparse_attention_03_gb300 as dsa
     xs = [gen.l300k(layer=layer, L=L) if L == L_LONG else gen.l64k(layer=layer, L=L)
           for layer in range(n_layers)]
+    if kv == "fp8":
+        xs = [gen.fp8_cache(x) for x in xs]
     x0 = xs[0]
+    fp8 = x0.kv_format == "e4m3"
 
     def stack(name, arr_of, dtype):
         host = np.stack([np.ascontiguousarray(arr_of(x)) for x in xs])
@@ -134,8 +146,11 @@ def make_layers(n_layers, L, device):
         "w_idx": stack("w_idx", lambda x: x.w_idx, torch.int32),
         "k_idx": stack("k_idx", lambda x: x.k_idx, torch.int8),
         "q": stack("q", lambda x: np.asarray(x.q).view(np.int16), torch.int16),
-        "kv": stack("kv", lambda x: np.asarray(x.kv).view(np.int16), torch.int16),
+        "kv": (stack("kv", lambda x: x.kv, torch.uint8) if fp8 else
+               stack("kv", lambda x: np.asarray(x.kv).view(np.int16), torch.int16)),
     }
+    if fp8:
+        packed["kv_scale"] = stack("kv_scale", lambda x: x.kv_scale, torch.float32)
     offsets = torch.from_numpy(x0.offsets).to(device)
     row_offsets = torch.from_numpy(x0.row_offsets).to(device)
     row_len = torch.from_numpy(x0.row_len).to(device)
@@ -147,7 +162,7 @@ def make_layers(n_layers, L, device):
         prob = dsa.Problem.from_tensors(k=x.k, D_v=x.D_v, softmax_scale=x.softmax_scale,
                                         L_max=int(np.max(x.row_len)), L_total=int(x.offsets[-1]),
                                         qk_abs_max=qk, offsets=offsets, row_offsets=row_offsets,
-                                        row_len=row_len, **t)
+                                        row_len=row_len, kv_fp8=fp8, **t)
         layers.append((x, prob, t))
     layers[0][2]["_packed"] = packed
     ws = dsa.alloc_workspace(layers[0][1], device=device)   # same sizes for every layer
@@ -178,8 +193,9 @@ def bench_ours(args):
     sp = stream.cuda_stream
 
     n_layers = args.layers
-    layers, ws, idx, nsel, out = make_layers(n_layers, L_LONG, device)
+    layers, ws, idx, nsel, out = make_layers(n_layers, L_LONG, device, kv=args.kv)
     x0 = layers[0][0]
+    kvb = kv_row_bytes(x0)
 
     def step():
         for i, (_, prob, _) in enumerate(layers):
@@ -269,8 +285,8 @@ def bench_ours(args):
         pass
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    step_bytes = n_layers * (L_LONG * x0.D_i + x0.k * x0.D_k * 2 + x0.H_q * x0.D_k * 2)
-    in_bytes = n_layers * L_LONG * (x0.D_i + x0.D_k * 2)
+    step_bytes = n_layers * (L_LONG * x0.D_i + x0.k * kvb + x0.H_q * x0.D_k * 2)
+    in_bytes = n_layers * L_LONG * (x0.D_i + kvb)
     step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
 
     stages = bench_stages(layers, ws, idx, nsel, out, stream) if not args.no_extras else None
@@ -278,20 +294,24 @@ def bench_ours(args):
 
     # The L = 65536 single-layer point of the metric: 12 independent layers
     # (1.0 GB, > 4x L2) rotated, one decode step per layer.
-    sec = bench_l64k(args, stream, device) if not args.no_extras else None
+    sec = bench_l64k(args, stream, device, kv=args.kv) if not args.no_extras else None
 
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
         return None
     res = {
-        "metric": METRIC, "value": round(us_per_layer, 3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC + ("" if args.kv == "bf16" else "; FP8 E4M3 latent cache"),
+        "value": round(us_per_layer, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8+bf16", "data": "synthetic",
+        "dtype": "int8+bf16" if args.kv == "bf16" else "int8+e4m3/bf16", "data": "synthetic",
         "config": {"workload": f"l300k: 1 query, L=307200, {n_layers} layers back to back; indexer 64x128 "
-                               "int8 (10% near-parallel keys), k=2048, 64 heads x 576 bf16 latent "
-                               "(D_v=512), scale 1/24",
+                               "int8 (10% near-parallel keys), k=2048, 64 heads x 576 "
+                               + ("bf16 latent" if args.kv == "bf16" else
+                                  "FP8 E4M3 latent with fp32 row scales") +
+                               " (D_v=512), scale 1/24",
+                   "kv": args.kv,
                    "layers": n_layers, "L": L_LONG, "k": x0.k, "batch": 1,
                    "l2": f"inputs {in_bytes / 1e9:.1f} GB > L2 (129 MB); not flushed", "cuda_graph": graph is not None,
                    "parallelism": f"replicas x{world}"},
@@ -385,8 +405,11 @@ def bench_e2e(args, layers, ws, idx, nsel, out, stream, device):
         "w_idx": torch.from_numpy(np.stack([x.w_idx for x in xs])).pin_memory(),
         "q": torch.from_numpy(np.stack([np.asarray(x.q).view(np.int16) for x in xs])).pin_memory(),
         "k_row": torch.from_numpy(np.stack([x.k_idx[-1] for x in xs])).pin_memory(),
-        "kv_row": torch.from_numpy(np.stack([np.asarray(x.kv[-1]).view(np.int16) for x in xs])).pin_memory(),
+        "kv_row": torch.from_numpy(np.stack([np.asarray(x.kv[-1]).view(np.int16) if x.kv_format == "bf16"
+                                             else np.asarray(x.kv[-1]) for x in xs])).pin_memory(),
     }
+    if "kv_scale" in packed:
+        host_in["kv_scale_row"] = torch.from_numpy(np.stack([x.kv_scale[-1:] for x in xs])).pin_memory()
     host_out = {"out": torch.empty(tuple(out.shape), dtype=torch.int16).pin_memory(),
                 "idx": torch.empty(tuple(idx.shape), dtype=torch.int32).pin_memory()}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
@@ -398,6 +421,8 @@ def bench_e2e(args, layers, ws, idx, nsel, out, stream, device):
         packed["q"].copy_(host_in["q"], non_blocking=True)
         packed["k_idx"][:, -1].copy_(host_in["k_row"], non_blocking=True)
         packed["kv"][:, -1].copy_(host_in["kv_row"], non_blocking=True)
+        if "kv_scale_row" in host_in:
+            packed["kv_scale"][:, -1:].copy_(host_in["kv_scale_row"], non_blocking=True)
         for i, (x, prob, t) in enumerate(layers):
             dsa.dsa_decode_step(prob, idx[i], nsel[i], out[i], ws, stream=sp)
         host_out["out"].copy_(out, non_blocking=True)
@@ -437,11 +462,11 @@ def bench_e2e(args, layers, ws, idx, nsel, out, stream, device):
             "eager_value": round(eager_ms * 1000.0 / len(layers), 3)}
 
 
-def bench_l64k(args, stream, device):
+def bench_l64k(args, stream, device, kv="bf16"):
     import torch
     import dsa_sparse_attention_03_gb300 as dsa
     n = 12
-    layers, ws, idx, nsel, out = make_layers(n, 65536, device)
+    layers, ws, idx, nsel, out = make_layers(n, 65536, device, kv=kv)
     sp = stream.cuda_stream
 
     def step(i):
@@ -473,9 +498,10 @@ def bench_l64k(args, stream, device):
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1000.0 / (reps * n)
     x0 = layers[0][0]
-    nbytes = 65536 * x0.D_i + x0.k * x0.D_k * 2 + x0.H_q * x0.D_k * 2
+    nbytes = 65536 * x0.D_i + x0.k * kv_row_bytes(x0) + x0.H_q * x0.D_k * 2
+    in_gb = n * 65536 * (x0.D_i + kv_row_bytes(x0)) / 1e9
     del layers, ws
-    return {"workload": "l64k: 1 query, L=65536, 1 layer (12 rotated layer buffers, 1.0 GB)",
+    return {"workload": f"l64k: 1 query, L=65536, 1 layer (12 rotated layer buffers, {in_gb:.1f} GB)",
             "us_per_layer": round(us, 3), "step_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
             "cuda_graph": graph is not None}
 
@@ -514,6 +540,8 @@ def bench_workload(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     x = {"tiny": gen.tiny, "l64k": gen.l64k, "batch32": gen.batch32, "causal64": gen.causal64}[args.workload]()
+    if args.kv == "fp8":
+        x = gen.fp8_cache(x)
     qk = int(max(np.abs(x.q_idx.astype(np.int32)).max(), np.abs(x.k_idx.astype(np.int32)).max()))
     prob, t = dsa.upload_inputs(x, device=device, qk_abs_max=qk)
     ws = dsa.alloc_workspace(prob, device=device)
@@ -546,12 +574,14 @@ def bench_workload(args):
     us = e0.elapsed_time(e1) * 1000.0 / reps
     status = dsa.dsa_read_device_status(ws, stream=sp)
     n = nsel.cpu().numpy().astype(np.int64)
-    nbytes = int(x.L_total) * x.D_i + int(n.sum()) * x.D_k * 2 + x.R * x.H_q * x.D_k * 2
-    in_bytes = int(x.L_total) * (x.D_i + x.D_k * 2)
-    return {"metric": f"DSA decode-step us per step, {args.workload}", "value": round(us, 3),
+    nbytes = int(x.L_total) * x.D_i + int(n.sum()) * kv_row_bytes(x) + x.R * x.H_q * x.D_k * 2
+    in_bytes = int(x.L_total) * (x.D_i + kv_row_bytes(x))
+    return {"metric": f"DSA decode-step us per step, {args.workload}" + ("" if args.kv == "bf16" else ", FP8 cache"),
+            "value": round(us, 3),
             "unit": "us/step", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
-            "higher_is_better": False, "dtype": "int8+bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "R": x.R, "B": x.B, "L_total": int(x.L_total),
+            "higher_is_better": False, "dtype": "int8+bf16" if args.kv == "bf16" else "int8+e4m3/bf16",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "kv": args.kv, "R": x.R, "B": x.B, "L_total": int(x.L_total),
                        "k": x.k, "H_i": x.H_i, "D_i": x.D_i, "H_q": x.H_q, "D_k": x.D_k,
                        "indexer": dsa.indexer_kind(prob), "cuda_graph": True,
                        "l2": f"inputs {in_bytes / 1e6:.1f} MB ({'>' if in_bytes > 129e6 else '<'} L2, 129 MB); not flushed"},
@@ -611,6 +641,8 @@ def main():
     ap.add_argument("--workload", default="l300k", choices=["l300k", "l64k", "tiny", "batch32", "causal64"],
                     help="l300k: the metric's 11-layer long-context step (default); the others time one "
                          "decode step of that workload")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="latent cache format: bf16 (default) or FP8 E4M3 with fp32 row scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers per token (the headline workload runs 11)")

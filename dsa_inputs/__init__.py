@@ -39,6 +39,13 @@ indexer)):
 * ``batch32``   : 32 requests, lengths U[4096, 131072], packed caches.
 * ``causal64``  : 64 causal query rows over L=131072 whose indexer keys come
                   from only 16 distinct vectors (heavy ties at the threshold).
+
+``fp8_cache(x)`` turns any of them into the same problem over an FP8 latent
+cache ("glm53-tensorfold-spark", page 4: FP8 KV storage), stored the way a cache
+writer would store it: per row j, scale_j = max_d |kv[j, d]| / 448 (float32;
+1 for an all-zero row) and code[j, d] = e4m3(kv[j, d] / scale_j), rounded to
+nearest even by PyTorch's float8_e4m3fn cast.  The decode step consumes the
+codes and scales as given; this writer is not part of it.
 """
 from __future__ import annotations
 
@@ -208,6 +215,10 @@ class DecodeInputs:
     offsets: np.ndarray
     row_offsets: np.ndarray
     row_len: np.ndarray
+    # "bf16": kv holds bf16 bits.  "e4m3": kv holds FP8 E4M3 codes (uint8) and
+    # kv_scale float32 [L_total] the per-row scales (None = all 1).
+    kv_format: str = "bf16"
+    kv_scale: Optional[np.ndarray] = None
 
     @property
     def L_total(self) -> int:
@@ -332,3 +343,25 @@ def causal64(L: int = 131072, R: int = 64, layer: int = 0, k: Optional[int] = No
         kw["k"] = k
     return make_inputs("causal64", seed=config_seed(5, layer), lengths=[L],
                        rows_per_request=[R], row_len=row_len, key_mode="distinct", **kw)
+
+
+def fp8_cache(x: DecodeInputs, with_scale: bool = True) -> DecodeInputs:
+    """The same problem over an FP8 E4M3 cache (codes uint8 [L_total, D_k] and
+    float32 per-row scales), written from ``x.kv`` as described in the module
+    docstring.  ``with_scale=False`` stores e4m3(kv) directly with no scales
+    (kv_scale None, i.e. all 1; N(0,1) rows stay far inside e4m3's range)."""
+    import torch
+
+    bits = np.ascontiguousarray(x.kv, dtype=np.uint16)
+    rows = torch.from_numpy((bits.astype(np.uint32) << np.uint32(16)).view(np.float32))
+    if with_scale:
+        amax = rows.abs().amax(dim=1) if rows.shape[1] else torch.zeros(rows.shape[0])
+        scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        y = (rows / scale[:, None]).clamp(-448.0, 448.0)
+        kv_scale = scale.numpy().astype(np.float32)
+    else:
+        y = rows.clamp(-448.0, 448.0)
+        kv_scale = None
+    codes = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return dataclasses.replace(x, name=x.name + "_fp8", kv=np.ascontiguousarray(codes),
+                               kv_format="e4m3", kv_scale=kv_scale)

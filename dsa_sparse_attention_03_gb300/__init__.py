@@ -40,6 +40,7 @@ DSA_INDEXER_AUTO = 0
 DSA_INDEXER_DP4A = 1
 DSA_INDEXER_TC = 2
 DSA_FLAG_NO_RELU = 0x100
+DSA_FLAG_KV_FP8 = 0x200
 
 INDEXERS = {"auto": DSA_INDEXER_AUTO, "dp4a": DSA_INDEXER_DP4A, "tc": DSA_INDEXER_TC}
 
@@ -61,6 +62,7 @@ class dsa_problem(ctypes.Structure):
         ("q_idx", ctypes.c_void_p), ("w_idx", ctypes.c_void_p), ("k_idx", ctypes.c_void_p),
         ("q", ctypes.c_void_p), ("kv", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
         ("row_offsets", ctypes.c_void_p), ("row_len", ctypes.c_void_p),
+        ("kv_scale", ctypes.c_void_p),
     ]
 
 
@@ -148,21 +150,22 @@ class Problem:
     @classmethod
     def from_tensors(cls, *, q_idx, w_idx, k_idx, q, kv, offsets, row_offsets, row_len, k,
                      softmax_scale, D_v=0, L_max=None, L_total=None, indexer="auto", relu=True,
-                     qk_abs_max=0, w_abs_max=0):
+                     qk_abs_max=0, w_abs_max=0, kv_fp8=False, kv_scale=None):
         R = int(row_len.shape[0])
         B = int(offsets.shape[0]) - 1
         if L_max is None:
             L_max = int(row_len.max().item()) if R else 0
         if L_total is None:
             L_total = int(offsets[-1].item())
-        flags = INDEXERS[indexer] | (0 if relu else DSA_FLAG_NO_RELU)
+        flags = (INDEXERS[indexer] | (0 if relu else DSA_FLAG_NO_RELU)
+                 | (DSA_FLAG_KV_FP8 if kv_fp8 else 0))
         H_i, D_i = (int(q_idx.shape[1]), int(q_idx.shape[2])) if q_idx is not None else (0, 0)
         H_q, D_k = (int(q.shape[1]), int(q.shape[2])) if q is not None else (0, 0)
         return cls(R=R, B=B, H_i=H_i, D_i=D_i, H_q=H_q, D_k=D_k, D_v=int(D_v), k=int(k),
                    L_max=int(L_max), flags=flags, L_total=int(L_total), qk_abs_max=qk_abs_max,
                    w_abs_max=w_abs_max, softmax_scale=float(softmax_scale), q_idx=q_idx,
                    w_idx=w_idx, k_idx=k_idx, q=q, kv=kv, offsets=offsets,
-                   row_offsets=row_offsets, row_len=row_len)
+                   row_offsets=row_offsets, row_len=row_len, kv_scale=kv_scale)
 
     def set(self, **kw):
         for f, v in kw.items():
@@ -181,24 +184,31 @@ class Problem:
 def upload_inputs(inp, device="cuda", indexer="auto", relu=True, qk_abs_max=0, w_abs_max=0):
     """Copy a host problem (numpy arrays named as in include/dsa.h: q_idx,
     w_idx, k_idx, q, kv, offsets, row_offsets, row_len, plus k, D_v,
-    softmax_scale) to ``device``.  Returns (Problem, dict of device tensors)."""
+    softmax_scale; an FP8 cache has ``kv_format == "e4m3"``, kv as uint8 codes
+    and ``kv_scale`` float32 or None) to ``device``.  Returns (Problem, dict of
+    device tensors)."""
     import numpy as np
     import torch
 
     def dev(a, dt):
         return torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dt)
 
+    fp8 = getattr(inp, "kv_format", "bf16") == "e4m3"
     t = dict(
         q_idx=dev(inp.q_idx, torch.int8), w_idx=dev(inp.w_idx, torch.int32),
         k_idx=dev(inp.k_idx, torch.int8),
         q=dev(np.asarray(inp.q).view(np.int16), torch.int16),
-        kv=dev(np.asarray(inp.kv).view(np.int16), torch.int16),
+        kv=(dev(np.asarray(inp.kv, dtype=np.uint8), torch.uint8) if fp8
+            else dev(np.asarray(inp.kv).view(np.int16), torch.int16)),
         offsets=dev(inp.offsets, torch.int32), row_offsets=dev(inp.row_offsets, torch.int32),
         row_len=dev(inp.row_len, torch.int32))
+    sc = getattr(inp, "kv_scale", None) if fp8 else None
+    t["kv_scale"] = None if sc is None else dev(np.asarray(sc, dtype=np.float32), torch.float32)
     L_max = int(np.max(inp.row_len)) if len(inp.row_len) else 0
     prob = Problem.from_tensors(k=inp.k, D_v=inp.D_v, softmax_scale=inp.softmax_scale,
                                 L_max=L_max, L_total=int(inp.offsets[-1]), indexer=indexer,
-                                relu=relu, qk_abs_max=qk_abs_max, w_abs_max=w_abs_max, **t)
+                                relu=relu, qk_abs_max=qk_abs_max, w_abs_max=w_abs_max,
+                                kv_fp8=fp8, **t)
     return prob, t
 
 

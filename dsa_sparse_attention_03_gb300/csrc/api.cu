@@ -44,6 +44,8 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   if (p->L_total < 0 || p->L_total >= (int64_t(1) << 31))
     return fail(DSA_ERR_UNSUPPORTED, "L_total=%lld outside [0,2^31)", (long long)p->L_total);
   if (p->k < 1 || p->k > kMaxK) return fail(DSA_ERR_UNSUPPORTED, "k=%d outside [1,%d]", p->k, kMaxK);
+  if (p->flags & ~(DSA_INDEXER_MASK | DSA_FLAG_NO_RELU | DSA_FLAG_KV_FP8))
+    return fail(DSA_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
   if (need && p->R > 0 && (!p->offsets || !p->row_offsets || !p->row_len))
     return fail(DSA_ERR_INVALID_ARG, "offsets/row_offsets/row_len must be set");
 
@@ -78,6 +80,8 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
       return fail(DSA_ERR_INVALID_ARG, "q/kv must be set");
     if (!aligned(p->q, 16) || !aligned(p->kv, 16))
       return fail(DSA_ERR_INVALID_ARG, "q/kv must be 16-byte aligned");
+    if ((p->flags & DSA_FLAG_KV_FP8) && !aligned(p->kv_scale, 4))
+      return fail(DSA_ERR_INVALID_ARG, "kv_scale must be 4-byte aligned");
     if (!(p->softmax_scale == p->softmax_scale) || p->softmax_scale <= 0.f)
       return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be positive");
   }
@@ -156,7 +160,7 @@ using namespace dsa;
 
 extern "C" {
 
-int dsa_version(void) { return 100; }
+int dsa_version(void) { return 101; }
 
 const char* dsa_last_error_string(void) { return g_err.c_str(); }
 

@@ -20,10 +20,21 @@
 //   even); with Kc > 1 each CTA writes its merged slice with (M, L) to the
 //   workspace, and the last of the Kc CTAs of slice x to arrive (an atomic
 //   counter, no waiting) merges the Kc slices in cluster order.
+//
+// FP8 cache (the FP8 KV storage of "glm53-tensorfold-spark", page 4): the rows
+// are e4m3 codes with one fp32 scale per row.  The bulk copies land the codes in
+// a staging buffer; all threads widen them to bf16 in the K buffer (exact: every
+// e4m3 value is a bf16 value), after which the staging buffer takes the next
+// tile's copies while this tile is computed.  The row scale s_j multiplies the
+// logit (z_j = scale * s_j * q . code_j) and the softmax weight of the P V
+// product (p_j s_j), both in fp32, so the result is attention over the
+// dequantised rows s_j * code_j.
 #include "common.cuh"
 
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math_constants.h>
 
 namespace dsa {
@@ -38,7 +49,8 @@ namespace cg = cooperative_groups;
 
 struct AttnArgs {
   const uint16_t* q;
-  const uint16_t* kv;
+  const uint16_t* kv;      // bf16 rows, or e4m3 bytes with F8
+  const float* kv_scale;   // F8: per-row scale, or null (= 1)
   const int32_t* offsets;
   const int32_t* row_offsets;
   const int32_t* row_len;
@@ -119,6 +131,26 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Sixteen e4m3 codes to sixteen bf16 values (eight packed pairs), exactly:
+// e4m3 -> f16 by the hardware conversion, f16 -> f32 -> bf16 lossless for
+// these values (at most 4 significant bits, exponents within both ranges).
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 v, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int hpair = 0; hpair < 2; ++hpair) {
+      const __nv_fp8x2_storage_t b = static_cast<__nv_fp8x2_storage_t>(w[i] >> (16 * hpair));
+      const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(b, __NV_E4M3));
+      const float2 f = __half22float2(h);
+      o[2 * i + hpair] = pack_bf16(f.x, f.y);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 __device__ int row_request(const int32_t* row_offsets, int B, int r) {
   int lo = 0, hi = B - 1;  // largest b with row_offsets[b] <= r
   while (lo < hi) {
@@ -129,7 +161,8 @@ __device__ int row_request(const int32_t* row_offsets, int B, int r) {
 }
 
 // NT: output n-tiles (of 8 columns) per warp; the 4 warps cover 32*NT >= D_v columns.
-template <int NT>
+// F8: the cache holds e4m3 codes and per-row scales.
+template <int NT, bool F8>
 __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);                          // [16][qs]
@@ -142,6 +175,8 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   float* invl = wts + 16 * kAttnHeads;                                      // [16]
   float* mlc = invl + kAttnHeads;                                           // [2][16]: cluster M, L
   int* idx_s = reinterpret_cast<int*>(mlc + 2 * kAttnHeads);               // [kMaxTiles][64]
+  float* sc_s = reinterpret_cast<float*>(idx_s + kMaxTiles * kAttnRows);     // F8: [kMaxTiles][64]
+  uint8_t* F8s = reinterpret_cast<uint8_t*>(sc_s + kMaxTiles * kAttnRows);  // F8: [64][D_k] codes
   float* Ob = reinterpret_cast<float*>(Kb);   // [16][D_v] partial O, after the tile loop
   __shared__ int req_s, last_s;
   __shared__ __align__(8) uint64_t bars[2];   // queries, K buffer
@@ -195,18 +230,20 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   // Whole rows by the bulk-copy engine, issued by warp 0: queries of this head
   // group (zero rows past H_q), then per tile its 64 selected latent rows
   // (zero rows where masked).  Each buffer's barrier counts the bytes.
-  const uint32_t rowb = (uint32_t)a.D_k * 2;
+  const uint32_t qrowb = (uint32_t)a.D_k * 2;
+  const uint32_t rowb = F8 ? (uint32_t)a.D_k : qrowb;
   if (warp == 0) {
     const int nq = min(kAttnHeads, a.H_q - h0);
-    if (lane == 0) mbar_expect_tx(bar_q, (uint32_t)nq * rowb);
+    if (lane == 0) mbar_expect_tx(bar_q, (uint32_t)nq * qrowb);
     __syncwarp();
     if (lane < nq)
-      bulk_row(smem_u32(Qs + lane * a.qs), a.q + ((int64_t)r * a.H_q + h0 + lane) * a.D_k, rowb, bar_q);
+      bulk_row(smem_u32(Qs + lane * a.qs), a.q + ((int64_t)r * a.H_q + h0 + lane) * a.D_k, qrowb, bar_q);
     else if (lane < kAttnHeads)
       for (int c8 = 0; c8 < a.D_k / 8; ++c8) *reinterpret_cast<int4*>(Qs + lane * a.qs + c8 * 8) = make_int4(0, 0, 0, 0);
   }
-  auto gather = [&](int i) {   // this CTA's tile i into the K buffer (warp 0)
+  auto gather = [&](int i) {   // this CTA's tile i into the K (F8: staging) buffer (warp 0)
     uint16_t* Ks = Kb;
+    const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(a.kv);
     const int* ids = idx_s + i * kAttnRows;
     const uint32_t bar = smem_u32(&bars[1]);
     const int t0 = ids[lane], t1 = ids[lane + 32];
@@ -217,13 +254,26 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int j = lane + 32 * h, t = h ? t1 : t0;
-      if (t >= 0)
-        bulk_row(smem_u32(Ks + j * a.ks), a.kv + (base + t) * a.D_k, rowb, bar);
-      else
-        for (int c8 = 0; c8 < a.D_k / 8; ++c8) *reinterpret_cast<int4*>(Ks + j * a.ks + c8 * 8) = make_int4(0, 0, 0, 0);
+      if (F8) {
+        if (t >= 0)
+          bulk_row(smem_u32(F8s + j * a.D_k), kv8 + (base + t) * a.D_k, rowb, bar);
+        else
+          for (int c16 = 0; c16 < a.D_k / 16; ++c16) *reinterpret_cast<int4*>(F8s + j * a.D_k + c16 * 16) = make_int4(0, 0, 0, 0);
+      } else {
+        if (t >= 0)
+          bulk_row(smem_u32(Ks + j * a.ks), a.kv + (base + t) * a.D_k, rowb, bar);
+        else
+          for (int c8 = 0; c8 < a.D_k / 8; ++c8) *reinterpret_cast<int4*>(Ks + j * a.ks + c8 * 8) = make_int4(0, 0, 0, 0);
+      }
     }
   };
   if (warp == 0 && my_tiles > 0) gather(0);
+  if (F8) {   // row scales of this CTA's positions (0 where masked), while the copies fly
+    for (int i = tid; i < my_tiles * kAttnRows; i += kThreads) {
+      const int t = idx_s[i];
+      sc_s[i] = t < 0 ? 0.f : (a.kv_scale ? __ldg(a.kv_scale + base + t) : 1.f);
+    }
+  }
   mbar_wait(bar_q, 0, a.status);
 
   float acc[NT][4];
@@ -233,11 +283,27 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   float l_run[2] = {0.f, 0.f};
 
   for (int i = 0; i < my_tiles; ++i) {
-    if (warp == 0 && i > 0) gather(i);   // the previous tile's math is done (barrier below)
+    if (!F8 && warp == 0 && i > 0) gather(i);   // the previous tile's math is done (barrier below)
     mbar_wait(smem_u32(&bars[1]), (uint32_t)i & 1u, a.status);
+    if (F8) {
+      // Widen the staged codes into the K buffer (the previous tile's math is
+      // done: barrier at the end of the loop), then hand the staging buffer to
+      // the next tile's copies.
+      const int chunks = a.D_k / 16;
+      for (int e = tid; e < kAttnRows * chunks; e += kThreads) {
+        const int row = e / chunks, ch = e - row * chunks;
+        uint4 lo, hi;
+        e4m3x16_to_bf16(*reinterpret_cast<const uint4*>(F8s + row * a.D_k + ch * 16), lo, hi);
+        *reinterpret_cast<uint4*>(Kb + row * a.ks + ch * 16) = lo;
+        *reinterpret_cast<uint4*>(Kb + row * a.ks + ch * 16 + 8) = hi;
+      }
+      __syncthreads();
+      if (warp == 0 && i + 1 < my_tiles) gather(i + 1);
+    }
     __syncthreads();
     const uint16_t* Ks = Kb;
     const int* ids = idx_s + i * kAttnRows;
+    const float* scs = sc_s + i * kAttnRows;
 
     // S = Q K^T for kv rows [warp*16, warp*16+16).
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -282,7 +348,8 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int col = warp * 16 + nt * 8 + 2 * c + (e & 1);
-        const float v = ids[col] >= 0 ? s[nt][e] * a.scale_log2 : -CUDART_INF_F;
+        const float sv = F8 ? s[nt][e] * scs[col] : s[nt][e];
+        const float v = ids[col] >= 0 ? sv * a.scale_log2 : -CUDART_INF_F;
         xv[nt][e] = v;
         mx[e >> 1] = fmaxf(mx[e >> 1], v);
       }
@@ -318,8 +385,10 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
         ps[e >> 1] += pv[e];
       }
       const int col = warp * 16 + nt * 8 + 2 * c;
-      *reinterpret_cast<uint32_t*>(Ps + g * kPStride + col) = pack_bf16(pv[0], pv[1]);
-      *reinterpret_cast<uint32_t*>(Ps + (g + 8) * kPStride + col) = pack_bf16(pv[2], pv[3]);
+      // F8: the weight of row j in O is p_j s_j (its sum l stays the plain p_j).
+      const float w0 = F8 ? scs[col] : 1.f, w1 = F8 ? scs[col + 1] : 1.f;
+      *reinterpret_cast<uint32_t*>(Ps + g * kPStride + col) = pack_bf16(pv[0] * w0, pv[1] * w1);
+      *reinterpret_cast<uint32_t*>(Ps + (g + 8) * kPStride + col) = pack_bf16(pv[2] * w0, pv[3] * w1);
     }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -516,9 +585,9 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   }
 }
 
-template <int NT>
+template <int NT, bool F8>
 cudaError_t launch_cluster(const AttnArgs& a, dim3 grid, int C, size_t smem, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<NT>,
+  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<NT, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -535,7 +604,7 @@ cudaError_t launch_cluster(const AttnArgs& a, dim3 grid, int C, size_t smem, cud
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<NT>, a);
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<NT, F8>, a);
 }
 
 }  // namespace
@@ -544,7 +613,9 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
                              const int32_t* nsel, uint16_t* out, float* lse, char* ws,
                              cudaStream_t st) {
   AttnArgs a;
-  a.q = p.q; a.kv = p.kv; a.offsets = p.offsets; a.row_offsets = p.row_offsets;
+  const bool f8 = (p.flags & DSA_FLAG_KV_FP8) != 0;
+  a.q = p.q; a.kv = p.kv; a.kv_scale = f8 ? p.kv_scale : nullptr;
+  a.offsets = p.offsets; a.row_offsets = p.row_offsets;
   a.row_len = p.row_len; a.idx = idx; a.nsel = nsel;
   a.out = out; a.lse = lse;
   a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
@@ -566,6 +637,7 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
                       2 * kAttnHeads * 4 + 16 * kAttnHeads * 8 + 16 * kAttnHeads * 4 + kAttnHeads * 4 +
                       2 * kAttnHeads * 4 +
                       (size_t)kMaxTiles * kAttnRows * 4;
+  if (f8) smem += (size_t)kMaxTiles * kAttnRows * 4 + (size_t)kAttnRows * p.D_k;   // scales, staging
   // Clusters of C CTAs, one 64-position tile per CTA; Kc clusters per (row,
   // head group) cover the k positions.  Clusters of 4 are placed one CTA per
   // SM (at least 116 KB of shared memory): two CTAs on an SM would share its
@@ -586,11 +658,19 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
   if (C <= 4 && per_kc * a.Kc <= 152 && smem < 116u * 1024u) smem = 116u * 1024u;
   // a.D_v / C must be even: D_v is a multiple of 32 and C <= 8.
   const dim3 grid(C * a.Kc, (p.H_q + kAttnHeads - 1) / kAttnHeads, p.R);
+  if (f8) {
+    switch (NT) {
+      case 2: return launch_cluster<2, true>(a, grid, C, smem, st);
+      case 4: return launch_cluster<4, true>(a, grid, C, smem, st);
+      case 8: return launch_cluster<8, true>(a, grid, C, smem, st);
+      default: return launch_cluster<16, true>(a, grid, C, smem, st);
+    }
+  }
   switch (NT) {
-    case 2: return launch_cluster<2>(a, grid, C, smem, st);
-    case 4: return launch_cluster<4>(a, grid, C, smem, st);
-    case 8: return launch_cluster<8>(a, grid, C, smem, st);
-    default: return launch_cluster<16>(a, grid, C, smem, st);
+    case 2: return launch_cluster<2, false>(a, grid, C, smem, st);
+    case 4: return launch_cluster<4, false>(a, grid, C, smem, st);
+    case 8: return launch_cluster<8, false>(a, grid, C, smem, st);
+    default: return launch_cluster<16, false>(a, grid, C, smem, st);
   }
 }
 

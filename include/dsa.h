@@ -44,7 +44,10 @@
  *   k_idx   int8  [L_total, D_i]  indexer key of each cached position, shared by
  *                                 all indexer heads; 16-byte aligned base
  *   q       bf16  [R, H_q, D_k]   attention queries (uint16 bit patterns)
- *   kv      bf16  [L_total, D_k]  latent cache rows; 16-byte aligned base
+ *   kv      bf16  [L_total, D_k]  latent cache rows; 16-byte aligned base.  With
+ *                                 DSA_FLAG_KV_FP8: e4m3 bytes [L_total, D_k]
+ *   kv_scale fp32 [L_total]       DSA_FLAG_KV_FP8 only: row j of the cache holds
+ *                                 kv_scale[j] * e4m3(kv[j, :]); NULL = all 1
  *   offsets     int32 [B+1]  cache rows of request b: offsets[b] .. offsets[b+1]-1;
  *                            offsets[0] = 0 and offsets[B] = L_total
  *   row_offsets int32 [B+1]  query rows of request b: row_offsets[b] .. row_offsets[b+1]-1;
@@ -97,6 +100,9 @@ typedef enum dsa_status {
 #define DSA_INDEXER_TC     2   /* tcgen05 tensor-core tiles (exact, fp16 operands) */
 #define DSA_INDEXER_MASK   0xF
 #define DSA_FLAG_NO_RELU   0x100  /* score without the per-head max(0, .)        */
+#define DSA_FLAG_KV_FP8    0x200  /* latent cache stored as FP8 e4m3, one fp32
+                                     scale per row ("glm53-tensorfold-spark",
+                                     page 4: FP8 KV storage)                    */
 
 /*
  * One decode-step problem.  Sizes are host values; pointers are device pointers
@@ -117,7 +123,16 @@ typedef enum dsa_status {
  *            The host rejects (DSA_ERR_OVERFLOW_RISK) any problem whose bound
  *            H_i * w_abs_max * D_i * qk_abs_max^2 reaches 2^31: scores are int32.
  *   softmax_scale  multiplies q . k before the softmax
- *   flags    DSA_INDEXER_* | DSA_FLAG_NO_RELU
+ *   flags    DSA_INDEXER_* | DSA_FLAG_NO_RELU | DSA_FLAG_KV_FP8
+ *   kv_scale read only with DSA_FLAG_KV_FP8 (so callers built against the
+ *            shorter struct of ABI 100, which never set that flag, still work)
+ *
+ * FP8 cache (DSA_FLAG_KV_FP8).  Byte (j, d) of kv is an OCP FP8 E4M3 code:
+ * sign, 4 exponent bits (bias 7), 3 mantissa bits; subnormals when the exponent
+ * field is 0; S.1111.111 is NaN; no infinities (largest finite 448).  The row's
+ * value is kv_scale[j] times the decoded code.  Attention is the same function
+ * of the dequantised rows as for a bf16 cache; the codes are widened exactly
+ * and the scale is applied in fp32 to the logits and the softmax weights.
  */
 typedef struct dsa_problem {
   int32_t R, B, H_i, D_i, H_q, D_k, D_v, k;
@@ -136,6 +151,7 @@ typedef struct dsa_problem {
   const int32_t* offsets;
   const int32_t* row_offsets;
   const int32_t* row_len;
+  const float* kv_scale;
 } dsa_problem;
 
 /* Library ABI version (major * 100 + minor). */
@@ -205,8 +221,8 @@ DSA_API dsa_status dsa_topk_static(const dsa_problem* p, const int32_t* scores, 
 /*
  * Step 3, sparse MLA attention over the selected rows only ("ds4
  * glm53-m3ultra", page 1; latent cache of "glm53-tensorfold-spark", page 4).
- * Reads q, kv, offsets, row_offsets, row_len, idx [R, k] and nsel [R] (NULL
- * means min(k, row_len[r]) entries per row).
+ * Reads q, kv (and kv_scale for an FP8 cache), offsets, row_offsets, row_len,
+ * idx [R, k] and nsel [R] (NULL means min(k, row_len[r]) entries per row).
  * An index outside [0, request length) is skipped and raises
  * DSA_DEVICE_BAD_INDEX.  Writes out [R, H_q, D_v] bf16 and, if non-NULL,
  * lse [R, H_q].  A row with no selected position gets zeros (lse = -inf).

@@ -13,7 +13,10 @@ int64 integers and float64 reals, no blocking and no reordering:
   full stable sort ("same positions selected, same order", page 1);
 * ``sparse_attention`` -- softmax attention of every query head over the
   selected latent rows only (page 1: "roughly 2,048 selected positions");
-* ``decode_step``     -- the three in sequence.
+* ``decode_step``     -- the three in sequence;
+* ``e4m3_to_f64``     -- the FP8 E4M3 code of the FP8 latent cache
+  ("glm53-tensorfold-spark", page 4: FP8 KV storage), decoded from the format's
+  definition.
 
 Readings where the pages are silent (each listed with its reason in the design
 notes): the indexer applies a per-head ReLU before weighting by ``w`` and summing
@@ -28,6 +31,7 @@ from .dsa import (  # noqa: F401
     sparse_attention,
     attention_lse,
     decode_step,
+    e4m3_to_f64,
     INT32_MIN,
     INT32_MAX,
 )

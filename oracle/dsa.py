@@ -7,7 +7,9 @@ Every function takes host numpy arrays in the library's layouts:
 ``k_idx`` int8 [L_total, D_i]  indexer keys, one per cached position (all heads)
 ``q``     bf16 bits [R, H_q, D_k] attention queries
 ``kv``    bf16 bits [L_total, D_k] latent cache rows (key = all D_k columns,
-                                value = the first D_v columns)
+                                value = the first D_v columns); for an FP8
+                                cache, E4M3 codes uint8 [L_total, D_k] with
+``kv_scale`` float32 [L_total] per-row scales (None = all 1)
 ``offsets`` [B+1]      cache rows of request b are offsets[b]..offsets[b+1]-1
 ``row_offsets`` [B+1]  query rows of request b are row_offsets[b]..row_offsets[b+1]-1
 ``row_len`` [R]        row r sees request-local positions 0..row_len[r]-1
@@ -29,6 +31,37 @@ def _row_request(row_offsets, R):
 
 def _bf16_to_f64(bits):
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def e4m3_to_f64(codes):
+    """Decode FP8 E4M3 codes (uint8) to float64, from the format's definition
+    (OCP 8-bit floating point, E4M3): bit 7 is the sign, bits 6..3 the exponent
+    field E (bias 7), bits 2..0 the mantissa M.  E = 0 encodes the subnormal
+    M/8 * 2**-6; otherwise the value is (1 + M/8) * 2**(E - 7), except that
+    E = 15 with M = 7 is NaN (the format has no infinities; the largest finite
+    value is 1.75 * 2**8 = 448).  The stored format of the FP8 KV cache of
+    "glm53-tensorfold-spark" (page 4), which does not name the variant; E4M3 is
+    the reading taken.
+    """
+    b = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    neg = (b >> 7) & 1
+    e = (b >> 3) & 15
+    m = (b & 7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    mag = np.where((e == 15) & ((b & 7) == 7), np.nan, mag)
+    return np.where(neg == 1, -mag, mag)
+
+
+def _kv_rows_f64(kv_req, sel, kv_scale_req):
+    """Rows ``sel`` of a request's cache as float64: bf16 bits widened exactly,
+    or E4M3 codes (uint8) decoded and multiplied by their row's scale."""
+    rows = np.asarray(kv_req)[sel]
+    if rows.dtype == np.uint8:
+        vals = e4m3_to_f64(rows)
+        if kv_scale_req is not None:
+            vals = vals * np.asarray(kv_scale_req, dtype=np.float64)[sel][:, None]
+        return vals
+    return _bf16_to_f64(rows)
 
 
 def indexer_scores(q_idx, w_idx, k_idx, offsets, row_offsets, row_len, relu=True, rows=None):
@@ -87,12 +120,14 @@ def topk_indices(scores, k):
     return out
 
 
-def sparse_attention(q_row, kv_req, idx, D_v, softmax_scale):
+def sparse_attention(q_row, kv_req, idx, D_v, softmax_scale, kv_scale_req=None):
     """Attention of every head of one query row over the selected latent rows.
 
     ``q_row`` bf16 bits [H_q, D_k]; ``kv_req`` bf16 bits [L_b, D_k] (the
-    request's own cache rows); ``idx`` the selected request-local positions
-    (entries < 0 are unused).  In float64, for head h:
+    request's own cache rows), or E4M3 codes uint8 [L_b, D_k] whose row j is
+    worth ``kv_scale_req[j]`` times the decoded codes (None = 1); ``idx`` the
+    selected request-local positions (entries < 0 are unused).  In float64,
+    with kv the rows' values, for head h:
 
         z_j  = softmax_scale * sum_{d < D_k} q[h, d] * kv[idx_j, d]
         p_j  = exp(z_j - max z) / sum_j' exp(z_j' - max z)
@@ -110,7 +145,7 @@ def sparse_attention(q_row, kv_req, idx, D_v, softmax_scale):
     if sel.size == 0:
         return np.zeros((H_q, D_v), dtype=np.float64)
     Q = _bf16_to_f64(q_row)                                   # [H_q, D_k]
-    K = _bf16_to_f64(kv_req[sel])                             # [n, D_k]
+    K = _kv_rows_f64(kv_req, sel, kv_scale_req)               # [n, D_k]
     z = softmax_scale * (Q @ K.T)                             # [H_q, n]
     z = z - z.max(axis=1, keepdims=True)
     e = np.exp(z)
@@ -118,7 +153,7 @@ def sparse_attention(q_row, kv_req, idx, D_v, softmax_scale):
     return p @ K[:, :D_v]                                     # [H_q, D_v]
 
 
-def attention_lse(q_row, kv_req, idx, softmax_scale):
+def attention_lse(q_row, kv_req, idx, softmax_scale, kv_scale_req=None):
     """Natural-log log-sum-exp of the scaled logits of each head over the
     selected rows, log(sum_j exp(z_j)) with z as in ``sparse_attention``;
     -inf when nothing is selected.  Returns float64 [H_q]."""
@@ -126,7 +161,7 @@ def attention_lse(q_row, kv_req, idx, softmax_scale):
     sel = sel[sel >= 0]
     if sel.size == 0:
         return np.full(q_row.shape[0], -np.inf)
-    z = softmax_scale * (_bf16_to_f64(q_row) @ _bf16_to_f64(kv_req[sel]).T)
+    z = softmax_scale * (_bf16_to_f64(q_row) @ _kv_rows_f64(kv_req, sel, kv_scale_req).T)
     m = z.max(axis=1)
     return m + np.log(np.exp(z - m[:, None]).sum(axis=1))
 
@@ -140,10 +175,12 @@ def decode_step(inp, relu=True, rows=None):
     scores = indexer_scores(inp.q_idx, inp.w_idx, inp.k_idx, inp.offsets, inp.row_offsets,
                             inp.row_len, relu=relu, rows=rows)
     idx = np.stack([topk_indices(s, inp.k) for s in scores]) if rows else np.zeros((0, inp.k), np.int64)
+    kv_scale = getattr(inp, "kv_scale", None)
     outs = []
     for j, r in enumerate(rows):
         b = int(req[r])
         lo, hi = int(inp.offsets[b]), int(inp.offsets[b + 1])
-        outs.append(sparse_attention(inp.q[r], inp.kv[lo:hi], idx[j], inp.D_v, inp.softmax_scale))
+        sc = None if kv_scale is None else kv_scale[lo:hi]
+        outs.append(sparse_attention(inp.q[r], inp.kv[lo:hi], idx[j], inp.D_v, inp.softmax_scale, sc))
     out = np.stack(outs) if outs else np.zeros((0, inp.H_q, inp.D_v))
     return scores, idx, out

@@ -32,9 +32,11 @@ def test_every_declared_symbol_is_exported(dsa):
 
 
 def test_struct_layout_matches_header(dsa):
-    assert ctypes.sizeof(dsa.dsa_problem) == 128
+    assert ctypes.sizeof(dsa.dsa_problem) == 136
     assert dsa.dsa_problem.L_total.offset == 40
     assert dsa.dsa_problem.q_idx.offset == 64
+    assert dsa.dsa_problem.kv_scale.offset == 128   # appended after the ABI-100 fields
+    assert dsa.dsa_version() == 101
 
 
 def _prob(dsa, **kw):
@@ -77,6 +79,15 @@ def test_host_validation_rejects_before_launch(dsa):
     assert b"2^31" in lib.dsa_last_error_string()
     assert lib.dsa_workspace_size(ctypes.byref(_prob(dsa, R=-1).c)) == 0
     assert b"R=-1" in lib.dsa_last_error_string()
+    assert status(flags=0x400) == dsa.DSA_ERR_INVALID_ARG          # unknown flag bit
+    assert b"flag" in lib.dsa_last_error_string()
+    p = _prob(dsa, flags=dsa.DSA_FLAG_KV_FP8)
+    for f in ("q_idx", "w_idx", "k_idx", "q", "kv", "offsets", "row_offsets", "row_len"):
+        setattr(p.c, f, fake)
+    p.c.kv_scale = fake + 2                                         # misaligned scales
+    assert lib.dsa_sparse_attn(ctypes.byref(p.c), fake, None, fake, None, ws, 1 << 40,
+                               None) == dsa.DSA_ERR_INVALID_ARG
+    assert b"kv_scale" in lib.dsa_last_error_string()
 
 
 def test_misaligned_and_small_workspace_rejected(dsa):

@@ -320,3 +320,102 @@ def test_attention_lse_closed_forms():
     np.testing.assert_allclose(oracle.attention_lse(qb, kvb, np.array([0, 1]), 0.25)[0],
                                math.log(math.exp(a) + math.exp(b)), rtol=1e-15)
     assert oracle.attention_lse(qb, kvb, np.array([-1]), 0.25)[0] == -np.inf
+
+
+# ---------------------------------------------------------------- FP8 cache
+
+def test_e4m3_decode_matches_library_for_all_codes():
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    a = oracle.e4m3_to_f64(codes)
+    b = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(a), np.isnan(b))
+    ok = ~np.isnan(a)
+    assert np.array_equal(a[ok], b[ok]) and np.array_equal(np.signbit(a[ok]), np.signbit(b[ok]))
+
+
+def test_e4m3_decode_named_values():
+    # OCP E4M3: bias 7, subnormals at E = 0, S.1111.111 NaN, max 448.
+    named = {0x00: 0.0, 0x38: 1.0, 0x40: 2.0, 0x3C: 1.5, 0x7E: 448.0, 0xFE: -448.0,
+             0x08: 2.0 ** -6, 0x07: 7 * 2.0 ** -9, 0x01: 2.0 ** -9, 0x81: -(2.0 ** -9),
+             0x77: 240.0, 0x78: 256.0}
+    got = oracle.e4m3_to_f64(np.array(list(named), np.uint8))
+    assert got.tolist() == list(named.values())
+    assert np.signbit(oracle.e4m3_to_f64(np.array([0x80], np.uint8))[0])
+    assert np.isnan(oracle.e4m3_to_f64(np.array([0x7F, 0xFF], np.uint8))).all()
+    # every finite non-NaN code is distinct and ordered within each sign
+    pos = oracle.e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))
+    assert (np.diff(pos) > 0).all()
+
+
+def _fp8_codes(vals):
+    import torch
+    return torch.tensor(np.asarray(vals, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_fp8_attention_two_rows_logistic_closed_form_with_scales():
+    # Row j is worth s_j * code_j: the scale must reach the logit and the value.
+    D = 32
+    c = np.zeros((2, D), np.float32)
+    c[0, 0], c[0, 1] = 2.0, 1.5
+    c[1, 0], c[1, 2] = -1.0, 3.0
+    codes = _fp8_codes(c)
+    s = np.array([0.3, 1.7], np.float32)
+    q = np.zeros((2, D), np.float32)
+    q[0, 0] = 1.0
+    q[1, 1], q[1, 2] = 0.5, -0.25
+    qb = _bf16(q)
+    scale = 0.75
+    o = oracle.sparse_attention(qb, codes, np.array([0, 1]), D, scale, kv_scale_req=s)
+    V = c.astype(np.float64) * s.astype(np.float64)[:, None]
+    Q = gen.bf16_bits_to_f64(qb)
+    for h in range(2):
+        z = scale * (Q[h] @ V.T)
+        p0 = 1.0 / (1.0 + math.exp(z[1] - z[0]))
+        np.testing.assert_allclose(o[h], p0 * V[0] + (1 - p0) * V[1], rtol=0, atol=1e-14)
+    lse = oracle.attention_lse(qb, codes, np.array([0, 1]), scale, kv_scale_req=s)
+    z = scale * (Q @ V.T)
+    np.testing.assert_allclose(lse, np.log(np.exp(z).sum(1)), rtol=1e-14)
+
+
+def test_fp8_attention_with_power_of_two_scales_equals_bf16_rows():
+    # s_j = 2^e_j: s_j * e4m3(code) is a bf16 value, so the FP8 problem is the
+    # bf16 problem over rows that the library's own conversion produces.
+    import torch
+    x = gen.fp8_cache(gen.l64k(L=400))
+    rng = np.random.default_rng(5)
+    s = np.exp2(rng.integers(-3, 3, x.L_total)).astype(np.float32)
+    rows = torch.from_numpy(x.kv).view(torch.float8_e4m3fn).to(torch.bfloat16)
+    rows = (rows * torch.from_numpy(s).to(torch.bfloat16)[:, None]).view(torch.int16).numpy().view(np.uint16)
+    idx = rng.choice(400, 150, replace=False)
+    a = oracle.sparse_attention(x.q[0], x.kv, idx, 512, 1 / 24, kv_scale_req=s)
+    b = oracle.sparse_attention(x.q[0], rows, idx, 512, 1 / 24)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
+    c = oracle.sparse_attention(x.q[0], x.kv, idx, 512, 1 / 24)          # scales dropped
+    assert np.abs(a - c).max() > 1e-3
+
+
+def test_fp8_cache_writer_round_trip_is_within_half_an_e4m3_step():
+    x = gen.l64k(L=500)
+    y = gen.fp8_cache(x)
+    assert y.kv.dtype == np.uint8 and y.kv.shape == x.kv.shape and y.kv_format == "e4m3"
+    assert not np.isin(y.kv, [0x7F, 0xFF]).any()
+    ref = gen.bf16_bits_to_f64(x.kv)
+    sc = y.kv_scale.astype(np.float64)[:, None]
+    back = oracle.e4m3_to_f64(y.kv) * sc
+    # relative half step 2^-4 for normals, absolute half of the subnormal step
+    assert (np.abs(back - ref) <= np.maximum(np.abs(ref) * 2.0 ** -4, sc * 2.0 ** -10) * 1.0001).all()
+    # each row's largest magnitude lands on the largest code
+    assert (np.abs(oracle.e4m3_to_f64(y.kv)).max(1) == 448.0).all()
+    z = gen.fp8_cache(x, with_scale=False)
+    assert z.kv_scale is None
+    np.testing.assert_allclose(oracle.e4m3_to_f64(z.kv), ref, rtol=2.0 ** -4, atol=2.0 ** -10)
+
+
+def test_fp8_decode_step_uses_the_scales():
+    x = gen.fp8_cache(gen.tiny(L=600))
+    _, idx, out = oracle.decode_step(x)
+    rows = oracle.e4m3_to_f64(x.kv) * x.kv_scale.astype(np.float64)[:, None]
+    sel = idx[0][idx[0] >= 0]
+    z = x.softmax_scale * (gen.bf16_bits_to_f64(x.q[0]) @ rows[sel].T)
+    np.testing.assert_allclose(out[0], sp_softmax(z, axis=1) @ rows[sel, :x.D_v], rtol=0, atol=1e-13)
