@@ -530,8 +530,9 @@ def _prefix(x, n):
 
 
 def bench_workload(args):
-    """One decode step of another workload (tiny, l64k, batch32, causal64),
-    replayed from a CUDA graph; reported per step (all rows of the step)."""
+    """One decode step of another workload (tiny, l64k, batch32, causal64, or a
+    2048-row prefill chunk), replayed from a CUDA graph; reported per step (all
+    rows of the step)."""
     import torch
     import dsa_sparse_attention_03_gb300 as dsa
     world, rank, local = _dist_env()
@@ -539,7 +540,8 @@ def bench_workload(args):
         return None
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    x = {"tiny": gen.tiny, "l64k": gen.l64k, "batch32": gen.batch32, "causal64": gen.causal64}[args.workload]()
+    x = {"tiny": gen.tiny, "l64k": gen.l64k, "batch32": gen.batch32, "causal64": gen.causal64,
+         "prefill": gen.prefill}[args.workload]()
     if args.kv == "fp8":
         x = gen.fp8_cache(x)
     qk = int(max(np.abs(x.q_idx.astype(np.int32)).max(), np.abs(x.k_idx.astype(np.int32)).max()))
@@ -638,7 +640,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--workload", default="l300k", choices=["l300k", "l64k", "tiny", "batch32", "causal64"],
+    ap.add_argument("--workload", default="l300k", choices=["l300k", "l64k", "tiny", "batch32", "causal64", "prefill"],
                     help="l300k: the metric's 11-layer long-context step (default); the others time one "
                          "decode step of that workload")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],

@@ -39,6 +39,10 @@ indexer)):
 * ``batch32``   : 32 requests, lengths U[4096, 131072], packed caches.
 * ``causal64``  : 64 causal query rows over L=131072 whose indexer keys come
                   from only 16 distinct vectors (heavy ties at the threshold).
+* ``prefill``   : a 2048-row causal prefill chunk at the end of a 10240-position
+                  context ("GLM-5.3-Flash-Alis-MLX-4bit", page 3: a prefill
+                  step of 2,048 tokens, and the gathered sparse prefill over
+                  query chunks), keys as ``l64k``.
 
 ``fp8_cache(x)`` turns any of them into the same problem over an FP8 latent
 cache ("glm53-tensorfold-spark", page 4: FP8 KV storage), stored the way a cache
@@ -343,6 +347,18 @@ def causal64(L: int = 131072, R: int = 64, layer: int = 0, k: Optional[int] = No
         kw["k"] = k
     return make_inputs("causal64", seed=config_seed(5, layer), lengths=[L],
                        rows_per_request=[R], row_len=row_len, key_mode="distinct", **kw)
+
+
+def prefill(L: int = 10240, R: int = 2048, layer: int = 0, k: Optional[int] = None) -> DecodeInputs:
+    """A prefill chunk: the last R positions of an L-position context are the
+    chunk's query rows; row i sees L - R + i + 1 positions (causal).  Keys as
+    ``l64k`` (10% near-parallel to the chunk's first query row)."""
+    row_len = np.arange(L - R + 1, L + 1, dtype=np.int32)
+    kw = dict(MLA)
+    if k is not None:
+        kw["k"] = k
+    return make_inputs("prefill", seed=config_seed(6, layer), lengths=[L],
+                       rows_per_request=[R], row_len=row_len, key_mode="near_parallel", **kw)
 
 
 def fp8_cache(x: DecodeInputs, with_scale: bool = True) -> DecodeInputs:

@@ -110,8 +110,7 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   // (row, head group) with more tiles uses several clusters (at most 8),
   // merged through per-slice partials and arrival counters.
   const int hgroups = p->H_q > 0 ? (p->H_q + kAttnHeads - 1) / kAttnHeads : 0;
-  const int tiles = (p->k + kAttnRows - 1) / kAttnRows;
-  P.attn_kc_max = (tiles + attn_cluster_size(p->k) - 1) / attn_cluster_size(p->k);
+  P.attn_kc_max = attn_clusters(p->R, hgroups, p->k);
   P.off_acnt = off; off = align_up(off + R * size_t(hgroups) * 16 * 4, 256);
   P.zero_end = off;
   P.off_surv = off; off = align_up(off + R * size_t(kCapFast) * 8, 256);

@@ -645,13 +645,11 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
   // critical path.  Clusters of 8 so padded would not all fit in one wave.
   const int tiles = (p.k + kAttnRows - 1) / kAttnRows;
   const int C = attn_cluster_size(p.k);
-  a.Kc = (tiles + C - 1) / C;
   // Many rows: fewer clusters per (row, head group), each CTA looping over
-  // several tiles, so the grid stays within about 600 CTAs (a few waves)
-  // instead of paying each CTA's fixed latency in dozens of waves.
+  // several tiles (the workspace holds partials for this many, no more).
   const int hgroups = (p.H_q + kAttnHeads - 1) / kAttnHeads;
   const int64_t per_kc = (int64_t)p.R * hgroups * C;
-  while (a.Kc > 1 && per_kc * a.Kc > 600) a.Kc = (a.Kc + 1) / 2;
+  a.Kc = attn_clusters(p.R, hgroups, p.k);
   if ((tiles + C * a.Kc - 1) / (C * a.Kc) > kMaxTiles) return cudaErrorInvalidConfiguration;
   if (a.Kc > pl.attn_kc_max || a.Kc > 8) return cudaErrorInvalidConfiguration;   // the merge holds <= 8
   // One CTA per SM while the grid fits in one wave.

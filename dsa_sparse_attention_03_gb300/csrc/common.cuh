@@ -54,6 +54,19 @@ __host__ __device__ inline int attn_cluster_size(int k) {
   return c;
 }
 
+// Clusters per (row, head group) for R rows, hgroups head groups and top-k k:
+// enough for one 64-position tile per CTA, halved while the grid exceeds about
+// 600 CTAs (a few waves), so that many rows make each CTA loop over several
+// tiles instead of paying each CTA's fixed latency in dozens of waves.
+inline int attn_clusters(int R, int hgroups, int k) {
+  const int tiles = (k + kAttnRows - 1) / kAttnRows;
+  const int C = attn_cluster_size(k);
+  int kc = (tiles + C - 1) / C;
+  const int64_t per_kc = (int64_t)R * hgroups * C;
+  while (kc > 1 && per_kc * kc > 600) kc = (kc + 1) / 2;
+  return kc;
+}
+
 // Order-preserving map of int32 onto uint32.
 __host__ __device__ __forceinline__ uint32_t ordered_key(int32_t s) {
   return static_cast<uint32_t>(s) ^ 0x80000000u;
