@@ -22,7 +22,10 @@
 //   rank    each survivor's rank is the number of survivors with a larger
 //           64-bit key (u << 32 | ~position).  Keys are unique, so the ranks
 //           are a permutation and sort by (score desc, position asc); a
-//           survivor with rank < k is written at idx[rank].
+//           survivor with rank < k is written at idx[rank].  This spreads one
+//           row's O(U^2) comparisons over many CTAs; once the rows alone fill
+//           the grid (R >= kSortRows) each CTA instead sorts whole rows'
+//           survivor keys (bitonic, O(U log^2 U)) and writes the first k.
 //   exact fallback  when the survivor list would exceed kCapFast (heavy ties
 //           at the threshold), one CTA resolves the row exactly: the
 //           candidates' key range, radix passes to the exact k-th key T,
@@ -40,6 +43,7 @@ constexpr int kRankLanes = kThreads / kRankSlice;          // threads per surviv
 constexpr int kRankSlices = kCapFast / kRankSlice;         // units per row (also covers idx[0, k))
 static_assert(kRankSlices * kRankSlice >= kMaxK, "rank units must cover idx");
 constexpr int kRadixBits = 11;
+constexpr int kSortRows = 8;                               // rank by per-row sort from this many rows
 constexpr uint64_t kGridWaitNs = 2000000000ull;            // grid barrier limit (2 s)
 
 enum Mode : uint32_t { kFast = 0, kAll = 1, kEmpty = 2, kExact = 3 };
@@ -169,6 +173,31 @@ __device__ void find_crossing(const uint32_t* h, int nbins, uint32_t need, uint3
   __syncthreads();
 }
 
+// Bitonic sort, descending, of keys[0, n) in shared memory (zero keys pad to a
+// power of two; every real key is nonzero).  All threads of the CTA; ends
+// with a barrier.
+__device__ void sort_desc(uint64_t* keys, int n0) {
+  constexpr int NT = kThreads;
+  int n = 1;
+  while (n < n0) n <<= 1;
+  for (int i = n0 + threadIdx.x; i < n; i += NT) keys[i] = 0;
+  __syncthreads();
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (n >> 1); i += NT) {
+        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+        const uint64_t x = keys[lo], y = keys[hi];
+        const bool desc = (lo & size) == 0;
+        if (desc ? (x < y) : (x > y)) {
+          keys[lo] = y;
+          keys[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
 // ------------------------------------------------------------------ exact fallback
 
 // One CTA resolves a row exactly: the candidates are the positions in bucket
@@ -268,25 +297,8 @@ __device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys
     __syncthreads();   // tie8 is rewritten next
   }
 
-  // Bitonic sort of the k winners, descending (zero keys pad to a power of two).
-  int n = 1;
-  while (n < a.k) n <<= 1;
-  for (int i = a.k + threadIdx.x; i < n; i += NT) keys[i] = 0;
   __syncthreads();
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (n >> 1); i += NT) {
-        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
-        const uint64_t x = keys[lo], y = keys[hi];
-        const bool desc = (lo & size) == 0;
-        if (desc ? (x < y) : (x > y)) {
-          keys[lo] = y;
-          keys[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
+  sort_desc(keys, a.k);
   int32_t* idx = a.idx + (size_t)r * a.k;
   for (int j = threadIdx.x; j < a.k; j += NT) idx[j] = key_pos(keys[j]);
 }
@@ -472,6 +484,30 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
     }
   }
   if (!grid_barrier(a.bar + nb++, a.status)) return;
+
+  // ---- rank by sort: whole rows per CTA (many rows).
+  if (a.R >= kSortRows) {
+    for (int r = blockIdx.x; r < a.R; r += gridDim.x) {
+      RowState* st = a.state + r;
+      const uint32_t mode = st->mode;
+      const int n_take = mode == kEmpty ? 0 : (int)st->n_take;
+      int32_t* idx = a.idx + (size_t)r * a.k;
+      if (threadIdx.x == 0 && a.nsel) a.nsel[r] = n_take;
+      if (mode == kExact) {
+        exact_row(a, st, r, keys);
+        __syncthreads();
+        continue;
+      }
+      const int U = mode == kEmpty ? 0 : (int)min(st->n_union, (uint32_t)kCapFast);
+      const uint64_t* surv = a.surv + (size_t)r * kCapFast;
+      __syncthreads();   // keys may still be read by the previous row
+      for (int i = threadIdx.x; i < U; i += kThreads) keys[i] = surv[i];
+      __syncthreads();
+      if (U > 1) sort_desc(keys, U);
+      for (int j = threadIdx.x; j < a.k; j += kThreads) idx[j] = j < n_take && j < U ? key_pos(keys[j]) : -1;
+    }
+    return;
+  }
 
   // ---- rank: units (row, slice of kRankSlice survivors), one warp per
   // survivor.  Units go out in runs of `run` consecutive units, run c to CTA
