@@ -57,3 +57,20 @@ def test_workload_shapes_and_structure():
     lens = np.diff(b.offsets)
     assert b.B == 32 and lens.min() >= 4096 and lens.max() <= 131072
     assert b.row_len.tolist() == lens.tolist()
+    p = gen.prefill(L=3000, R=512)
+    assert (p.R, p.B, p.L_total) == (512, 1, 3000)
+    assert p.row_len.tolist() == list(range(2489, 3001))
+    assert p.row_offsets.tolist() == [0, 512] and p.kv_format == "bf16" and p.kv_scale is None
+    near = (np.abs(p.k_idx.astype(int) - p.q_idx[0, 0].astype(int)[None]) <= 2).all(1)
+    assert 0.08 < near.mean() < 0.12
+
+
+def test_fp8_cache_keeps_everything_but_the_cache():
+    x = gen.l64k(L=700)
+    y = gen.fp8_cache(x)
+    for f in ("q_idx", "w_idx", "k_idx", "q", "offsets", "row_offsets", "row_len"):
+        assert np.array_equal(getattr(x, f), getattr(y, f)), f
+    assert y.kv.dtype == np.uint8 and y.kv_scale.dtype == np.float32 and y.kv_scale.shape == (700,)
+    assert (y.kv_scale > 0).all() and x.kv_format == "bf16"
+    # deterministic: the same problem gives the same codes
+    assert np.array_equal(gen.fp8_cache(gen.l64k(L=700)).kv, y.kv)
