@@ -65,3 +65,33 @@ def assert_out_close(got_bits, ref):
     err = np.abs(got - ref).max()
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert err <= ATOL and rel <= RTOL_L2, f"max|d|={err:.3e} relL2={rel:.3e}"
+
+
+def topk_properties(scores, idx, nsel, row_len, k):
+    """For every row: nsel = min(k, len); the selection is distinct positions
+    in range, ordered by (score desc, position asc), padded with -1; no
+    unselected position scores above the last selected score T; and of the
+    positions scoring exactly T, the lowest ones are the selected ones."""
+    for r in range(idx.shape[0]):
+        n = int(row_len[r])
+        m = min(k, n)
+        assert nsel[r] == m
+        sel = idx[r, :m]
+        assert (idx[r, m:] == -1).all()
+        if m == 0:
+            continue
+        assert sel.min() >= 0 and sel.max() < n and np.unique(sel).size == m
+        s = scores[r, :n].astype(np.int64)
+        key = s[sel]
+        assert (np.diff(key) <= 0).all(), f"row {r}: scores not descending"
+        eq = np.diff(key) == 0
+        assert (np.diff(sel)[eq] > 0).all(), f"row {r}: ties not by position"
+        if m < n:
+            T = key[-1]
+            rest = np.ones(n, bool)
+            rest[sel] = False
+            assert s[rest].max() <= T, f"row {r}: an unselected score beats the threshold"
+            tied_out = np.nonzero(rest & (s == T))[0]
+            tied_in = sel[key == T]
+            if tied_out.size:
+                assert tied_in.max() < tied_out.min(), f"row {r}: ties at T not lowest positions"

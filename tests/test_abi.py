@@ -105,3 +105,17 @@ def test_misaligned_and_small_workspace_rejected(dsa):
     p.c.k_idx = fake + 4
     st = lib.dsa_index_scores(ctypes.byref(p.c), fake, ctypes.c_void_p(fake + 16), need, None)
     assert st == dsa.DSA_ERR_INVALID_ARG and b"k_idx" in lib.dsa_last_error_string()
+
+
+def test_many_rows_reserve_no_cross_cluster_partials(dsa):
+    # With many rows the attention runs one cluster per (row, head group), so
+    # the workspace holds no cross-cluster partials: a 2048-row prefill chunk
+    # needs its scores (R x L_max x 4), survivor keys (R x 4096 x 8) and
+    # histograms, about 168 MB, not the 2.4 GB that 8 clusters' partials
+    # would add.
+    R, L = 2048, 10240
+    n = dsa.dsa_workspace_size(_prob(dsa, R=R, B=1, L_max=L, L_total=L))
+    assert R * L * 4 + R * 4096 * 8 < n < 200_000_000
+    # one decode row keeps them (8 clusters of 4 CTAs per head group)
+    one = dsa.dsa_workspace_size(_prob(dsa, R=1, B=1, L_max=L, L_total=L))
+    assert one > 4 * 8 * 16 * 512 * 4

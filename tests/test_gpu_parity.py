@@ -12,7 +12,7 @@ import pytest
 
 import dsa_inputs as gen
 import oracle
-from gpu_harness import assert_out_close, run_ops, run_step
+from gpu_harness import assert_out_close, run_ops, run_step, topk_properties
 
 pytestmark = pytest.mark.gpu
 
@@ -63,6 +63,7 @@ def test_batch32_varlen_sampled_rows():
     lens = np.diff(x.offsets)
     rows = sorted({0, 17, 31, int(np.argmin(lens)), int(np.argmax(lens))})
     _check_rows(x, res, rows)
+    topk_properties(res["scores"], res["idx"], res["nsel"], x.row_len, x.k)   # every row
 
 
 def test_causal64_heavy_ties_sampled_rows():
@@ -70,6 +71,7 @@ def test_causal64_heavy_ties_sampled_rows():
     res = run_ops(x)
     rows = [0, 1, 40, 63]
     _check_rows(x, res, rows)
+    topk_properties(res["scores"], res["idx"], res["nsel"], x.row_len, x.k)   # every row
     # the threshold really is ambiguous: more positions tie than are taken
     s = res["scores"][0, :x.row_len[0]]
     sel = res["idx"][0]

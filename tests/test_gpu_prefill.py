@@ -11,44 +11,16 @@ import pytest
 
 import dsa_inputs as gen
 import oracle
-from gpu_harness import assert_out_close, run_ops, run_step
+from gpu_harness import assert_out_close, run_ops, run_step, topk_properties
 
 pytestmark = pytest.mark.gpu
-
-
-def _topk_properties(scores, idx, nsel, row_len, k):
-    """For every row: nsel = min(k, len); the selection is distinct positions
-    in range, ordered by (score desc, position asc), padded with -1; no
-    unselected position scores above the last selected score T; and of the
-    positions scoring exactly T, the lowest ones are the selected ones."""
-    for r in range(idx.shape[0]):
-        n = int(row_len[r])
-        m = min(k, n)
-        assert nsel[r] == m
-        sel = idx[r, :m]
-        assert (idx[r, m:] == -1).all()
-        assert sel.min() >= 0 and sel.max() < n and np.unique(sel).size == m
-        s = scores[r, :n].astype(np.int64)
-        key = s[sel]
-        assert (np.diff(key) <= 0).all(), f"row {r}: scores not descending"
-        eq = np.diff(key) == 0
-        assert (np.diff(sel)[eq] > 0).all(), f"row {r}: ties not by position"
-        if m < n:
-            T = key[-1]
-            rest = np.ones(n, bool)
-            rest[sel] = False
-            assert s[rest].max() <= T, f"row {r}: an unselected score beats the threshold"
-            tied_out = np.nonzero(rest & (s == T))[0]
-            tied_in = sel[key == T]
-            if tied_out.size:
-                assert tied_in.max() < tied_out.min(), f"row {r}: ties at T not lowest positions"
 
 
 def test_prefill_chunk_2048_rows():
     x = gen.prefill()
     res = run_ops(x)
     assert res["status"] == 0
-    _topk_properties(res["scores"], res["idx"], res["nsel"], x.row_len, x.k)
+    topk_properties(res["scores"], res["idx"], res["nsel"], x.row_len, x.k)
     rows = [0, 1, 777, 2047]
     scores, idx, out = oracle.decode_step(x, rows=rows)
     for j, r in enumerate(rows):
