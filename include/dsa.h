@@ -82,7 +82,7 @@ extern "C" {
 typedef enum dsa_status {
   DSA_OK = 0,
   DSA_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size            */
-  DSA_ERR_UNSUPPORTED = 2,     /* valid but outside this build's shape limits  */
+  DSA_ERR_UNSUPPORTED = 2,     /* valid but outside the library's shape limits */
   DSA_ERR_OVERFLOW_RISK = 3,   /* declared value ranges could overflow int32   */
   DSA_ERR_CUDA = 4,            /* a CUDA runtime call failed                    */
   DSA_ERR_TIMEOUT = 5,         /* device: a bounded wait ran out (status bit)   */
