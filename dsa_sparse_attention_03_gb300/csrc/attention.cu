@@ -8,7 +8,10 @@
 //   z_j = scale * q[r,h,:] . kv[idx_j, :],  o[h,:] = sum_j softmax(z)_j kv[idx_j, :D_v]
 //
 // attn_cluster_kernel  grid (C * Kc, head group of 16, row), cluster (C, 1, 1)
-//   with C = 4 (k <= 2048) or 8, 4 warps.  The S = C * Kc CTAs of a (row, head group) split
+//   with C = 4 (k <= 2048) or 8, 4 warps.  With so many rows that one cluster
+//   serves each (row, head group), a CTA of 16 warps serves 64 heads instead
+//   (grid (C, H_q / 64, row)), so that each selected row is gathered once
+//   rather than once per head group of 16.  The S = C * Kc CTAs of a (row, head group) split
 //   the selected positions: CTA sp takes the tiles sp, sp + S, ... of 64
 //   positions (one tile at k = 2048).  It gathers the rows (one bulk copy per
 //   whole row, as the front-axis gather of "GLM-5.3-Flash-Alis-MLX-4bit",
@@ -160,24 +163,32 @@ __device__ int row_request(const int32_t* row_offsets, int B, int r) {
   return lo;
 }
 
-// NT: output n-tiles (of 8 columns) per warp; the 4 warps cover 32*NT >= D_v columns.
+// NT: output n-tiles (of 8 columns) per warp; 4 warps cover 32*NT >= D_v columns.
 // F8: the cache holds e4m3 codes and per-row scales.
-template <int NT, bool F8>
-__global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
+// HG: head groups of 16 per CTA (1, or 4 for many rows: each gathered tile then
+// serves 64 heads; warp w computes head group w / 4, columns (w % 4) * 8 * NT..).
+template <int NT, bool F8, int HG>
+__global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a) {
+  constexpr int NH = kAttnHeads * HG;   // heads per CTA
+  constexpr int NTH = kThreads * HG;    // threads per CTA (eight per head in the merge)
+  constexpr int NW = kWarps * HG;
+  static_assert(NTH == NH * 8, "merge: eight lanes per head");
   extern __shared__ __align__(16) unsigned char smem[];
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);                          // [16][qs]
-  uint16_t* Kb = Qs + kAttnHeads * a.qs;                                    // [64][ks]
-  uint16_t* Ps = Kb + kAttnRows * a.ks;                                     // [16][kPStride]
-  float* red = reinterpret_cast<float*>(Ps + kAttnHeads * kPStride);        // [2][4][16]
-  float* mls = red + 2 * kWarps * kAttnHeads;                               // [16][2]: m, l
-  float* mall = mls + 2 * kAttnHeads;                                       // [C][16][2]: every CTA's
-  float* wts = mall + 16 * kAttnHeads * 2;                                  // [C][16]
-  float* invl = wts + 16 * kAttnHeads;                                      // [16]
-  float* mlc = invl + kAttnHeads;                                           // [2][16]: cluster M, L
-  int* idx_s = reinterpret_cast<int*>(mlc + 2 * kAttnHeads);               // [kMaxTiles][64]
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);                          // [NH][qs]
+  uint16_t* Kb = Qs + NH * a.qs;                                            // [64][ks]
+  uint16_t* Ps = Kb + kAttnRows * a.ks;                                     // [HG][16][kPStride]
+  float* red = reinterpret_cast<float*>(Ps + NH * kPStride);                // [2][NW][16]
+  float* mls = red + 2 * NW * kAttnHeads;                                   // [NH][2]: m, l
+  float* mall = mls + 2 * NH;                                               // [16][NH][2]
+  float* wts = mall + 16 * NH * 2;                                          // [C][NH]
+  float* invl = wts + 16 * NH;                                              // [NH]
+  float* mlc = invl + NH;                                                   // [2][NH]: cluster M, L
+  int* idx_s = reinterpret_cast<int*>(mlc + 2 * NH);                       // [kMaxTiles][64]
   float* sc_s = reinterpret_cast<float*>(idx_s + kMaxTiles * kAttnRows);     // F8: [kMaxTiles][64]
   uint8_t* F8s = reinterpret_cast<uint8_t*>(sc_s + kMaxTiles * kAttnRows);  // F8: [64][D_k] codes
-  float* Ob = reinterpret_cast<float*>(Kb);   // [16][D_v] partial O, after the tile loop
+  // [NH][D_v] partial O after the tile loop: on the K buffer (HG = 1), or on
+  // the queries and the K buffer (HG = 4; 64 D_v floats <= (qs + ks) bf16 rows).
+  float* Ob = reinterpret_cast<float*>(HG == 1 ? reinterpret_cast<unsigned char*>(Kb) : smem);
   __shared__ int req_s, last_s;
   __shared__ __align__(8) uint64_t bars[2];   // queries, K buffer
 
@@ -188,8 +199,9 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   const int S = a.Kc * C;                    // position splits of the row
   const int sp = kc * C + x;                 // this CTA's split: tiles sp, sp + S, ...
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int hg = warp >> 2, wq = warp & 3;   // head group of the warp, its quarter
   const int g = lane >> 2, c = lane & 3;
-  const int r = blockIdx.z, h0 = blockIdx.y * kAttnHeads;
+  const int r = blockIdx.z, h0 = blockIdx.y * NH;
 
   const uint32_t bar_q = smem_u32(&bars[0]);
   if (tid == 0) {
@@ -201,7 +213,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   if (tid == 0 && a.B > 1) req_s = row_request(a.row_offsets, a.B, r);
   // This CTA's selected positions (masked below once n is known).
   const int32_t* idx_row = a.idx + (int64_t)r * a.k;
-  for (int i = tid; i < kMaxTiles * kAttnRows; i += kThreads) {
+  for (int i = tid; i < kMaxTiles * kAttnRows; i += NTH) {
     const int p = (sp + (i / kAttnRows) * S) * kAttnRows + (i % kAttnRows);
     idx_s[i] = p < a.k ? idx_row[p] : -1;
   }
@@ -214,7 +226,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   n = max(0, min(n, a.k));
   const int ntiles = (n + kAttnRows - 1) / kAttnRows;
   const int my_tiles = ntiles > sp ? (ntiles - sp + S - 1) / S : 0;   // <= kMaxTiles
-  for (int i = tid; i < my_tiles * kAttnRows; i += kThreads) {
+  for (int i = tid; i < my_tiles * kAttnRows; i += NTH) {
     const int p = (sp + (i / kAttnRows) * S) * kAttnRows + (i % kAttnRows);
     int t = idx_s[i];
     if (p >= n) {
@@ -233,13 +245,15 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   const uint32_t qrowb = (uint32_t)a.D_k * 2;
   const uint32_t rowb = F8 ? (uint32_t)a.D_k : qrowb;
   if (warp == 0) {
-    const int nq = min(kAttnHeads, a.H_q - h0);
+    const int nq = min(NH, a.H_q - h0);
     if (lane == 0) mbar_expect_tx(bar_q, (uint32_t)nq * qrowb);
     __syncwarp();
-    if (lane < nq)
-      bulk_row(smem_u32(Qs + lane * a.qs), a.q + ((int64_t)r * a.H_q + h0 + lane) * a.D_k, qrowb, bar_q);
-    else if (lane < kAttnHeads)
-      for (int c8 = 0; c8 < a.D_k / 8; ++c8) *reinterpret_cast<int4*>(Qs + lane * a.qs + c8 * 8) = make_int4(0, 0, 0, 0);
+    for (int hq = lane; hq < NH; hq += 32) {
+      if (hq < nq)
+        bulk_row(smem_u32(Qs + hq * a.qs), a.q + ((int64_t)r * a.H_q + h0 + hq) * a.D_k, qrowb, bar_q);
+      else
+        for (int c8 = 0; c8 < a.D_k / 8; ++c8) *reinterpret_cast<int4*>(Qs + hq * a.qs + c8 * 8) = make_int4(0, 0, 0, 0);
+    }
   }
   auto gather = [&](int i) {   // this CTA's tile i into the K (F8: staging) buffer (warp 0)
     uint16_t* Ks = Kb;
@@ -269,7 +283,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   };
   if (warp == 0 && my_tiles > 0) gather(0);
   if (F8) {   // row scales of this CTA's positions (0 where masked), while the copies fly
-    for (int i = tid; i < my_tiles * kAttnRows; i += kThreads) {
+    for (int i = tid; i < my_tiles * kAttnRows; i += NTH) {
       const int t = idx_s[i];
       sc_s[i] = t < 0 ? 0.f : (a.kv_scale ? __ldg(a.kv_scale + base + t) : 1.f);
     }
@@ -290,7 +304,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
       // done: barrier at the end of the loop), then hand the staging buffer to
       // the next tile's copies.
       const int chunks = a.D_k / 16;
-      for (int e = tid; e < kAttnRows * chunks; e += kThreads) {
+      for (int e = tid; e < kAttnRows * chunks; e += NTH) {
         const int row = e / chunks, ch = e - row * chunks;
         uint4 lo, hi;
         e4m3x16_to_bf16(*reinterpret_cast<const uint4*>(F8s + row * a.D_k + ch * 16), lo, hi);
@@ -311,8 +325,8 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
       // Two accumulator pairs (even and odd k-steps) halve the mma dependency chain.
       float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
-      const int brow = warp * 16 + (lane & 7) + (lane >> 4) * 8, bcol = ((lane >> 3) & 1) * 8;
-      const uint32_t aaddr = smem_u32(Qs + arow * a.qs + acol);
+      const int brow = wq * 16 + (lane & 7) + (lane >> 4) * 8, bcol = ((lane >> 3) & 1) * 8;
+      const uint32_t aaddr = smem_u32(Qs + (hg * kAttnHeads + arow) * a.qs + acol);
       const uint32_t baddr = smem_u32(Ks + brow * a.ks + bcol);
       const int nk = a.D_k / 16;
       int kk = 0;
@@ -347,7 +361,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int col = warp * 16 + nt * 8 + 2 * c + (e & 1);
+        const int col = wq * 16 + nt * 8 + 2 * c + (e & 1);
         const float sv = F8 ? s[nt][e] * scs[col] : s[nt][e];
         const float v = ids[col] >= 0 ? sv * a.scale_log2 : -CUDART_INF_F;
         xv[nt][e] = v;
@@ -358,8 +372,10 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
       mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 1));
       mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 2));
     }
+    // Per-warp partial max and sum of each head, reduced over the 4 warps of
+    // the head group (warps hg * 4 .. hg * 4 + 3).
     float* red_max = red;
-    float* red_sum = red + kWarps * kAttnHeads;
+    float* red_sum = red + NW * kAttnHeads;
     if (c == 0) {
       red_max[warp * kAttnHeads + g] = mx[0];
       red_max[warp * kAttnHeads + g + 8] = mx[1];
@@ -370,7 +386,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
     for (int j = 0; j < 2; ++j) {
       float tm = -CUDART_INF_F;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) tm = fmaxf(tm, red_max[w * kAttnHeads + g + 8 * j]);
+      for (int w = 0; w < kWarps; ++w) tm = fmaxf(tm, red_max[(hg * kWarps + w) * kAttnHeads + g + 8 * j]);
       m_new[j] = fmaxf(m_run[j], tm);
       alpha[j] = m_new[j] == -CUDART_INF_F ? 1.f : exp2f(m_run[j] - m_new[j]);
     }
@@ -384,11 +400,12 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
         pv[e] = (xv[nt][e] == -CUDART_INF_F) ? 0.f : exp2f(xv[nt][e] - mm);
         ps[e >> 1] += pv[e];
       }
-      const int col = warp * 16 + nt * 8 + 2 * c;
+      const int col = wq * 16 + nt * 8 + 2 * c;
       // F8: the weight of row j in O is p_j s_j (its sum l stays the plain p_j).
       const float w0 = F8 ? scs[col] : 1.f, w1 = F8 ? scs[col + 1] : 1.f;
-      *reinterpret_cast<uint32_t*>(Ps + g * kPStride + col) = pack_bf16(pv[0] * w0, pv[1] * w1);
-      *reinterpret_cast<uint32_t*>(Ps + (g + 8) * kPStride + col) = pack_bf16(pv[2] * w0, pv[3] * w1);
+      uint16_t* Pg = Ps + hg * kAttnHeads * kPStride;
+      *reinterpret_cast<uint32_t*>(Pg + g * kPStride + col) = pack_bf16(pv[0] * w0, pv[1] * w1);
+      *reinterpret_cast<uint32_t*>(Pg + (g + 8) * kPStride + col) = pack_bf16(pv[2] * w0, pv[3] * w1);
     }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -404,7 +421,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
     for (int j = 0; j < 2; ++j) {
       float ts = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) ts += red_sum[w * kAttnHeads + g + 8 * j];
+      for (int w = 0; w < kWarps; ++w) ts += red_sum[(hg * kWarps + w) * kAttnHeads + g + 8 * j];
       l_run[j] = l_run[j] * alpha[j] + ts;
       m_run[j] = m_new[j];
     }
@@ -413,11 +430,11 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
       acc[nt][0] *= alpha[0]; acc[nt][1] *= alpha[0];
       acc[nt][2] *= alpha[1]; acc[nt][3] *= alpha[1];
     }
-    // O += P V for output columns [warp*8*NT, (warp+1)*8*NT).
+    // O += P V for output columns [wq*8*NT, (wq+1)*8*NT) of head group hg.
     {
       const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
-      const uint32_t paddr = smem_u32(Ps + arow * kPStride + acol);
-      const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8, vcol = warp * 8 * NT + (lane >> 4) * 8;
+      const uint32_t paddr = smem_u32(Ps + (hg * kAttnHeads + arow) * kPStride + acol);
+      const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8, vcol = wq * 8 * NT + (lane >> 4) * 8;
       const uint32_t vaddr = smem_u32(Ks + vrow * a.ks + vcol);
 #pragma unroll
       for (int kq = 0; kq < kAttnRows / 16; ++kq) {
@@ -439,15 +456,15 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   // This CTA's unnormalised partial O, m and l, for the cluster to read.
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    float* dst = Ob + (g + 8 * j) * a.D_v;
+    float* dst = Ob + (hg * kAttnHeads + g + 8 * j) * a.D_v;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int col = warp * 8 * NT + nt * 8 + 2 * c;
+      const int col = wq * 8 * NT + nt * 8 + 2 * c;
       if (col < a.D_v) *reinterpret_cast<float2*>(dst + col) = make_float2(acc[nt][2 * j], acc[nt][2 * j + 1]);
     }
-    if (warp == 0 && c == 0) {
-      mls[(g + 8 * j) * 2] = m_run[j];
-      mls[(g + 8 * j) * 2 + 1] = l_run[j];
+    if (wq == 0 && c == 0) {
+      mls[(hg * kAttnHeads + g + 8 * j) * 2] = m_run[j];
+      mls[(hg * kAttnHeads + g + 8 * j) * 2 + 1] = l_run[j];
     }
   }
   cluster.sync();
@@ -470,28 +487,28 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
     float L = w * l;
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (cc < C) wts[cc * kAttnHeads + hh] = w;
+    if (cc < C) wts[cc * NH + hh] = w;
     if (cc == 0) {
       invl[hh] = L > 0.f ? 1.f / L : 0.f;
       mlc[hh] = M;
-      mlc[kAttnHeads + hh] = L;
+      mlc[NH + hh] = L;
       if (a.Kc == 1 && a.lse && x == 0 && h0 + hh < a.H_q)
         a.lse[(int64_t)r * a.H_q + h0 + hh] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
     }
   }
   __syncthreads();
   const int cs = a.D_v / C;            // columns of this CTA's slice (even: D_v % 32 == 0, C <= 8)
-  const int nq = kAttnHeads * (cs / 4);   // column quads of this slice (cs % 4 == 0)
-  const size_t pstride = 2 * kAttnHeads + (size_t)kAttnHeads * cs;
+  const int nq = NH * (cs / 4);   // column quads of this slice (cs % 4 == 0)
+  const size_t pstride = 2 * NH + (size_t)NH * cs;
   const size_t slot0 = (((size_t)r * gridDim.y + blockIdx.y) * a.Kc) * C + x;   // (kc' = 0, slice x)
   float* mypart = a.Kc > 1 ? a.apart + (slot0 + (size_t)kc * C) * pstride : nullptr;
   // Two quads per thread per sweep, all 2 x C remote loads issued before the
   // (CTA-ordered) accumulation.
-  for (int e0 = tid; e0 < nq; e0 += 2 * kThreads) {
+  for (int e0 = tid; e0 < nq; e0 += 2 * NTH) {
     float4 v[2][8];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const int e = e0 + u * kThreads;
+      const int e = e0 + u * NTH;
       const int hh = e / (cs / 4), col = x * cs + 4 * (e % (cs / 4));
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc)
@@ -500,21 +517,21 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const int e = e0 + u * kThreads;
+      const int e = e0 + u * NTH;
       if (e >= nq) continue;
       const int hh = e / (cs / 4), col = x * cs + 4 * (e % (cs / 4));
       float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc)
         if (cc < C) {
-          const float w = wts[cc * kAttnHeads + hh];
+          const float w = wts[cc * NH + hh];
           o.x += w * v[u][cc].x;
           o.y += w * v[u][cc].y;
           o.z += w * v[u][cc].z;
           o.w += w * v[u][cc].w;
         }
       if (a.Kc > 1) {
-        *reinterpret_cast<float4*>(mypart + 2 * kAttnHeads + hh * cs + (col - x * cs)) = o;
+        *reinterpret_cast<float4*>(mypart + 2 * NH + hh * cs + (col - x * cs)) = o;
       } else if (h0 + hh < a.H_q) {
         const float il = invl[hh];
         *reinterpret_cast<uint2*>(a.out + ((int64_t)r * a.H_q + h0 + hh) * a.D_v + col) =
@@ -522,7 +539,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
       }
     }
   }
-  if (a.Kc > 1 && tid < 2 * kAttnHeads) mypart[tid] = mlc[tid];
+  if (a.Kc > 1 && tid < 2 * NH) mypart[tid] = mlc[tid];
   cluster.sync();   // peers may still be reading this CTA's shared memory
   if (a.Kc == 1) return;
 
@@ -535,14 +552,14 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   __syncthreads();
   if (!last_s) return;
   __threadfence();
-  float* fw = mall;                    // [Kc][16] weights of the cluster partials
+  float* fw = mall;                    // [Kc][NH] weights of the cluster partials
   {
     const int hh = tid >> 3, q = tid & 7;   // Kc <= 8
     float m = -CUDART_INF_F, l = 0.f;
     if (q < a.Kc) {
       const float* pp = a.apart + (slot0 + (size_t)q * C) * pstride;
       m = __ldcg(pp + hh);
-      l = __ldcg(pp + kAttnHeads + hh);
+      l = __ldcg(pp + NH + hh);
     }
     float M = l > 0.f ? m : -CUDART_INF_F;
 #pragma unroll
@@ -551,7 +568,7 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
     float L = w * l;
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (q < a.Kc) fw[q * kAttnHeads + hh] = w;
+    if (q < a.Kc) fw[q * NH + hh] = w;
     if (q == 0) {
       invl[hh] = L > 0.f ? 1.f / L : 0.f;
       if (a.lse && x == 0 && h0 + hh < a.H_q)
@@ -559,19 +576,19 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
     }
   }
   __syncthreads();
-  for (int e = tid; e < nq; e += kThreads) {
+  for (int e = tid; e < nq; e += NTH) {
     const int hh = e / (cs / 4), cl = 4 * (e % (cs / 4));
     float4 v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
       if (q < a.Kc)
         v[q] = __ldcg(reinterpret_cast<const float4*>(
-            a.apart + (slot0 + (size_t)q * C) * pstride + 2 * kAttnHeads + hh * cs + cl));
+            a.apart + (slot0 + (size_t)q * C) * pstride + 2 * NH + hh * cs + cl));
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int q = 0; q < 8; ++q)
       if (q < a.Kc) {
-        const float w = fw[q * kAttnHeads + hh];
+        const float w = fw[q * NH + hh];
         o.x += w * v[q].x;
         o.y += w * v[q].y;
         o.z += w * v[q].z;
@@ -585,14 +602,14 @@ __global__ void __launch_bounds__(kThreads) attn_cluster_kernel(AttnArgs a) {
   }
 }
 
-template <int NT, bool F8>
+template <int NT, bool F8, int HG>
 cudaError_t launch_cluster(const AttnArgs& a, dim3 grid, int C, size_t smem, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<NT, F8>,
+  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<NT, F8, HG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kThreads * HG);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -604,7 +621,20 @@ cudaError_t launch_cluster(const AttnArgs& a, dim3 grid, int C, size_t smem, cud
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<NT, F8>, a);
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<NT, F8, HG>, a);
+}
+
+// Shared memory of a CTA serving hg head groups (the kernel's layout).
+size_t attn_smem(int hg, int qs, int ks, int D_k, int D_v, bool f8) {
+  const size_t nh = (size_t)kAttnHeads * hg, nw = (size_t)kWarps * hg;
+  const size_t qbytes = nh * qs * 2, kbytes = (size_t)kAttnRows * ks * 2;
+  const size_t obytes = nh * D_v * 4;   // partial O after the tile loop, aliased (see the kernel)
+  const size_t region = hg == 1 ? qbytes + (kbytes > obytes ? kbytes : obytes)
+                                : (qbytes + kbytes > obytes ? qbytes + kbytes : obytes);
+  size_t smem = region + nh * kPStride * 2 + 2 * nw * kAttnHeads * 4 + 2 * nh * 4 + 16 * nh * 8 +
+                16 * nh * 4 + nh * 4 + 2 * nh * 4 + (size_t)kMaxTiles * kAttnRows * 4;
+  if (f8) smem += (size_t)kMaxTiles * kAttnRows * 4 + (size_t)kAttnRows * D_k;   // scales, staging
+  return smem;
 }
 
 }  // namespace
@@ -630,14 +660,6 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
   const int cols = NT * 32;
   a.qs = p.D_k + 8;
   a.ks = (p.D_k > cols ? p.D_k : cols) + 8;
-  const size_t kbytes = (size_t)kAttnRows * a.ks * 2;    // one tile per CTA: one K buffer
-  const size_t obytes = (size_t)kAttnHeads * p.D_v * 4;   // partial O, aliased on the K buffers
-  size_t smem = (size_t)kAttnHeads * a.qs * 2 + (kbytes > obytes ? kbytes : obytes) +
-                      (size_t)kAttnHeads * kPStride * 2 + 2 * kWarps * kAttnHeads * 4 +
-                      2 * kAttnHeads * 4 + 16 * kAttnHeads * 8 + 16 * kAttnHeads * 4 + kAttnHeads * 4 +
-                      2 * kAttnHeads * 4 +
-                      (size_t)kMaxTiles * kAttnRows * 4;
-  if (f8) smem += (size_t)kMaxTiles * kAttnRows * 4 + (size_t)kAttnRows * p.D_k;   // scales, staging
   // Clusters of C CTAs, one 64-position tile per CTA; Kc clusters per (row,
   // head group) cover the k positions.  Clusters of 4 are placed one CTA per
   // SM (at least 116 KB of shared memory): two CTAs on an SM would share its
@@ -652,23 +674,41 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
   a.Kc = attn_clusters(p.R, hgroups, p.k);
   if ((tiles + C * a.Kc - 1) / (C * a.Kc) > kMaxTiles) return cudaErrorInvalidConfiguration;
   if (a.Kc > pl.attn_kc_max || a.Kc > 8) return cudaErrorInvalidConfiguration;   // the merge holds <= 8
+  // So many rows that one cluster serves each (row, 64 heads): one CTA per
+  // (row, position split) serves 4 head groups, so each selected row is
+  // gathered once instead of once per head group.  bf16 cache, H_q a multiple
+  // of 64.
+  const bool wide = !f8 && p.H_q % (4 * kAttnHeads) == 0 && a.Kc == 1 &&
+                    attn_clusters(p.R, p.H_q / (4 * kAttnHeads), p.k) == 1;
+  if (wide) {
+    const size_t smem = attn_smem(4, a.qs, a.ks, p.D_k, p.D_v, false);
+    if (smem > 227u * 1024u) return cudaErrorInvalidConfiguration;
+    const dim3 grid(C, p.H_q / (4 * kAttnHeads), p.R);
+    switch (NT) {
+      case 2: return launch_cluster<2, false, 4>(a, grid, C, smem, st);
+      case 4: return launch_cluster<4, false, 4>(a, grid, C, smem, st);
+      case 8: return launch_cluster<8, false, 4>(a, grid, C, smem, st);
+      default: return launch_cluster<16, false, 4>(a, grid, C, smem, st);
+    }
+  }
+  size_t smem = attn_smem(1, a.qs, a.ks, p.D_k, p.D_v, f8);
   // One CTA per SM while the grid fits in one wave.
   if (C <= 4 && per_kc * a.Kc <= 152 && smem < 116u * 1024u) smem = 116u * 1024u;
   // a.D_v / C must be even: D_v is a multiple of 32 and C <= 8.
-  const dim3 grid(C * a.Kc, (p.H_q + kAttnHeads - 1) / kAttnHeads, p.R);
+  const dim3 grid(C * a.Kc, hgroups, p.R);
   if (f8) {
     switch (NT) {
-      case 2: return launch_cluster<2, true>(a, grid, C, smem, st);
-      case 4: return launch_cluster<4, true>(a, grid, C, smem, st);
-      case 8: return launch_cluster<8, true>(a, grid, C, smem, st);
-      default: return launch_cluster<16, true>(a, grid, C, smem, st);
+      case 2: return launch_cluster<2, true, 1>(a, grid, C, smem, st);
+      case 4: return launch_cluster<4, true, 1>(a, grid, C, smem, st);
+      case 8: return launch_cluster<8, true, 1>(a, grid, C, smem, st);
+      default: return launch_cluster<16, true, 1>(a, grid, C, smem, st);
     }
   }
   switch (NT) {
-    case 2: return launch_cluster<2, false>(a, grid, C, smem, st);
-    case 4: return launch_cluster<4, false>(a, grid, C, smem, st);
-    case 8: return launch_cluster<8, false>(a, grid, C, smem, st);
-    default: return launch_cluster<16, false>(a, grid, C, smem, st);
+    case 2: return launch_cluster<2, false, 1>(a, grid, C, smem, st);
+    case 4: return launch_cluster<4, false, 1>(a, grid, C, smem, st);
+    case 8: return launch_cluster<8, false, 1>(a, grid, C, smem, st);
+    default: return launch_cluster<16, false, 1>(a, grid, C, smem, st);
   }
 }
 
