@@ -119,3 +119,20 @@ def test_many_rows_reserve_no_cross_cluster_partials(dsa):
     # one decode row keeps them (8 clusters of 4 CTAs per head group)
     one = dsa.dsa_workspace_size(_prob(dsa, R=1, B=1, L_max=L, L_total=L))
     assert one > 4 * 8 * 16 * 512 * 4
+
+
+def test_binding_marshals_fp8_cache_and_flags(dsa):
+    # Argument marshalling only (CPU tensors, nothing launched): an FP8 cache
+    # sets DSA_FLAG_KV_FP8 and passes the codes and the row scales.
+    import dsa_inputs as gen
+    x = gen.fp8_cache(gen.tiny(L=300))
+    prob, t = dsa.upload_inputs(x, device="cpu", indexer="dp4a", relu=False)
+    c = prob.c
+    assert c.flags == dsa.DSA_INDEXER_DP4A | dsa.DSA_FLAG_NO_RELU | dsa.DSA_FLAG_KV_FP8
+    assert c.kv == t["kv"].data_ptr() and t["kv"].dtype.itemsize == 1 and tuple(t["kv"].shape) == (300, 64)
+    assert c.kv_scale == t["kv_scale"].data_ptr() and t["kv_scale"].numel() == 300
+    assert (c.R, c.B, c.L_max, c.L_total, c.D_k, c.D_v, c.k) == (1, 1, 300, 300, 64, 64, 256)
+    y = gen.tiny(L=300)
+    prob2, t2 = dsa.upload_inputs(y, device="cpu")
+    assert prob2.c.flags == dsa.DSA_INDEXER_AUTO and not prob2.c.kv_scale
+    assert t2["kv"].dtype.itemsize == 2
