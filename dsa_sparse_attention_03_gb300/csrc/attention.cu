@@ -674,11 +674,11 @@ cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t
   a.Kc = attn_clusters(p.R, hgroups, p.k);
   if ((tiles + C * a.Kc - 1) / (C * a.Kc) > kMaxTiles) return cudaErrorInvalidConfiguration;
   if (a.Kc > pl.attn_kc_max || a.Kc > 8) return cudaErrorInvalidConfiguration;   // the merge holds <= 8
-  // So many rows that one cluster serves each (row, 64 heads): one CTA per
-  // (row, position split) serves 4 head groups, so each selected row is
-  // gathered once instead of once per head group.  bf16 cache, H_q a multiple
-  // of 64.
-  const bool wide = !f8 && p.H_q % (4 * kAttnHeads) == 0 && a.Kc == 1 &&
+  // So many rows that the grid of 16-head CTAs runs in many waves and one
+  // cluster serves each (row, 64 heads): one CTA per (row, position split)
+  // serves 4 head groups, so each selected row is gathered once instead of
+  // once per head group.  bf16 cache, H_q a multiple of 64.
+  const bool wide = !f8 && p.H_q % (4 * kAttnHeads) == 0 && a.Kc == 1 && per_kc > 600 &&
                     attn_clusters(p.R, p.H_q / (4 * kAttnHeads), p.k) == 1;
   if (wide) {
     const size_t smem = attn_smem(4, a.qs, a.ks, p.D_k, p.D_v, false);
