@@ -11,9 +11,9 @@
 //   with C = 4 (k <= 2048) or 8, 4 warps.  With so many rows that one cluster
 //   serves each (row, head group), a CTA of 16 warps serves 64 heads instead
 //   (grid (C, H_q / 64, row)), so that each selected row is gathered once
-//   rather than once per head group of 16.  The S = C * Kc CTAs of a (row, head group) split
-//   the selected positions: CTA sp takes the tiles sp, sp + S, ... of 64
-//   positions (one tile at k = 2048).  It gathers the rows (one bulk copy per
+//   rather than once per head group of 16.  The S = C * Kc CTAs of a (row,
+//   head group) split the selected positions: CTA sp takes the tiles sp,
+//   sp + S, ... of 64 positions (one tile at k = 2048).  It gathers the rows (one bulk copy per
 //   whole row, as the front-axis gather of "GLM-5.3-Flash-Alis-MLX-4bit",
 //   page 3), computes S = Q K^T and O += P V with bf16 mma.sync (fp32
 //   accumulation) and an online softmax in fp32 (log2 domain), and leaves its
