@@ -623,7 +623,7 @@ def bench_reference(args):
               f"time scaled by {L / n_pos:.2f}")
     return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(us * LAYERS / 1000.0, 3), "higher_is_better": False,
+            "ms_per_step": round(dt * 1000.0 / n, 3), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64", "data": "synthetic",
             "config": {"workload": "l300k: 1 query, L=307200 (one layer per timed step: a "
                                    "bounded sample of the 11-layer token)", "layers": LAYERS},

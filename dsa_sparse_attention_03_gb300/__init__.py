@@ -48,7 +48,10 @@ INDEXERS = {"auto": DSA_INDEXER_AUTO, "dp4a": DSA_INDEXER_DP4A, "tc": DSA_INDEXE
 EXPORTS = ("dsa_version", "dsa_last_error_string", "dsa_indexer_kind", "dsa_workspace_size",
            "dsa_index_scores",
            "dsa_topk", "dsa_topk_static", "dsa_sparse_attn", "dsa_decode_step",
-           "dsa_read_device_status")
+           "dsa_read_device_status", "dsa_get_device_status",
+           # include/dsa_testing.h
+           "dsa_test_topk_missing_arrival", "dsa_test_attn_missing_gather",
+           "dsa_test_indexer_missing_tile")
 
 
 class dsa_problem(ctypes.Structure):
@@ -91,6 +94,10 @@ def _load() -> ctypes.CDLL:
         ("dsa_sparse_attn", [P, vp, vp, vp, vp, vp, sz, vp]),
         ("dsa_decode_step", [P, vp, vp, vp, vp, sz, vp]),
         ("dsa_read_device_status", [vp, vp, ctypes.POINTER(ctypes.c_int32)]),
+        ("dsa_get_device_status", [vp, vp]),
+        ("dsa_test_topk_missing_arrival", [P, vp, vp, vp, vp, sz, ctypes.c_int, ctypes.c_int64, vp]),
+        ("dsa_test_attn_missing_gather", [P, vp, vp, vp, vp, vp, sz, ctypes.c_int64, vp]),
+        ("dsa_test_indexer_missing_tile", [P, vp, vp, sz, ctypes.c_int64, vp]),
     ):
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
@@ -265,6 +272,36 @@ def dsa_sparse_attn(prob: Problem, idx, nsel, out, lse, ws, stream=None) -> None
 def dsa_decode_step(prob: Problem, idx, nsel, out, ws, stream=None) -> None:
     _check(_lib.dsa_decode_step(ctypes.byref(prob.c), _ptr(idx), _ptr(nsel), _ptr(out),
                                 _ptr(ws), ws.numel(), _stream(stream)))
+
+
+# Test hooks (include/dsa_testing.h): one bounded device wait made to run out.
+
+def dsa_test_topk_missing_arrival(prob: Problem, scores, idx, nsel, ws, skip_cta, limit_ns,
+                                  stream=None) -> None:
+    _check(_lib.dsa_test_topk_missing_arrival(ctypes.byref(prob.c), _ptr(scores), _ptr(idx),
+                                              _ptr(nsel), _ptr(ws), ws.numel(), int(skip_cta),
+                                              int(limit_ns), _stream(stream)))
+
+
+def dsa_test_attn_missing_gather(prob: Problem, idx, nsel, out, lse, ws, limit_ns,
+                                 stream=None) -> None:
+    _check(_lib.dsa_test_attn_missing_gather(ctypes.byref(prob.c), _ptr(idx), _ptr(nsel),
+                                             _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                             int(limit_ns), _stream(stream)))
+
+
+def dsa_test_indexer_missing_tile(prob: Problem, scores, ws, limit_ns, stream=None) -> None:
+    _check(_lib.dsa_test_indexer_missing_tile(ctypes.byref(prob.c), _ptr(scores), _ptr(ws),
+                                              ws.numel(), int(limit_ns), _stream(stream)))
+
+
+def dsa_get_device_status(ws, stream=None) -> int:
+    """Synchronises the stream; returns DSA_OK, DSA_ERR_TIMEOUT or
+    DSA_ERR_DEVICE_INDEX from the device status word (raises on other errors)."""
+    st = _lib.dsa_get_device_status(_ptr(ws), _stream(stream))
+    if st not in (DSA_OK, DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX):
+        _check(st)
+    return st
 
 
 def dsa_read_device_status(ws, stream=None) -> int:

@@ -3,7 +3,6 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -145,9 +144,6 @@ dsa_status run_indexer(const dsa_problem& p, const Plan& pl, int32_t* scores, ch
 // Scratch of dsa_topk_static: the top-k's status block, row state, histograms
 // and survivor lists, for problems whose top-k scratch fits in 4 MiB.
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;
-constexpr int kMaxDevices = 64;
-std::mutex g_static_mu;
-void* g_static_ptr[kMaxDevices] = {};
 
 }  // namespace
 
@@ -229,23 +225,12 @@ dsa_status dsa_topk_static(const dsa_problem* p, const int32_t* scores, int32_t*
   if (p->R > 0 && (!idx || (p->L_max > 0 && !scores)))
     return fail(DSA_ERR_INVALID_ARG, "scores/idx is NULL");
   if (!aligned(scores, 16)) return fail(DSA_ERR_INVALID_ARG, "scores must be 16-byte aligned");
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "current device");
-  if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  // The array's device address in the current device's context, looked up on
+  // every call (it allocates nothing), so no stale address survives a device
+  // reset or a change of context.
   void* base = nullptr;
-  {
-    // First call on a device: look the scratch up once (no allocation).
-    std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_ptr[dev]) {
-      e = cudaGetSymbolAddress(&g_static_ptr[dev], g_topk_scratch);
-      if (e != cudaSuccess) {
-        g_static_ptr[dev] = nullptr;
-        return cuda_fail(e, "static scratch address");
-      }
-    }
-    base = g_static_ptr[dev];
-  }
+  cudaError_t e = cudaGetSymbolAddress(&base, g_topk_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The status block, row state and histograms must start at zero.
   e = cudaMemsetAsync(base, 0, pl.zero_end, st);
@@ -298,6 +283,83 @@ dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* nsel, ui
   e = launch_attention(*p, pl, idx, nsel, out, nullptr, w, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention");
   return DSA_OK;
+}
+
+// ------------------------------------------------------------------ test hooks
+
+static dsa_status check_limit(int64_t limit_ns, TestHooks* h) {
+  if (limit_ns <= 0 || limit_ns > 10000000000ll)
+    return fail(DSA_ERR_INVALID_ARG, "limit_ns=%lld outside (0, 1e10]", (long long)limit_ns);
+  h->wait_ns = (uint64_t)limit_ns;
+  return DSA_OK;
+}
+
+dsa_status dsa_test_topk_missing_arrival(const dsa_problem* p, const int32_t* scores, int32_t* idx,
+                                         int32_t* nsel, void* ws, size_t ws_bytes, int skip_cta,
+                                         int64_t limit_ns, void* stream) {
+  g_err.clear();
+  TestHooks h;
+  dsa_status s = check_limit(limit_ns, &h);
+  if (s != DSA_OK) return s;
+  Plan pl;
+  if ((s = make_plan(p, kNeedTopk, &pl)) != DSA_OK) return s;
+  if ((s = check_ws(pl, ws, ws_bytes)) != DSA_OK) return s;
+  if (p->R < 1 || !idx || !scores) return fail(DSA_ERR_INVALID_ARG, "need R >= 1, scores and idx");
+  if (skip_cta < 0) return fail(DSA_ERR_INVALID_ARG, "skip_cta=%d < 0", skip_cta);
+  h.topk_skip_cta = skip_cta;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, pl.zero_end, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
+  e = launch_topk(*p, pl, scores, idx, nsel, static_cast<char*>(ws), st, false, &h);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k");
+  return DSA_OK;
+}
+
+dsa_status dsa_test_attn_missing_gather(const dsa_problem* p, const int32_t* idx, const int32_t* nsel,
+                                        uint16_t* out, float* lse, void* ws, size_t ws_bytes,
+                                        int64_t limit_ns, void* stream) {
+  g_err.clear();
+  TestHooks h;
+  dsa_status s = check_limit(limit_ns, &h);
+  if (s != DSA_OK) return s;
+  Plan pl;
+  if ((s = make_plan(p, kNeedAttn, &pl)) != DSA_OK) return s;
+  if ((s = check_ws(pl, ws, ws_bytes)) != DSA_OK) return s;
+  if (p->R < 1 || !idx || !out) return fail(DSA_ERR_INVALID_ARG, "need R >= 1, idx and out");
+  if (!aligned(out, 8)) return fail(DSA_ERR_INVALID_ARG, "out must be 8-byte aligned");
+  h.attn_no_gather = 1;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, pl.zero_end, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
+  e = launch_attention(*p, pl, idx, nsel, out, lse, static_cast<char*>(ws), st, &h);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse attention");
+  return DSA_OK;
+}
+
+dsa_status dsa_test_indexer_missing_tile(const dsa_problem* p, int32_t* scores, void* ws,
+                                         size_t ws_bytes, int64_t limit_ns, void* stream) {
+  g_err.clear();
+  TestHooks h;
+  dsa_status s = check_limit(limit_ns, &h);
+  if (s != DSA_OK) return s;
+  Plan pl;
+  if ((s = make_plan(p, kNeedIndexer, &pl)) != DSA_OK) return s;
+  if ((s = check_ws(pl, ws, ws_bytes)) != DSA_OK) return s;
+  if (p->R < 1 || !scores) return fail(DSA_ERR_INVALID_ARG, "need R >= 1 and scores");
+  if (!aligned(scores, 16)) return fail(DSA_ERR_INVALID_ARG, "scores must be 16-byte aligned");
+  const int ix = p->flags & DSA_INDEXER_MASK;
+  if (ix == DSA_INDEXER_DP4A || !indexer_tc_tmem_operand(*p))
+    return fail(DSA_ERR_UNSUPPORTED, "the hook needs the tensor-memory-operand indexer");
+  h.indexer_no_load = 1;
+  cudaError_t e = launch_indexer_tc(*p, pl, scores, static_cast<char*>(ws),
+                                    static_cast<cudaStream_t>(stream), &h);
+  if (e != cudaSuccess) return cuda_fail(e, "indexer (tensor core)");
+  return DSA_OK;
+}
+
+dsa_status dsa_get_device_status(void* ws, void* stream) {
+  int32_t bits = 0;
+  return dsa_read_device_status(ws, stream, &bits);
 }
 
 dsa_status dsa_read_device_status(void* ws, void* stream, int32_t* bits) {

@@ -69,6 +69,8 @@ struct AttnArgs {
   int L1;             // B == 1: the request's length (L_total), known on the host
   int qs, ks;         // shared-memory row strides (elements)
   float scale_log2;
+  uint64_t wait_ns;   // bound of every mbarrier wait (then DSA_DEVICE_TIMEOUT)
+  int test_no_gather; // test hook: arm the first gather's barrier but issue no copy
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -112,8 +114,9 @@ __device__ __forceinline__ void bulk_row(uint32_t dst, const void* src, uint32_t
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
-// Bounded wait for the phase of parity `parity` (2 s; then DSA_DEVICE_TIMEOUT).
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
+// Bounded wait for the phase of parity `parity`: false (and DSA_DEVICE_TIMEOUT
+// raised, if `status`) once `limit_ns` have passed.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status, uint64_t limit_ns) {
   const uint64_t t0 = gtimer();
   for (;;) {
     uint32_t ok;
@@ -122,7 +125,7 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
         "selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     if (ok) return true;
-    if (gtimer() - t0 > 2000000000ull) {
+    if (gtimer() - t0 > limit_ns) {
       raise_status(status, DSA_DEVICE_TIMEOUT);
       return false;
     }
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
   // the queries and the K buffer (HG = 4; 64 D_v floats <= (qs + ks) bf16 rows).
   float* Ob = reinterpret_cast<float*>(HG == 1 ? reinterpret_cast<unsigned char*>(Kb) : smem);
   __shared__ int req_s, last_s;
+  __shared__ int bad_s;                        // a bounded wait of this CTA ran out
   __shared__ __align__(8) uint64_t bars[2];   // queries, K buffer
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -222,7 +226,9 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
   const int b = a.B > 1 ? req_s : 0;
   const int64_t base = a.B > 1 ? a.offsets[b] : 0;
   const int L_b = a.B > 1 ? a.offsets[b + 1] - a.offsets[b] : a.L1;
-  int n = a.nsel ? a.nsel[r] : min(a.k, a.row_len[r]);
+  const int rl = a.row_len[r];
+  const int lim = min(rl, L_b);              // valid positions of this row: [0, row_len)
+  int n = a.nsel ? a.nsel[r] : min(a.k, rl);
   n = max(0, min(n, a.k));
   const int ntiles = (n + kAttnRows - 1) / kAttnRows;
   const int my_tiles = ntiles > sp ? (ntiles - sp + S - 1) / S : 0;   // <= kMaxTiles
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
     int t = idx_s[i];
     if (p >= n) {
       t = -1;
-    } else if (t < 0 || t >= L_b) {
+    } else if (t < 0 || t >= lim) {
       raise_status(a.status, DSA_DEVICE_BAD_INDEX);
       t = -1;
     }
@@ -255,27 +261,31 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
         for (int c8 = 0; c8 < a.D_k / 8; ++c8) *reinterpret_cast<int4*>(Qs + hq * a.qs + c8 * 8) = make_int4(0, 0, 0, 0);
     }
   }
+  const uint32_t kbar = smem_u32(&bars[1]);
   auto gather = [&](int i) {   // this CTA's tile i into the K (F8: staging) buffer (warp 0)
     uint16_t* Ks = Kb;
     const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(a.kv);
     const int* ids = idx_s + i * kAttnRows;
-    const uint32_t bar = smem_u32(&bars[1]);
     const int t0 = ids[lane], t1 = ids[lane + 32];
     const uint32_t nv = __popc(__ballot_sync(0xffffffffu, t0 >= 0)) + __popc(__ballot_sync(0xffffffffu, t1 >= 0));
+    // Test hook: the barrier expects the tile's bytes but no copy is issued, so
+    // the wait for it runs out (no copy is in flight when it does).
+    const bool issue = !(a.test_no_gather && i == 0);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier zero fills of this buffer
-    if (lane == 0) mbar_expect_tx(bar, nv * rowb);
+    if (lane == 0) mbar_expect_tx(kbar, nv * rowb);
     __syncwarp();
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int j = lane + 32 * h, t = h ? t1 : t0;
+      const int j = lane + 32 * h, t = (h ? t1 : t0) >= 0 && !issue ? -2 : (h ? t1 : t0);
+      if (t == -2) continue;
       if (F8) {
         if (t >= 0)
-          bulk_row(smem_u32(F8s + j * a.D_k), kv8 + (base + t) * a.D_k, rowb, bar);
+          bulk_row(smem_u32(F8s + j * a.D_k), kv8 + (base + t) * a.D_k, rowb, kbar);
         else
           for (int c16 = 0; c16 < a.D_k / 16; ++c16) *reinterpret_cast<int4*>(F8s + j * a.D_k + c16 * 16) = make_int4(0, 0, 0, 0);
       } else {
         if (t >= 0)
-          bulk_row(smem_u32(Ks + j * a.ks), a.kv + (base + t) * a.D_k, rowb, bar);
+          bulk_row(smem_u32(Ks + j * a.ks), a.kv + (base + t) * a.D_k, rowb, kbar);
         else
           for (int c8 = 0; c8 < a.D_k / 8; ++c8) *reinterpret_cast<int4*>(Ks + j * a.ks + c8 * 8) = make_int4(0, 0, 0, 0);
       }
@@ -288,7 +298,18 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
       sc_s[i] = t < 0 ? 0.f : (a.kv_scale ? __ldg(a.kv_scale + base + t) : 1.f);
     }
   }
-  mbar_wait(bar_q, 0, a.status);
+  // A wait that runs out makes the CTA stop: it waits once more (bounded) for
+  // the copies it has in flight, computes nothing further, and its cluster
+  // writes no output for this (row, head group) (see the merge below).
+  const bool q_ok = mbar_wait(bar_q, 0, a.status, a.wait_ns);
+  int bad = __syncthreads_or(!q_ok);
+  if (bad) {
+    if (tid == 0) {
+      mbar_wait(bar_q, 0, nullptr, a.wait_ns);
+      if (my_tiles > 0) mbar_wait(kbar, 0, nullptr, a.wait_ns);
+    }
+    __syncthreads();
+  }
 
   float acc[NT][4];
 #pragma unroll
@@ -296,9 +317,15 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
   float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
   float l_run[2] = {0.f, 0.f};
 
-  for (int i = 0; i < my_tiles; ++i) {
+  for (int i = 0; i < my_tiles && !bad; ++i) {
     if (!F8 && warp == 0 && i > 0) gather(i);   // the previous tile's math is done (barrier below)
-    mbar_wait(smem_u32(&bars[1]), (uint32_t)i & 1u, a.status);
+    const bool ok = mbar_wait(kbar, (uint32_t)i & 1u, a.status, a.wait_ns);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) mbar_wait(kbar, (uint32_t)i & 1u, nullptr, a.wait_ns);   // drain this tile's copies
+      __syncthreads();
+      bad = 1;
+      break;
+    }
     if (F8) {
       // Widen the staged codes into the K buffer (the previous tile's math is
       // done: barrier at the end of the loop), then hand the staging buffer to
@@ -452,6 +479,13 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
     __syncthreads();  // the K buffer, Ps and red are rewritten next
   }
   __syncthreads();
+  if (bad) {   // a neutral partial: nothing of this CTA enters the merge
+#pragma unroll
+    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    m_run[0] = m_run[1] = -CUDART_INF_F;
+    l_run[0] = l_run[1] = 0.f;
+  }
+  if (tid == 0) bad_s = bad;
 
   // This CTA's unnormalised partial O, m and l, for the cluster to read.
 #pragma unroll
@@ -472,14 +506,18 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
   // Merge: weights exp2(m_c - M) per (CTA c, head), then columns of slice x.
   // Thread (head hh, CTA cc) reads that CTA's (m, l); eight lanes per head
   // reduce M and L with shuffles (C <= 8).
+  int cl_bad;   // some CTA of the cluster stopped on a wait that ran out
   {
     const int hh = tid >> 3, cc = tid & 7;
     float m = -CUDART_INF_F, l = 0.f;
+    int pb = 0;
     if (cc < C) {
       const float2 v = *reinterpret_cast<const float2*>(cluster.map_shared_rank(mls, cc) + hh * 2);
       m = v.x;
       l = v.y;
+      pb = *cluster.map_shared_rank(&bad_s, cc);
     }
+    cl_bad = __any_sync(0xffffffffu, pb);
     float M = l > 0.f ? m : -CUDART_INF_F;
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -492,7 +530,7 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
       invl[hh] = L > 0.f ? 1.f / L : 0.f;
       mlc[hh] = M;
       mlc[NH + hh] = L;
-      if (a.Kc == 1 && a.lse && x == 0 && h0 + hh < a.H_q)
+      if (a.Kc == 1 && a.lse && x == 0 && h0 + hh < a.H_q && !cl_bad)
         a.lse[(int64_t)r * a.H_q + h0 + hh] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
     }
   }
@@ -532,7 +570,7 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
         }
       if (a.Kc > 1) {
         *reinterpret_cast<float4*>(mypart + 2 * NH + hh * cs + (col - x * cs)) = o;
-      } else if (h0 + hh < a.H_q) {
+      } else if (h0 + hh < a.H_q && !cl_bad) {
         const float il = invl[hh];
         *reinterpret_cast<uint2*>(a.out + ((int64_t)r * a.H_q + h0 + hh) * a.D_v + col) =
             make_uint2(pack_bf16(o.x * il, o.y * il), pack_bf16(o.z * il, o.w * il));
@@ -545,10 +583,13 @@ __global__ void __launch_bounds__(kThreads * HG) attn_cluster_kernel(AttnArgs a)
 
   // Several clusters share (row, head group): the last to finish slice x merges
   // the Kc cluster partials of that slice, in cluster order.
+  // Word 15 of the (row, head group)'s counters marks a cluster that stopped
+  // on a wait that ran out; then no output is written for it.
+  uint32_t* cnt = a.acnt + ((size_t)r * gridDim.y + blockIdx.y) * 16;
+  if (tid == 0 && cl_bad) atomicOr(cnt + 15, 1u);
   __threadfence();
   __syncthreads();
-  if (tid == 0)
-    last_s = atomicAdd(a.acnt + ((size_t)r * gridDim.y + blockIdx.y) * 16 + x, 1u) == (uint32_t)(a.Kc - 1);
+  if (tid == 0) last_s = atomicAdd(cnt + x, 1u) == (uint32_t)(a.Kc - 1) && !(atomicOr(cnt + 15, 0u) & 1u);
   __syncthreads();
   if (!last_s) return;
   __threadfence();
@@ -641,8 +682,12 @@ size_t attn_smem(int hg, int qs, int ks, int D_k, int D_v, bool f8) {
 
 cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t* idx,
                              const int32_t* nsel, uint16_t* out, float* lse, char* ws,
-                             cudaStream_t st) {
+                             cudaStream_t st, const TestHooks* hooks) {
   AttnArgs a;
+  const TestHooks none;
+  if (!hooks) hooks = &none;
+  a.wait_ns = hooks->wait_ns;
+  a.test_no_gather = hooks->attn_no_gather;
   const bool f8 = (p.flags & DSA_FLAG_KV_FP8) != 0;
   a.q = p.q; a.kv = p.kv; a.kv_scale = f8 ? p.kv_scale : nullptr;
   a.offsets = p.offsets; a.row_offsets = p.row_offsets;

@@ -6,6 +6,7 @@
 #include <stddef.h>
 
 #include "dsa.h"
+#include "dsa_testing.h"
 
 namespace dsa {
 
@@ -141,19 +142,36 @@ __device__ __forceinline__ void row_minmax_flush(RowState* st, uint32_t umax, ui
   }
 }
 
+// Limit of every bounded device wait in normal operation.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+// Fault injection for the tests of the bounded waits (include/dsa_testing.h):
+// each hook makes one wait run out on purpose, with no copy in flight when it
+// does.  Normal calls pass none (nullptr).
+struct TestHooks {
+  uint64_t wait_ns = kDefaultWaitNs;   // limit of every bounded wait
+  int topk_skip_cta = -1;              // this top-k CTA returns before its first grid barrier
+  int attn_no_gather = 0;              // attention CTAs arm their first gather, issue no copy
+  int indexer_no_load = 0;             // indexer CTAs arm their first key tile, issue no copy
+};
+
 // Launchers (one per translation unit).  Each returns the launch error.
 // Both indexers also clear the workspace's status word, top-k state and
 // histograms ([0, Plan::zero_end)), so a decode step needs no separate memset.
 cudaError_t launch_indexer_dp4a(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                                 cudaStream_t st);
 cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
-                              cudaStream_t st);
+                              cudaStream_t st, const TestHooks* hooks = nullptr);
 bool indexer_tc_supported(const dsa_problem& p);
+// The tensor-core indexer keeps its A operand in tensor memory (D_i = 128, at
+// most 128 accumulator columns per tile, at least one full key tile).
+bool indexer_tc_tmem_operand(const dsa_problem& p);
 // minmax_done: the indexer already merged each row's key range into RowState.
 cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* scores,
-                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st, bool minmax_done);
+                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st, bool minmax_done,
+                        const TestHooks* hooks = nullptr);
 cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t* idx,
                              const int32_t* nsel, uint16_t* out, float* lse, char* ws,
-                             cudaStream_t st);
+                             cudaStream_t st, const TestHooks* hooks = nullptr);
 
 }  // namespace dsa

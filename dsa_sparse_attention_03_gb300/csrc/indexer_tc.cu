@@ -3,41 +3,52 @@
 // s[r, t] = sum_h w[r, h] * max(0, q_idx[r, h, :] . k_idx[t, :])   ("ds4
 // glm53-m3ultra", page 1: every cached position scored against the query).
 //
-// The 64 heads of a query share each 128-byte key, so scoring is a dense
-// contraction [keys x D_i] . [D_i x heads]: 8192 multiply-adds per key, which
-// CUDA-core dp4a cannot sustain at HBM speed.  Here the keys are the M = 128
-// rows of a tcgen05.mma tile and the group's query heads (up to 4 rows x 64
-// heads) are N; K = D_i.  sm_103a has no int8 MMA, so both operands are
-// widened to fp16 in shared memory, where every int8 is exact, and the fp32
-// accumulator keeps every per-head dot exact (the host checks the bound):
+// The heads of a query share each key, so scoring is a dense contraction
+// [keys x D_i] . [D_i x heads]: 8192 multiply-adds per 128-byte key at 64
+// heads.  The keys are the M = 128 rows of a tcgen05.mma tile, the query heads
+// of a group of up to four rows are N, and K = D_i.  sm_103a has no integer
+// MMA, so both operands are converted on chip to a float format that holds
+// every value exactly; the fp32 accumulator keeps every per-head dot exact
+// (the host checks the declared value bound):
 //
-//   exact conversion  k -> fp16(k): splice the biased byte into the mantissa
-//                     of 1024 and subtract 1152 (5 ops per 4 keys bytes);
-//   biased conversion k -> fp16(k + 1152) without the subtraction (3 ops per
-//                     4 bytes).  The MMA then returns q.k + 1152 * sum_d q_d,
-//                     and the epilogue removes the per-head constant exactly;
-//                     used when D_i * max|q| * 1279 < 2^24 keeps every partial
-//                     sum exact in fp32.
+//   e4m3 (kind::f8f6f4, K = 32 per MMA)  when D_i * qk^2 < 2^14: every |v| <= 16
+//                     is an e4m3 integer and every partial sum stays small;
+//   biased fp16       k -> fp16(k + 1152) by splicing the biased byte under the
+//                     exponent of 1024 (3 operations per 4 bytes); the MMA then
+//                     returns q.k + 1152 * sum_d q_d and the epilogue removes the
+//                     per-head constant; when D_i * qk * 1279 < 2^24;
+//   exact fp16        otherwise (the biased value minus 1152).
+// The epilogue turns max(d + c_h, 1.5 * 2^23) into integer bits (the magic
+// number add folds the ReLU and the bias removal into one fmax), applies the
+// weights with wrapping uint32 multiply-adds, and merges the row's key range
+// for the top-k.
 //
-// One persistent CTA per SM walks a contiguous range of 128-key tiles (the
-// tile list of all (request, row group) pairs), with warp roles:
-//   warp 0        TMA producer: cp.async.bulk of each int8 key tile (16 KB,
-//                 contiguous) into an S-stage ring, mbarrier complete_tx;
-//                 also allocates / frees TMEM.
-//   warp 1        MMA issuer (one thread): D[tmem] = A . B^T, K/16 MMAs per
-//                 tile, tcgen05.commit to the accumulator barrier.
-//   warps 2-5     converters: int8 tile -> fp16 A tile in the canonical K-major
-//                 128-byte-swizzled layout; queries -> fp16 B when the row
-//                 group changes.
-//   warps 6-13    epilogue, two groups of four taking alternate tiles (one per
-//                 TMEM accumulator buffer): tcgen05.ld of each key's head dots
-//                 (one TMEM lane per key), ReLU, weight, head sum in exact
-//                 int32, store, and the row's running key range for the top-k.
-// A is double-buffered and the accumulator 4-deep in TMEM (2-deep at N = 256),
-// so conversion, MMA and epilogue of consecutive tiles overlap the key stream.  Every mbarrier wait is bounded
-// (a few seconds of %globaltimer); on expiry the CTA sets DSA_DEVICE_TIMEOUT,
-// the other roles stop at their next wait, in-flight copies and MMAs are
-// drained (bounded) and TMEM is freed before exit.
+// indexer_tc_tm_kernel (D_i = 128, up to 128 accumulator columns per tile): the
+// A operand lives in tensor memory.  One persistent CTA per SM walks a
+// contiguous range of 128-key tiles (the tile list of all (request, row group)
+// pairs); key tiles arrive through the tensor map (TMA, 128-byte swizzle) in an
+// S-stage ring.  Warp roles:
+//   warp 0        TMA producer; allocates and frees tensor memory
+//   warps 1-4     MMA issuers, one per SM sub-partition, tile i to issuer i % 4,
+//                 each committing its tile to the accumulator's barrier
+//                 (epilogue) and to the A buffer's barrier (converters)
+//   warps 5-12    converters, two per sub-partition on alternate tiles: each
+//                 thread converts its key row (conflict-free under the swizzle)
+//                 and writes it into its tensor-memory lane with tcgen05.st;
+//                 each tile parity has its own B operand (the converted
+//                 queries), written while the key tile is still loading
+//   warps 13-20   epilogue, two groups of four on alternate tiles, reading the
+//                 accumulators 16 columns at a time with tcgen05.ld
+// Rings: S key stages, four A buffers, up to four accumulators.
+//
+// indexer_tc_kernel (D_i = 64, more accumulator columns, or caches shorter than
+// one tile): the A operand is staged in shared memory in the canonical K-major
+// 128-byte-swizzled layout by four converter warps; one MMA issuer; the same
+// epilogue.
+//
+// Every mbarrier wait is bounded (%globaltimer); on expiry the CTA sets
+// DSA_DEVICE_TIMEOUT, the other roles stop at their next wait, in-flight
+// copies and MMAs are drained (bounded) and tensor memory is freed before exit.
 #include "common.cuh"
 
 #include <cuda.h>
@@ -52,7 +63,6 @@ constexpr int kConvWarps = 4;
 constexpr int kEpiWarps = 8;                 // two groups of four
 constexpr int kThreads = (2 + kConvWarps + kEpiWarps) * 32;
 constexpr int kTile = 128;                   // keys per tile (MMA M)
-constexpr uint64_t kWaitNs = 4000000000ull;
 constexpr int kConvWarp0 = 2;
 constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
 constexpr int kMaxRG = 4;                    // query rows per MMA group (N <= 256)
@@ -99,6 +109,8 @@ struct TcArgs {
   int na;               // TMEM A buffers (TMEM-operand kernel)
   uint32_t b_stride;    // bytes between the two B buffers (TMEM-operand kernel)
   uint32_t a_col0;      // first TMEM column of the A buffers
+  uint64_t wait_ns;     // limit of every bounded wait
+  int test_no_load;     // test hook: arm the first key tile's barrier, issue no copy
   CUtensorMap tmap;     // k_idx as [L_total, 128] bytes, 128-byte swizzle
 };
 
@@ -145,14 +157,14 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase of parity `parity`; false if the CTA is aborting
 // or the wait ran out (which starts the abort).
 __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                      uint32_t* status) {
+                                      uint32_t* status, uint64_t limit_ns) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try(bar, parity)) return true;
     {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         raise_status(status, DSA_DEVICE_TIMEOUT);
         return false;
@@ -165,8 +177,8 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
 // proceeds only if all lanes succeeded, so it never diverges before the
 // .sync.aligned tcgen05 instructions that follow.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              uint32_t* status) {
-  const bool ok = wait_bar(bar, parity, abort_flag, status);
+                                              uint32_t* status, uint64_t limit_ns) {
+  const bool ok = wait_bar(bar, parity, abort_flag, status, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -513,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
     if (lane == 0) {
       for (int i = issued; i < n_local; ++i) {
         const int s = i % S;
-        if (i >= S && !wait_bar(bar_empty + 8 * s, ((i / S) - 1) & 1, abort_flag, a.status)) break;
+        if (i >= S && !wait_bar(bar_empty + 8 * s, ((i / S) - 1) & 1, abort_flag, a.status, a.wait_ns)) break;
         tile_step(a, prefix, t_begin + i, ti);
         const int rows = min(kTile, ti.L_b - ti.j * kTile);
         const uint32_t bytes = (uint32_t)rows * D_I;
@@ -525,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
       // Drain: every issued copy must have landed before the CTA can exit.
       for (int i = max(0, issued - S); i < issued; ++i) {
         const uint64_t t0 = globaltimer();
-        while (!mbar_try(bar_full + 8 * (i % S), (i / S) & 1) && globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try(bar_full + 8 * (i % S), (i / S) & 1) && globaltimer() - t0 < a.wait_ns) {
         }
       }
     }
@@ -539,9 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
         tile_step(a, prefix, t_begin + i, ti);
         const uint32_t idesc = idesc_f16(kTile, ti.nrows * a.H_i);
         if (i >= NACC &&
-            !wait_bar(bar_accempty + 8 * acc, ((i / NACC) - 1) & 1, abort_flag, a.status))
+            !wait_bar(bar_accempty + 8 * acc, ((i / NACC) - 1) & 1, abort_flag, a.status, a.wait_ns))
           break;
-        if (!wait_bar(bar_afull + 8 * abuf, (i >> 1) & 1, abort_flag, a.status)) break;
+        if (!wait_bar(bar_afull + 8 * abuf, (i >> 1) & 1, abort_flag, a.status, a.wait_ns)) break;
         tc_fence_after();
         const uint32_t a_base = cvta_smem(A + abuf * kABytes);
 #pragma unroll
@@ -556,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
       // Drain: the last MMAs must finish before TMEM is freed.
       for (int i = max(0, issued - NACC); i < issued; ++i) {
         const uint64_t t0 = globaltimer();
-        while (!mbar_try(bar_accfull + 8 * (i % NACC), (i / NACC) & 1) && globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try(bar_accfull + 8 * (i % NACC), (i / NACC) & 1) && globaltimer() - t0 < a.wait_ns) {
         }
       }
     }
@@ -571,14 +583,14 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
     for (int i = 0; i < n_local; ++i) {
       const int s = i % S, buf = i & 1;
       const bool new_group = tile_step(a, prefix, t_begin + i, ti);
-      if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status)) break;
+      if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status, a.wait_ns)) break;
       if (i >= 2 &&
-          !wait_bar_warp(bar_accfull + 8 * ((i - 2) % NACC), ((i - 2) / NACC) & 1, abort_flag, a.status))
+          !wait_bar_warp(bar_accfull + 8 * ((i - 2) % NACC), ((i - 2) / NACC) & 1, abort_flag, a.status, a.wait_ns))
         break;
       if (new_group) {
         // B may be rewritten once every issued MMA has finished.
         if (i >= 1 &&
-            !wait_bar_warp(bar_accfull + 8 * ((i - 1) % NACC), ((i - 1) / NACC) & 1, abort_flag, a.status))
+            !wait_bar_warp(bar_accfull + 8 * ((i - 1) % NACC), ((i - 1) / NACC) & 1, abort_flag, a.status, a.wait_ns))
           break;
         const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
         const int nchunks = ti.nrows * a.H_i * CPR;
@@ -657,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
         rlen3 = ti.nrows > 3 ? a.row_len[ti.r0 + 3] : 0;
       }
       const int accb = i % NACC;
-      if (!wait_bar_warp(bar_accfull + 8 * accb, (i / NACC) & 1, abort_flag, a.status)) break;
+      if (!wait_bar_warp(bar_accfull + 8 * accb, (i / NACC) & 1, abort_flag, a.status, a.wait_ns)) break;
       tc_fence_after();
       const int t = ti.j * kTile + m;
       const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + accb * N_max;
@@ -831,6 +843,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
       for (; issued < S && issued < te - tb; ++issued) {
         tile_step(a, prefix, tb + issued, ti);
         mbar_arrive_tx(bar_full + 8 * issued, kStageBytes);
+        if (a.test_no_load && issued == 0) continue;   // test hook: a tile that never lands
         tma_load_2d(cvta_smem(stage + issued * kStageBytes), &a.tmap, 0,
                     (int)(ti.base + (int64_t)ti.j * kTile), bar_full + 8 * issued);
       }
@@ -853,7 +866,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
     if (lane == 0) {
       for (int i = issued; i < n_local; ++i) {
         const int s = i % S;
-        if (i >= S && !wait_bar(bar_empty + 8 * s, ((i / S) - 1) & 1, abort_flag, a.status)) break;
+        if (i >= S && !wait_bar(bar_empty + 8 * s, ((i / S) - 1) & 1, abort_flag, a.status, a.wait_ns)) break;
         tile_step(a, prefix, t_begin + i, ti);
         mbar_arrive_tx(bar_full + 8 * s, kStageBytes);
         tma_load_2d(cvta_smem(stage + s * kStageBytes), &a.tmap, 0,
@@ -862,7 +875,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
       }
       for (int i = max(0, issued - S); i < issued; ++i) {
         const uint64_t t0 = globaltimer();
-        while (!mbar_try(bar_full + 8 * (i % S), (i / S) & 1) && globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try(bar_full + 8 * (i % S), (i / S) & 1) && globaltimer() - t0 < a.wait_ns) {
         }
       }
     }
@@ -880,9 +893,9 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
         tile_step(a, prefix, t_begin + i, ti);
         const uint32_t idesc = idesc_f16(kTile, ti.nrows * a.H_i);
         if (i >= NACC &&
-            !wait_bar(bar_accempty + 8 * acc, ((i / NACC) - 1) & 1, abort_flag, a.status))
+            !wait_bar(bar_accempty + 8 * acc, ((i / NACC) - 1) & 1, abort_flag, a.status, a.wait_ns))
           break;
-        if (!wait_bar(bar_afull + 8 * ab, (i / NA) & 1, abort_flag, a.status)) break;
+        if (!wait_bar(bar_afull + 8 * ab, (i / NA) & 1, abort_flag, a.status, a.wait_ns)) break;
         tc_fence_after();
         const uint32_t a_tm = tmem + a.a_col0 + ab * kACols;
         if (FP8) {
@@ -903,9 +916,9 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
       // Drain: both commit arrivals of this issuer's last tile must land.
       if (last >= 0) {
         const uint64_t t0 = globaltimer();
-        while (!mbar_try(bar_accfull + 8 * (last % NACC), (last / NACC) & 1) && globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try(bar_accfull + 8 * (last % NACC), (last / NACC) & 1) && globaltimer() - t0 < a.wait_ns) {
         }
-        while (!mbar_try(bar_afree + 8 * (last % NA), (last / NA) & 1) && globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try(bar_afree + 8 * (last % NA), (last / NA) & 1) && globaltimer() - t0 < a.wait_ns) {
         }
       }
     }
@@ -920,13 +933,13 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
     for (int i = par; i < n_local; i += 2) {
       const int s = i % S, ab = i % NA;
       const bool new_group = tile_step(a, prefix, t_begin + i, ti);
-      if (i >= NA && !wait_bar_warp(bar_afree + 8 * ab, ((i / NA) - 1) & 1, abort_flag, a.status)) break;
+      if (i >= NA && !wait_bar_warp(bar_afree + 8 * ab, ((i / NA) - 1) & 1, abort_flag, a.status, a.wait_ns)) break;
       if (new_group) {   // (B does not depend on the key tile: written before waiting for it)
         // This parity's B is read by the MMAs of tiles i-2, i-4, ...; issuers
         // (i-2) % 4 and i % 4 complete theirs in order, and tile i-4 (buffer
         // ab) was waited for above, so tile i-2 is the one left.
         if (i >= 2 &&
-            !wait_bar_warp(bar_afree + 8 * ((i - 2) % NA), ((i - 2) / NA) & 1, abort_flag, a.status))
+            !wait_bar_warp(bar_afree + 8 * ((i - 2) % NA), ((i - 2) / NA) & 1, abort_flag, a.status, a.wait_ns))
           break;
         const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
         const int nchunks = ti.nrows * a.H_i * (D_I / 16);
@@ -946,7 +959,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
         }
         fence_proxy_async();                  // B is read by the MMA (async proxy)
       }
-      if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status)) break;
+      if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status, a.wait_ns)) break;
       const unsigned char* row = stage + s * kStageBytes + m * 128;
       if (FP8) {
 #pragma unroll
@@ -1044,7 +1057,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
         rlen3 = ti.nrows > 3 ? a.row_len[ti.r0 + 3] : 0;
       }
       const int accb = i % NACC;
-      if (!wait_bar_warp(bar_accfull + 8 * accb, (i / NACC) & 1, abort_flag, a.status)) break;
+      if (!wait_bar_warp(bar_accfull + 8 * accb, (i / NACC) & 1, abort_flag, a.status, a.wait_ns)) break;
       tc_fence_after();
       const int t = ti.j * kTile + m;
       const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + accb * N_max;
@@ -1105,6 +1118,21 @@ bool indexer_tc_supported(const dsa_problem& p) {
   return (p.D_i == 64 || p.D_i == 128) && (p.H_i == 32 || p.H_i == 64 || p.H_i == 128);
 }
 
+// Query rows per MMA group: up to 256 columns (heads x rows), at most kMaxRG,
+// no more than a request's rows.
+static int indexer_row_group(const dsa_problem& p) {
+  const int per_req = (p.R + p.B - 1) / p.B;
+  int RG = 256 / p.H_i;
+  if (RG > kMaxRG) RG = kMaxRG;
+  if (per_req < RG) RG = per_req < 1 ? 1 : per_req;
+  return RG;
+}
+
+bool indexer_tc_tmem_operand(const dsa_problem& p) {
+  return indexer_tc_supported(p) && p.D_i == 128 && indexer_row_group(p) * p.H_i <= 128 &&
+         p.L_total >= 128;
+}
+
 template <int D_I, int S, bool BIASED>
 cudaError_t launch_tc(const TcArgs& a, int sms, size_t smem, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<D_I, S, BIASED>,
@@ -1152,9 +1180,13 @@ cudaError_t launch_tm_s(const TcArgs& a, int sms, size_t smem, cudaStream_t st) 
 }
 
 cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
-                              cudaStream_t st) {
+                              cudaStream_t st, const TestHooks* hooks) {
   TcArgs a;
   std::memset(&a, 0, sizeof a);
+  const TestHooks none;
+  if (!hooks) hooks = &none;
+  a.wait_ns = hooks->wait_ns;
+  a.test_no_load = hooks->indexer_no_load;
   a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
   a.rows = reinterpret_cast<RowState*>(ws + pl.off_state);
   a.zero = reinterpret_cast<uint4*>(ws);
@@ -1164,10 +1196,7 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   a.scores = scores; a.L_max = p.L_max;
   a.B = p.B; a.H_i = p.H_i; a.D_i = p.D_i; a.relu = (p.flags & DSA_FLAG_NO_RELU) ? 0 : 1;
   a.L1 = (int)p.L_total; a.R1 = p.R;
-  const int per_req = (p.R + p.B - 1) / p.B;
-  int RG = 256 / p.H_i;
-  if (RG > kMaxRG) RG = kMaxRG;
-  if (per_req < RG) RG = per_req < 1 ? 1 : per_req;
+  const int RG = indexer_row_group(p);
   a.RG = RG;
   const int N_max = RG * p.H_i;
   const int D_i = p.D_i;

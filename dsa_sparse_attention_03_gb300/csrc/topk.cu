@@ -32,6 +32,7 @@
 //           every key > T plus the lowest-index positions with key == T in
 //           index order, then a bitonic sort.
 // A row with row_len <= k selects every position; an empty row selects none.
+#include "barrier_protocol.h"
 #include "common.cuh"
 
 namespace dsa {
@@ -44,7 +45,6 @@ constexpr int kRankSlices = kCapFast / kRankSlice;         // units per row (als
 static_assert(kRankSlices * kRankSlice >= kMaxK, "rank units must cover idx");
 constexpr int kRadixBits = 11;
 constexpr int kSortRows = 8;                               // rank by per-row sort from this many rows
-constexpr uint64_t kGridWaitNs = 2000000000ull;            // grid barrier limit (2 s)
 
 enum Mode : uint32_t { kFast = 0, kAll = 1, kEmpty = 2, kExact = 3 };
 
@@ -60,6 +60,8 @@ struct TopkArgs {
   uint32_t* bar;       // grid barrier counters (zeroed with the status block)
   int64_t L_max;
   int R, k, chunk, nchunk, hist_rep, range;
+  uint64_t wait_ns;    // grid barrier limit
+  int skip_cta;        // test hook: this CTA returns before its first grid barrier (-1: none)
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -317,27 +319,28 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
+// Device operations of the barrier protocol (barrier_protocol.h) on one
+// global counter.
+struct GridOps {
+  uint32_t* c;
+  uint32_t* status;
+  __device__ void fence() { __threadfence(); }
+  __device__ void arrive() { atomicAdd(c, 1u); }
+  __device__ uint32_t count() { return ld_acquire(c); }
+  __device__ uint64_t now() { return gtimer(); }
+  __device__ void timeout() { raise_status(status, DSA_DEVICE_TIMEOUT); }
+};
+
 // Barrier over the whole grid (co-resident by the cooperative launch): the
 // CTA's writes are published before it arrives at counter c, and every later
-// read sees the other CTAs' writes.  Bounded: after kGridWaitNs the CTA raises
+// read sees the other CTAs' writes.  Bounded: after limit_ns the CTA raises
 // DSA_DEVICE_TIMEOUT and returns false (the caller then exits).
-__device__ bool grid_barrier(uint32_t* c, uint32_t* status) {
+__device__ bool grid_barrier(uint32_t* c, uint32_t* status, uint64_t limit_ns) {
   __shared__ int ok;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(c, 1u);
-    int good = 1;
-    const uint64_t t0 = gtimer();
-    while (ld_acquire(c) < gridDim.x) {
-      if (gtimer() - t0 > kGridWaitNs) {
-        raise_status(status, DSA_DEVICE_TIMEOUT);
-        good = 0;
-        break;
-      }
-    }
-    __threadfence();
-    ok = good;
+    GridOps ops{c, status};
+    ok = barrier_arrive_and_wait(ops, gridDim.x, limit_ns) ? 1 : 0;
   }
   __syncthreads();
   return ok != 0;
@@ -384,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
   pdl_trigger();
   const int nunits = a.R * a.nchunk;
   int nb = 0;
+  if ((int)blockIdx.x == a.skip_cta) return;   // test hook: an arrival that never comes
 
   // ---- range (standalone call): the row's max key and max complemented key.
   if (a.range) {
@@ -404,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
         if (uminv) atomicMax(&a.state[r].uminv, uminv);
       }
     }
-    if (!grid_barrier(a.bar + nb++, a.status)) return;
+    if (!grid_barrier(a.bar + nb++, a.status, a.wait_ns)) return;
   }
 
   // ---- hist
@@ -424,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
       if (h[i]) atomicAdd(&mine[i], h[i]);
     __syncthreads();
   }
-  if (!grid_barrier(a.bar + nb++, a.status)) return;
+  if (!grid_barrier(a.bar + nb++, a.status, a.wait_ns)) return;
 
   // ---- select
   {
@@ -483,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
       }
     }
   }
-  if (!grid_barrier(a.bar + nb++, a.status)) return;
+  if (!grid_barrier(a.bar + nb++, a.status, a.wait_ns)) return;
 
   // ---- rank by sort: whole rows per CTA (many rows).
   if (a.R >= kSortRows) {
@@ -560,8 +564,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
 }  // namespace
 
 cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* scores,
-                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st, bool minmax_done) {
+                        int32_t* idx, int32_t* nsel, char* ws, cudaStream_t st, bool minmax_done,
+                        const TestHooks* hooks) {
   TopkArgs a;
+  const TestHooks none;
+  if (!hooks) hooks = &none;
+  a.wait_ns = hooks->wait_ns;
+  a.skip_cta = hooks->topk_skip_cta;
   a.scores = scores;
   a.row_len = p.row_len;
   a.idx = idx;

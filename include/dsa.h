@@ -204,9 +204,11 @@ DSA_API dsa_status dsa_topk(const dsa_problem* p, const int32_t* scores, int32_t
  * histogram copies, more for long rows split over many CTAs), so roughly 40
  * to 100 rows fit.
  *
- * - The first call on each device looks the array's address up
- *   (cudaGetSymbolAddress) and caches it; make that first call before any
- *   stream capture begins.
+ * - Every call looks the array's address up in the current device's context
+ *   (cudaGetSymbolAddress, which allocates nothing), so a device reset or a
+ *   new context never leaves a stale address behind.  The first call in a
+ *   process may load the library's device code; make it before any stream
+ *   capture begins.
  * - Every call first clears the scratch's status block, row state and
  *   histograms (cudaMemsetAsync on `stream`); the rest needs no clearing.
  * - All calls share the one array: two calls whose executions overlap (on
@@ -245,6 +247,13 @@ DSA_API dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* 
  * DSA_ERR_DEVICE_INDEX when the matching bit is set, else DSA_OK.
  */
 DSA_API dsa_status dsa_read_device_status(void* ws, void* stream, int32_t* bits);
+
+/*
+ * The same check without the bits: synchronises `stream` and returns
+ * DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX or DSA_OK from the workspace's device
+ * status word (a CUDA failure returns DSA_ERR_CUDA).
+ */
+DSA_API dsa_status dsa_get_device_status(void* ws, void* stream);
 
 #ifdef __cplusplus
 }

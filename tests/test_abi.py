@@ -18,7 +18,8 @@ def dsa():
 
 
 def _declared():
-    txt = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    inc = os.path.join(ROOT, "include")
+    txt = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     return sorted(set(re.findall(r"DSA_API\s+[\w\s\*]+?\b(dsa_\w+)\s*\(", txt)))
 
 

@@ -122,6 +122,37 @@ def test_tc_fp8_path_at_its_exactness_limit():
     _check_one(x, None, False, True, 11)
 
 
+def _worst_case_rows(n, D_i=128, v=11):
+    """Deterministic int8 rows at +-v that drive each head's dot product to its
+    extremes: all +v, all -v, alternating signs (complete cancellation), signs
+    per block of 32 (one MMA K-step of the e4m3 mode), half and half, zero."""
+    d = np.arange(D_i)
+    pats = [np.full(D_i, v), np.full(D_i, -v), np.where(d % 2 == 0, v, -v),
+            np.where((d // 32) % 2 == 0, v, -v), np.where(d < D_i // 2, v, -v),
+            np.zeros(D_i, np.int64), np.where((d // 32) % 2 == 0, -v, v)]
+    return np.stack([pats[i % len(pats)] for i in range(n)]).astype(np.int8)
+
+
+@pytest.mark.parametrize("rows", [1, 2])
+def test_tc_fp8_worst_case_dots_at_the_bound(rows):
+    # Declared bound 11: e4m3 operands.  Every key and query value is +-11 or 0,
+    # so a head's dot reaches 128 * 11^2 = 15488 (and -15488 without ReLU), and
+    # every partial sum over a K-step of 32 is at its largest magnitude (3872 per
+    # step); with w = 4 on every head the score reaches 64 * 4 * 15488.
+    x = gen.causal64(L=3000, R=rows) if rows > 1 else gen.l64k(L=3000)
+    x.k_idx[:] = _worst_case_rows(x.k_idx.shape[0])
+    rng = np.random.default_rng(12)
+    for r in range(x.R):
+        q = _worst_case_rows(64)
+        x.q_idx[r] = q[rng.permutation(64)]
+    x.q_idx[0, 0] = 11                     # head 0 of row 0 against all +11 keys: +15488
+    x.w_idx[:] = 4
+    ref = oracle.indexer_scores(x.q_idx, x.w_idx, x.k_idx, x.offsets, x.row_offsets, x.row_len)
+    assert ref[0].max() >= 4 * 15488
+    _check_one(x, None, True, True, 11)
+    _check_one(x, None, False, True, 11)
+
+
 def test_tc_fp8_with_128_column_accumulators():
     # 32 heads x 4 rows per request fill 128 accumulator columns per tile in the
     # e4m3 mode; the two tile parities must still own separate accumulators.

@@ -35,6 +35,15 @@ def _check_rows(x, res, rows, relu=True, check_lse=True):
     assert res["status"] == 0
 
 
+def _fused_equals_ops(x, res):
+    """The fused dsa_decode_step gives the same indices, counts and output bits
+    as the three separate calls (which the caller compared with the oracle)."""
+    step = run_step(x)
+    for key in ("idx", "nsel", "out"):
+        assert np.array_equal(step[key], res[key]), key
+    assert step["status"] == 0
+
+
 @pytest.mark.parametrize("indexer", INDEXERS)
 def test_tiny_workload(indexer):
     x = gen.tiny()
@@ -57,26 +66,32 @@ def test_l300k_one_layer_full_size():
     _check_rows(x, res, [0])
 
 
-def test_batch32_varlen_sampled_rows():
+@pytest.mark.slow
+def test_batch32_varlen_every_row():
+    # All 32 requests (2.0 M cached positions): scores, ordered indices and
+    # output of every row against the oracle.
     x = gen.batch32()
     res = run_ops(x)
-    lens = np.diff(x.offsets)
-    rows = sorted({0, 17, 31, int(np.argmin(lens)), int(np.argmax(lens))})
-    _check_rows(x, res, rows)
-    topk_properties(res["scores"], res["idx"], res["nsel"], x.row_len, x.k)   # every row
+    _check_rows(x, res, list(range(x.R)))
+    topk_properties(res["scores"], res["idx"], res["nsel"], x.row_len, x.k)
+    _fused_equals_ops(x, res)
 
 
-def test_causal64_heavy_ties_sampled_rows():
+@pytest.mark.slow
+def test_causal64_heavy_ties_every_row():
+    # All 64 causal rows, each with thousands of scores tied at its threshold
+    # (the exact fallback), against the oracle's full stable sort.
     x = gen.causal64()
     res = run_ops(x)
-    rows = [0, 1, 40, 63]
-    _check_rows(x, res, rows)
-    topk_properties(res["scores"], res["idx"], res["nsel"], x.row_len, x.k)   # every row
+    _check_rows(x, res, list(range(x.R)))
+    topk_properties(res["scores"], res["idx"], res["nsel"], x.row_len, x.k)
+    _fused_equals_ops(x, res)
     # the threshold really is ambiguous: more positions tie than are taken
-    s = res["scores"][0, :x.row_len[0]]
-    sel = res["idx"][0]
-    T = s[sel[-1]]
-    assert (s == T).sum() > (s[sel] == T).sum() > 0
+    for r in (0, 63):
+        s = res["scores"][r, :x.row_len[r]]
+        sel = res["idx"][r]
+        T = s[sel[-1]]
+        assert (s == T).sum() > (s[sel] == T).sum() > 0
 
 
 @pytest.mark.parametrize("L", [1, 2, 255, 256, 257, 1000, 4099, 20000])

@@ -1,7 +1,10 @@
-"""dsa_topk on crafted score rows, against the oracle's full stable sort: the
-sampled-threshold path, rows whose sample over- or under-counts (which must
-take the histogram path), heavy ties (the exact path), and rows of every kind
-in one call.  Scores are given directly, so each path is reached on purpose."""
+"""dsa_topk on crafted score rows, against the oracle's full stable sort:
+long random rows, the largest scores on a regular stride, a crowded threshold
+bin and heavy ties (the exact fallback), scores spanning the whole int32 range
+(rows of only INT32_MIN or only INT32_MAX included), and rows of every kind in
+one call, with one row (survivors ranked across the grid) and with many rows
+(each row's survivors sorted by one CTA).  Scores are given directly, so each
+path is reached on purpose."""
 import numpy as np
 import pytest
 
@@ -53,14 +56,13 @@ def _check(rows, k=K):
         assert np.array_equal(idx[i], ref), f"row {i}"
 
 
-def test_random_long_row_sampled_path():
+def test_random_long_row():
     rng = np.random.default_rng(3)
     _check([rng.integers(-10**6, 10**6, 300000, dtype=np.int64).astype(np.int32)])
 
 
-def test_sample_positions_hold_the_top_scores():
-    # Positions on the sampling stride carry the largest scores, so the sample
-    # overestimates the threshold and too few positions survive.
+def test_top_scores_on_a_regular_stride():
+    # Every 37th position carries one of the largest scores (all distinct).
     L = 300000
     stride = -(-L // 8192)
     rng = np.random.default_rng(4)
@@ -69,8 +71,9 @@ def test_sample_positions_hold_the_top_scores():
     _check([s])
 
 
-def test_top_scores_avoid_the_sample_positions():
-    # The sample sees only ordinary scores, so far more than 4096 survive.
+def test_twenty_thousand_scores_crowd_the_threshold():
+    # 20000 positions share ten values just above the rest, so the threshold
+    # bin holds thousands of positions (the exact fallback).
     L = 300000
     stride = -(-L // 8192)
     rng = np.random.default_rng(5)
@@ -91,16 +94,42 @@ def test_rows_of_every_kind_in_one_call():
     stride = -(-L // 8192)
     hit = rng.integers(0, 50, L).astype(np.int32)
     hit[::stride] = 10**5
-    rows = [rng.integers(-5000, 5000, L).astype(np.int32),   # sampled
-            hit,                                            # retried, heavy ties at the top
+    rows = [rng.integers(-5000, 5000, L).astype(np.int32),   # random
+            hit,                                            # heavy ties at the top, on a stride
             np.array([], dtype=np.int32),                   # empty
             rng.integers(0, 3, 1500).astype(np.int32),      # shorter than k
-            rng.integers(-7, 7, 6000).astype(np.int32),     # whole row sampled: exact T, ties
+            rng.integers(-7, 7, 6000).astype(np.int32),     # few values: ties at T
             np.full(9000, -1, dtype=np.int32)]              # ties beyond the survivor cap
     _check(rows)
 
 
-def test_small_k_and_lengths_around_the_sample_size():
+def test_small_k_and_lengths_around_8192():
     rng = np.random.default_rng(7)
     rows = [rng.integers(-100, 100, n).astype(np.int32) for n in (8191, 8192, 8193, 20000)]
     _check(rows, k=300)
+
+
+def _int32_extreme_rows(rng):
+    lo, hi = np.iinfo(np.int32).min, np.iinfo(np.int32).max
+    full = rng.integers(lo, hi, 300000, dtype=np.int64, endpoint=True).astype(np.int32)
+    full[[5, 77, 299999]] = hi
+    full[[6, 1000, 250000]] = lo
+    two = rng.choice(np.array([lo, hi], np.int32), 40000)
+    few_max = np.full(30000, lo, np.int32)
+    few_max[rng.choice(30000, 100, replace=False)] = hi
+    near_edges = rng.choice(np.array([lo, lo + 1, -1, 0, 1, hi - 1, hi], np.int32), 50000)
+    return [full, np.full(5000, lo, np.int32), np.full(5000, hi, np.int32), two, few_max,
+            near_edges, np.array([hi, lo, 0], np.int32)]
+
+
+def test_int32_extremes_one_row_at_a_time():
+    # One row per call: the range and bins span INT32_MIN..INT32_MAX (the widest
+    # bin shift), and the survivors are ranked across the grid.
+    for row in _int32_extreme_rows(np.random.default_rng(8)):
+        _check([row])
+
+
+def test_int32_extremes_many_rows():
+    # Eight or more rows in one call: each row's survivors are sorted by a CTA.
+    rows = _int32_extreme_rows(np.random.default_rng(9))
+    _check(rows + rows[:2])
