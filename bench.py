@@ -174,9 +174,9 @@ def make_layers(n_layers, L, device, kv="bf16"):
     return layers, ws, idx, nsel, out
 
 
-def kernels_per_step():
+def kernels_per_step(prob):
     import dsa_sparse_attention_03_gb300 as dsa
-    return dsa.KERNELS_PER_DECODE_STEP
+    return dsa.dsa_decode_step_kernels(prob)
 
 
 def bench_ours(args):
@@ -327,7 +327,7 @@ def bench_ours(args):
         "stages_us_per_layer": stages,
         "secondary": sec,
         "e2e": e2e,
-        "gpu_launches": args.steps * n_layers * kernels_per_step(),
+        "gpu_launches": args.steps * n_layers * kernels_per_step(layers[0][1]),
         "clocks": clk,
         "device_status": status,
     }
@@ -588,7 +588,7 @@ def bench_workload(args):
                        "indexer": dsa.indexer_kind(prob), "cuda_graph": True,
                        "l2": f"inputs {in_bytes / 1e6:.1f} MB ({'>' if in_bytes > 129e6 else '<'} L2, 129 MB); not flushed"},
             "step_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
-            "gpu_launches": reps * kernels_per_step(), "device_status": status}
+            "gpu_launches": reps * kernels_per_step(prob), "device_status": status}
 
 
 def bench_reference(args):

@@ -45,7 +45,8 @@ DSA_FLAG_KV_FP8 = 0x200
 INDEXERS = {"auto": DSA_INDEXER_AUTO, "dp4a": DSA_INDEXER_DP4A, "tc": DSA_INDEXER_TC}
 
 # Symbols the header declares (checked by the ABI test).
-EXPORTS = ("dsa_version", "dsa_last_error_string", "dsa_indexer_kind", "dsa_workspace_size",
+EXPORTS = ("dsa_version", "dsa_last_error_string", "dsa_indexer_kind", "dsa_decode_step_kernels",
+           "dsa_workspace_size",
            "dsa_index_scores",
            "dsa_topk", "dsa_topk_static", "dsa_sparse_attn", "dsa_decode_step",
            "dsa_read_device_status", "dsa_get_device_status",
@@ -85,6 +86,8 @@ def _load() -> ctypes.CDLL:
     lib.dsa_last_error_string.restype = ctypes.c_char_p
     lib.dsa_indexer_kind.restype = ctypes.c_int
     lib.dsa_indexer_kind.argtypes = [P]
+    lib.dsa_decode_step_kernels.restype = ctypes.c_int
+    lib.dsa_decode_step_kernels.argtypes = [P]
     lib.dsa_workspace_size.restype = sz
     lib.dsa_workspace_size.argtypes = [P]
     for name, args in (
@@ -219,8 +222,9 @@ def upload_inputs(inp, device="cuda", indexer="auto", relu=True, qk_abs_max=0, w
     return prob, t
 
 
-# Kernels one dsa_decode_step enqueues: indexer 1, top-k 1, attention 1.
-KERNELS_PER_DECODE_STEP = 3
+def dsa_decode_step_kernels(prob: Problem) -> int:
+    """Kernels one dsa_decode_step launches for this problem (2 or 3)."""
+    return _lib.dsa_decode_step_kernels(ctypes.byref(prob.c))
 
 
 def dsa_indexer_kind(prob: Problem) -> int:

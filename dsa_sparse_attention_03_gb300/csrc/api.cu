@@ -111,13 +111,22 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   const int hgroups = p->H_q > 0 ? (p->H_q + kAttnHeads - 1) / kAttnHeads : 0;
   P.attn_kc_max = attn_clusters(p->R, hgroups, p->k);
   P.off_acnt = off; off = align_up(off + R * size_t(hgroups) * 16 * 4, 256);
+  // Single-row decode step (one layout for every entry point): its histogram
+  // and arrival counters start at zero.
+  P.fused_row = decode_row_supported(*p) ? 1 : 0;
+  P.off_lhist = off;
+  if (P.fused_row) off = align_up(off + kRowHistBytes, 256);
   P.zero_end = off;
+  P.off_lkeep = off;
+  if (P.fused_row) off = align_up(off + kRowKeepBytes, 256);
   P.off_surv = off; off = align_up(off + R * size_t(kCapFast) * 8, 256);
   P.off_scores = off; off = align_up(off + R * size_t(p->L_max) * 4, 256);
   const size_t dv = p->D_v > 0 ? size_t(p->D_v) : 0;
   P.off_apart = off;
   if (P.attn_kc_max > 1)
     off = align_up(off + R * size_t(hgroups) * P.attn_kc_max * (16 * dv + 32 * 16) * 4, 256);
+  P.off_rpart = off;
+  if (P.fused_row) off = align_up(off + decode_row_partials_bytes(*p), 256);
   P.total = off;
   return DSA_OK;
 }
@@ -165,6 +174,13 @@ int dsa_indexer_kind(const dsa_problem* p) {
   const int ix = p->flags & DSA_INDEXER_MASK;
   const bool tc = ix == DSA_INDEXER_TC || (ix == DSA_INDEXER_AUTO && indexer_tc_supported(*p));
   return tc ? DSA_INDEXER_TC : DSA_INDEXER_DP4A;
+}
+
+int dsa_decode_step_kernels(const dsa_problem* p) {
+  Plan pl;
+  if (make_plan(p, 0, &pl) != DSA_OK) return -1;
+  if (p->R == 0) return 0;
+  return pl.fused_row ? 2 : 3;
 }
 
 size_t dsa_workspace_size(const dsa_problem* p) {
@@ -278,6 +294,11 @@ dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* nsel, ui
   }
   int32_t* scores = reinterpret_cast<int32_t*>(w + pl.off_scores);
   if ((s = run_indexer(*p, pl, scores, w, st)) != DSA_OK) return s;
+  if (pl.fused_row) {
+    e = launch_decode_row(*p, pl, scores, idx, nsel, out, w, st);
+    if (e != cudaSuccess) return cuda_fail(e, "selection and attention (one row)");
+    return DSA_OK;
+  }
   e = launch_topk(*p, pl, scores, idx, nsel, w, st, true);
   if (e != cudaSuccess) return cuda_fail(e, "top-k");
   e = launch_attention(*p, pl, idx, nsel, out, nullptr, w, st);

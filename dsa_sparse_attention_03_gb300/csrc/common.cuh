@@ -1,6 +1,7 @@
 // Internal definitions shared by the libdsa translation units (not installed).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stddef.h>
@@ -40,8 +41,10 @@ struct Plan {
   int chunk, nchunk;       // top-k: positions per CTA, CTAs per row
   int hist_rep;            // top-k: copies of each row's global histogram
   int attn_kc_max;          // attention: clusters per (row, head group), at most
-  size_t off_status, off_state, off_hist, off_acnt, zero_end;
-  size_t off_surv, off_scores, off_apart, total;
+  int fused_row;            // dsa_decode_step runs the single-row kernel (decode_row.cu)
+  size_t off_status, off_state, off_hist, off_acnt, off_lhist, zero_end;
+  size_t off_lkeep;         // single-row step: words the indexer must not clear (see decode_row.cu)
+  size_t off_surv, off_scores, off_apart, off_rpart, total;
 };
 
 // Attention cluster size for k selected positions: one 64-position tile per
@@ -66,6 +69,24 @@ inline int attn_clusters(int R, int hgroups, int k) {
   const int64_t per_kc = (int64_t)R * hgroups * C;
   while (kc > 1 && per_kc * kc > 600) kc = (kc + 1) / 2;
   return kc;
+}
+
+// Log-spaced score bins of the single-row step, shared by the indexer's
+// epilogue (which counts its scores into them) and decode_row.cu.  A score's
+// bin is its magnitude |s| (or -1 - s when negative) as a float with 7 mantissa
+// bits -- exact below 128, then 128 bins per octave -- above 4096 for s >= 0
+// and mirrored below it for s < 0: monotone in s, independent of the data.
+constexpr int kLogMant = 7;
+constexpr int kLogBins = 8192;
+constexpr int kLogCoarse = kLogBins / 128;   // coarse bins of 128 log bins (one octave)
+__device__ __forceinline__ uint32_t score_bin(int32_t s) {
+  const uint32_t a = s >= 0 ? (uint32_t)s : (uint32_t)(-1 - s);
+  uint32_t g = a;
+  if (a >= (1u << kLogMant)) {
+    const int e = 31 - __clz(a);   // floor(log2 a) >= 7
+    g = ((uint32_t)(e - kLogMant + 1) << kLogMant) + ((a >> (e - kLogMant)) & ((1u << kLogMant) - 1));
+  }
+  return s >= 0 ? (kLogBins / 2) + g : (kLogBins / 2 - 1) - g;
 }
 
 // Order-preserving map of int32 onto uint32.
@@ -155,6 +176,14 @@ struct TestHooks {
   int indexer_no_load = 0;             // indexer CTAs arm their first key tile, issue no copy
 };
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (null if the driver lacks it).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
 // Launchers (one per translation unit).  Each returns the launch error.
 // Both indexers also clear the workspace's status word, top-k state and
 // histograms ([0, Plan::zero_end)), so a decode step needs no separate memset.
@@ -173,5 +202,17 @@ cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* sco
 cudaError_t launch_attention(const dsa_problem& p, const Plan& pl, const int32_t* idx,
                              const int32_t* nsel, uint16_t* out, float* lse, char* ws,
                              cudaStream_t st, const TestHooks* hooks = nullptr);
+// Single-row decode step after the indexer: selection and attention in one
+// cooperative kernel (decode_row.cu).
+bool decode_row_supported(const dsa_problem& p);
+size_t decode_row_partials_bytes(const dsa_problem& p);
+constexpr int kRowHistCopies = 8;   // CTA c of the indexer adds into copy c % 8 (spreads the atomics)
+constexpr size_t kRowHistWords = 8192 + 64;             // one copy: log-bin histogram and its coarse sums
+constexpr size_t kRowHistBytes = kRowHistCopies * kRowHistWords * 4;
+constexpr size_t kRowKeepBytes = 256 + 8192 * 4;       // arrival counter of the indexer's CTAs; bin cursors
+// Status-block words of the single-row step (the block is cleared by the indexer).
+constexpr int kRowRedoWord = 2;    // words 2, 3: a bin cursor ran past its bin in the first / second scatter
+cudaError_t launch_decode_row(const dsa_problem& p, const Plan& pl, const int32_t* scores, int32_t* idx,
+                              int32_t* nsel, uint16_t* out, char* ws, cudaStream_t st);
 
 }  // namespace dsa

@@ -51,7 +51,6 @@
 // copies and MMAs are drained (bounded) and tensor memory is freed before exit.
 #include "common.cuh"
 
-#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include <cstring>
@@ -111,6 +110,14 @@ struct TcArgs {
   uint32_t a_col0;      // first TMEM column of the A buffers
   uint64_t wait_ns;     // limit of every bounded wait
   int test_no_load;     // test hook: arm the first key tile's barrier, issue no copy
+  // Single-row decode step: the epilogue counts the row's scores into log
+  // bins in shared memory (off_lh); every CTA adds its counts into lhist and
+  // lcoarse (cleared with the zero range) once all CTAs have cleared their
+  // share, which each announces by incrementing *zcount.
+  uint32_t* lhist;      // [kLogBins], or null
+  uint32_t* lcoarse;    // [kLogCoarse]
+  uint32_t* zcount;
+  uint32_t off_lh;
   CUtensorMap tmap;     // k_idx as [L_total, 128] bytes, 128-byte swizzle
 };
 
@@ -124,6 +131,12 @@ __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -737,6 +750,34 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
   }
 }
 
+// The B operand of a row group for the tensor-memory kernel (D_i = 128): the
+// queries of rows r0 .. r0 + nrows - 1, all heads, as e4m3 rows of 128 bytes
+// (FP8) or exact fp16 in the canonical K-major 128-byte-swizzled layout.  One
+// of the four converter warps of a tile parity (thread ct of 128); ends with
+// the proxy fence that makes the operand visible to the MMA.
+template <bool FP8>
+__device__ __forceinline__ void convert_b(const TcArgs& a, unsigned char* Bp, int r0, int nrows, int ct) {
+  constexpr int D_I = 128;
+  const int N_max = a.RG * a.H_i;
+  const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)r0 * a.H_i * D_I);
+  const int nchunks = nrows * a.H_i * (D_I / 16);
+  for (int q = ct; q < nchunks; q += kTmConvPerTile * 32) {
+    const int n = q / (D_I / 16), c = q % (D_I / 16);
+    if (FP8) {
+      // e4m3 rows of 128 bytes: 16-byte unit c of row n at unit c ^ (n mod 8).
+      const int4 v = __ldg(src + q);
+      *reinterpret_cast<uint4*>(Bp + n * 128 + ((c ^ (n & 7)) << 4)) =
+          make_uint4(i8x4_to_e4m3x4((uint32_t)v.x), i8x4_to_e4m3x4((uint32_t)v.y),
+                     i8x4_to_e4m3x4((uint32_t)v.z), i8x4_to_e4m3x4((uint32_t)v.w));
+    } else {
+      uint32_t b0, b1;
+      sw128_offsets(n, c, (uint32_t)N_max * 128, b0, b1);
+      convert16<false>(__ldg(src + q), Bp + b0, Bp + b1);   // queries stay exact
+    }
+  }
+  fence_proxy_async();   // B is read by the MMA (async proxy)
+}
+
 // ---------------------------------------------------------------------------
 // D_i = 128 with the A operand in TMEM.  Key tiles arrive through the tensor
 // map with the 128-byte swizzle, so a converter thread reads its own key row
@@ -764,6 +805,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.off_bar);
   volatile int* misc = reinterpret_cast<volatile int*>(smem + a.off_misc);  // [0] tmem, [1] abort
   int* prefix = reinterpret_cast<int*>(smem + a.off_prefix);               // [B+1]
+  uint32_t* lh = reinterpret_cast<uint32_t*>(smem + a.off_lh);             // [kLogBins + kLogCoarse]
 
   const int NA = a.na, NACC = a.nacc;
   const uint32_t bar_full = cvta_smem(bars);                   // S
@@ -792,6 +834,10 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tmap)) : "memory");
     }
+  }
+  if (a.lhist)
+    for (int i = tid; i < kLogBins + kLogCoarse; i += kTmThreads) lh[i] = 0;
+  if (warp == 0) {
     __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      cvta_smem((const void*)misc)),
@@ -800,14 +846,53 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
 
+  // Parameters read right after the wait, fetched into the constant cache
+  // while the previous kernel finishes (each asm forces the read here).
+  asm volatile("" ::"l"(a.q_idx), "l"(a.scores), "l"(a.rows), "l"(a.zero), "r"(a.B), "r"(a.RG), "r"(a.L1),
+               "r"(a.R1), "r"(a.pstride), "r"(a.n_zero), "r"(a.off_lh), "l"(a.lhist), "l"(a.zcount),
+               "l"(a.wait_ns), "r"(a.b_stride), "r"(a.a_col0));
   pdl_wait();
   pdl_trigger();
+  int issued = 0;
+  // One request: the tile map comes from host sizes, so this CTA's first key
+  // tiles go out before anything else, and the converters build the first
+  // B operand of their tile parity (the queries of that tile's row group)
+  // while the other warps clear the workspace.
+  const int tiles_1 = (a.L1 + kTile - 1) / kTile;
+  const int tot_1 = ((a.R1 + a.RG - 1) / a.RG) * tiles_1;
+  // A single row group is dealt to the CTAs round robin (CTA c takes tiles c,
+  // c + grid, ...), so each wave of key loads covers one contiguous stretch of
+  // the cache; otherwise each CTA takes a contiguous range of tiles, which
+  // keeps its row groups, and B operands, together.
+  const bool dealt = a.B == 1 && a.R1 <= a.RG;
+  const int tb_1 = (int)(((int64_t)blockIdx.x * tot_1) / gridDim.x);
+  const int te_1 = (int)(((int64_t)(blockIdx.x + 1) * tot_1) / gridDim.x);
+  const int n_1 = dealt ? (tot_1 > (int)blockIdx.x ? (tot_1 - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0)
+                        : te_1 - tb_1;
+  auto tile_1 = [&](int i) { return dealt ? (int)blockIdx.x + i * (int)gridDim.x : tb_1 + i; };
+  if (a.B == 1 && warp == 0 && lane == 0) {
+    for (; issued < S && issued < n_1; ++issued) {
+      mbar_arrive_tx(bar_full + 8 * issued, kStageBytes);
+      if (a.test_no_load && issued == 0) continue;   // test hook: a tile that never lands
+      tma_load_2d(cvta_smem(stage + issued * kStageBytes), &a.tmap, 0, (tile_1(issued) % tiles_1) * kTile,
+                  bar_full + 8 * issued);
+    }
+  }
+  const bool early_b = a.B == 1;
+  if (early_b && warp >= kTmConvWarp0 && warp < kTmEpiWarp0) {
+    const int par = (warp - kTmConvWarp0) >> 2;
+    if (par < n_1) {
+      const int ct = ((warp - kTmConvWarp0) & 3) * 32 + lane;
+      const int g0 = tile_1(par) / tiles_1;
+      const int r0 = g0 * a.RG, nrows = min(a.RG, a.R1 - r0);
+      convert_b<FP8>(a, Bop + par * a.b_stride, r0, nrows, ct);
+    }
+  }
   for (int i = blockIdx.x * kTmThreads + tid; i < a.n_zero; i += gridDim.x * kTmThreads)
     a.zero[i] = make_uint4(0, 0, 0, 0);
 
   TileInfo ti;
   ti.lo = ti.hi = 0;
-  int issued = 0;
   if (warp == 0) {
     int run = 0;
     for (int base = 0; base < a.B; base += 32) {
@@ -836,7 +921,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
     }
     if (lane == 0) prefix[a.B] = run;
     __syncwarp();
-    if (lane == 0) {
+    if (lane == 0 && a.B != 1) {   // (one request: issued above)
       const int tot = prefix[a.B];
       const int tb = (int)(((int64_t)blockIdx.x * tot) / gridDim.x);
       const int te = (int)(((int64_t)(blockIdx.x + 1) * tot) / gridDim.x);
@@ -854,11 +939,16 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
   tc_fence_after();
   const uint32_t tmem = (uint32_t)misc[0];
   volatile int* abort_flag = misc + 1;
+  if (a.lhist && tid == 0) {   // this CTA's share of the zero range is cleared
+    __threadfence();
+    atomicAdd(a.zcount, 1u);
+  }
 
   const int total = prefix[a.B];
   const int t_begin = (int)(((int64_t)blockIdx.x * total) / gridDim.x);
   const int t_end = (int)(((int64_t)(blockIdx.x + 1) * total) / gridDim.x);
-  const int n_local = t_end - t_begin;
+  const int n_local = dealt ? n_1 : t_end - t_begin;
+  auto gtile = [&](int i) { return dealt ? (int)blockIdx.x + i * (int)gridDim.x : t_begin + i; };
   const int N_max = a.RG * a.H_i;
 
   if (warp == 0) {
@@ -867,7 +957,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
       for (int i = issued; i < n_local; ++i) {
         const int s = i % S;
         if (i >= S && !wait_bar(bar_empty + 8 * s, ((i / S) - 1) & 1, abort_flag, a.status, a.wait_ns)) break;
-        tile_step(a, prefix, t_begin + i, ti);
+        tile_step(a, prefix, gtile(i), ti);
         mbar_arrive_tx(bar_full + 8 * s, kStageBytes);
         tma_load_2d(cvta_smem(stage + s * kStageBytes), &a.tmap, 0,
                     (int)(ti.base + (int64_t)ti.j * kTile), bar_full + 8 * s);
@@ -890,7 +980,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
       const uint32_t b_base = cvta_smem(Bop) + (uint32_t)(j & 1) * a.b_stride;   // B of this tile parity
       for (int i = j; i < n_local; i += kTmMmaWarps) {
         const int acc = i % NACC, ab = i % NA;
-        tile_step(a, prefix, t_begin + i, ti);
+        tile_step(a, prefix, gtile(i), ti);
         const uint32_t idesc = idesc_f16(kTile, ti.nrows * a.H_i);
         if (i >= NACC &&
             !wait_bar(bar_accempty + 8 * acc, ((i / NACC) - 1) & 1, abort_flag, a.status, a.wait_ns))
@@ -932,32 +1022,16 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
     unsigned char* Bp = Bop + par * a.b_stride;                // B of this parity
     for (int i = par; i < n_local; i += 2) {
       const int s = i % S, ab = i % NA;
-      const bool new_group = tile_step(a, prefix, t_begin + i, ti);
+      const bool new_group = tile_step(a, prefix, gtile(i), ti);
       if (i >= NA && !wait_bar_warp(bar_afree + 8 * ab, ((i / NA) - 1) & 1, abort_flag, a.status, a.wait_ns)) break;
-      if (new_group) {   // (B does not depend on the key tile: written before waiting for it)
+      if (new_group && !(early_b && i == par)) {   // (B does not depend on the key tile)
         // This parity's B is read by the MMAs of tiles i-2, i-4, ...; issuers
         // (i-2) % 4 and i % 4 complete theirs in order, and tile i-4 (buffer
         // ab) was waited for above, so tile i-2 is the one left.
         if (i >= 2 &&
             !wait_bar_warp(bar_afree + 8 * ((i - 2) % NA), ((i - 2) / NA) & 1, abort_flag, a.status, a.wait_ns))
           break;
-        const int4* src = reinterpret_cast<const int4*>(a.q_idx + (int64_t)ti.r0 * a.H_i * D_I);
-        const int nchunks = ti.nrows * a.H_i * (D_I / 16);
-        for (int q = ct; q < nchunks; q += kTmConvPerTile * 32) {
-          const int n = q / (D_I / 16), c = q % (D_I / 16);
-          if (FP8) {
-            // e4m3 rows of 128 bytes: 16-byte unit c of row n at unit c ^ (n mod 8).
-            const int4 v = __ldg(src + q);
-            *reinterpret_cast<uint4*>(Bp + n * 128 + ((c ^ (n & 7)) << 4)) =
-                make_uint4(i8x4_to_e4m3x4((uint32_t)v.x), i8x4_to_e4m3x4((uint32_t)v.y),
-                           i8x4_to_e4m3x4((uint32_t)v.z), i8x4_to_e4m3x4((uint32_t)v.w));
-          } else {
-            uint32_t b0, b1;
-            sw128_offsets(n, c, (uint32_t)N_max * 128, b0, b1);
-            convert16<false>(__ldg(src + q), Bp + b0, Bp + b1);   // queries stay exact
-          }
-        }
-        fence_proxy_async();                  // B is read by the MMA (async proxy)
+        convert_b<FP8>(a, Bp, ti.r0, ti.nrows, ct);
       }
       if (!wait_bar_warp(bar_full + 8 * s, (i / S) & 1, abort_flag, a.status, a.wait_ns)) break;
       const unsigned char* row = stage + s * kStageBytes + m * 128;
@@ -1018,7 +1092,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
     uint32_t mx0 = 0, mx1 = 0, mx2 = 0, mx3 = 0, mn0 = 0, mn1 = 0, mn2 = 0, mn3 = 0;
     int cur_r0 = -1, cur_n = 0;
     for (int i = grp; i < n_local; i += 2) {
-      if (tile_step(a, prefix, t_begin + i, ti)) {
+      if (tile_step(a, prefix, gtile(i), ti)) {
         if (cur_n > 0) row_minmax_flush(a.rows + cur_r0, mx0, mn0);
         if (cur_n > 1) row_minmax_flush(a.rows + cur_r0 + 1, mx1, mn1);
         if (cur_n > 2) row_minmax_flush(a.rows + cur_r0 + 2, mx2, mn2);
@@ -1086,6 +1160,7 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
         const int rl = jr == 0 ? rlen0 : (jr == 1 ? rlen1 : (jr == 2 ? rlen2 : rlen3));
         if (t < rl) {
           a.scores[(int64_t)(ti.r0 + jr) * a.L_max + t] = (int32_t)acc;
+          if (a.lhist) atomicAdd(&lh[score_bin((int32_t)acc)], 1u);   // one row (R = 1)
           const uint32_t u = acc ^ 0x80000000u;
           if (jr == 0) { mx0 = max(mx0, u); mn0 = max(mn0, ~u); }
           if (jr == 1) { mx1 = max(mx1, u); mn1 = max(mn1, ~u); }
@@ -1109,6 +1184,36 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
   if (warp == 0) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
                  : "memory");
+  }
+  if (a.lhist) {
+    // Add this CTA's counts once every CTA has cleared its share of the
+    // histogram (bounded; on expiry the counts are not added, and the row
+    // kernel, finding the total short, rebuilds the histogram itself).
+    if (tid == 0) {
+      const uint64_t t0 = globaltimer();
+      int ok = 1;
+      while (ld_acquire_u32(a.zcount) < gridDim.x) {
+        if (globaltimer() - t0 > a.wait_ns) {
+          raise_status(a.status, DSA_DEVICE_TIMEOUT);
+          ok = 0;
+          break;
+        }
+      }
+      misc[2] = ok;
+    }
+    __syncthreads();
+    if (misc[2]) {
+      uint32_t* lc = lh + kLogBins;
+      const size_t copy = (size_t)(blockIdx.x % kRowHistCopies) * kRowHistWords;
+      for (int i = tid; i < kLogBins; i += kTmThreads) {   // a warp: 32 bins of one coarse bin
+        const uint32_t n = lh[i];
+        if (n) atomicAdd(a.lhist + copy + i, n);
+        const uint32_t cs = __reduce_add_sync(0xffffffffu, n);
+        if (lane == 0 && cs) atomicAdd(&lc[i >> 7], cs);
+      }
+      __syncthreads();
+      if (tid < kLogCoarse && lc[tid]) atomicAdd(a.lcoarse + copy + tid, lc[tid]);
+    }
   }
 }
 
@@ -1146,12 +1251,6 @@ cudaError_t launch_tc_s(const TcArgs& a, int sms, size_t smem, cudaStream_t st) 
   return a.stages == 8 ? launch_tc<D_I, 8, BIASED>(a, sms, smem, st)
                        : launch_tc<D_I, 4, BIASED>(a, sms, smem, st);
 }
-
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_tiled_fn() {
   static EncodeTiledFn fn = []() -> EncodeTiledFn {
@@ -1249,14 +1348,21 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
     // the converters sooner, and four tiles of look-ahead outrun the per-tile
     // work at HBM speed.
     const int S = 4;
-    if (total_for(S) > budget) return cudaErrorInvalidConfiguration;
+    const uint32_t lh_bytes = pl.fused_row ? (uint32_t)(kLogBins + kLogCoarse) * 4u : 0u;
+    if (total_for(S) + lh_bytes > budget) return cudaErrorInvalidConfiguration;
     a.stages = S;
     a.off_b = S * stage_bytes;
     a.off_w = a.off_b + b_bytes;
     a.off_bar = a.off_w + w_bytes;
     a.off_misc = a.off_bar + (2 * S + 2 * kMaxA + 2 * kMaxAcc) * 8;
     a.off_prefix = a.off_misc + 16;
-    size_t smem = (size_t)a.off_prefix + prefix_bytes + 1024;
+    a.off_lh = (a.off_prefix + prefix_bytes + 15) / 16 * 16;
+    if (pl.fused_row && hooks->indexer_no_load == 0) {
+      a.lhist = reinterpret_cast<uint32_t*>(ws + pl.off_lhist);   // copy (CTA % kRowHistCopies) in the kernel
+      a.lcoarse = a.lhist + kLogBins;
+      a.zcount = reinterpret_cast<uint32_t*>(ws + pl.off_lkeep);
+    }
+    size_t smem = (size_t)a.off_lh + lh_bytes + 1024;
     if (smem < 120u * 1024u) smem = 120u * 1024u;   // one CTA per SM: TMEM is never contended
     if (mode == kModeFp8) return launch_tm_s<kModeFp8>(a, sms, smem, st);
     if (mode == kModeBiased) return launch_tm_s<kModeBiased>(a, sms, smem, st);

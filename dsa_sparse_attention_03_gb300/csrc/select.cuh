@@ -1,0 +1,235 @@
+// Block-level building blocks of the exact ordered top-k, shared by the top-k
+// kernel and the single-row decode kernel.  Keys: u = s ^ 0x80000000 is the
+// order-preserving unsigned key of an int32 score s; a survivor's 64-bit key
+// (u << 32 | ~position) orders by (score desc, position asc) when sorted
+// descending, and is never zero.
+#pragma once
+
+#include "common.cuh"
+
+namespace dsa {
+namespace sel {
+
+constexpr int kRadixBits = 11;
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Visits s[t] for t in [begin, end) with `t += NT` striding, eight loads in
+// flight per thread; f(value, t) is called in increasing t for each thread.
+template <int NT, typename F>
+__device__ __forceinline__ void scan_row(const int32_t* s, int begin, int end, F f) {
+  constexpr int U = 8;
+  for (int base = begin + (int)threadIdx.x; base < end; base += U * NT) {
+    int32_t v[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int t = base + j * NT;
+      v[j] = t < end ? s[t] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int t = base + j * NT;
+      if (t < end) f(v[j], t);
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t surv_key(uint32_t u, int t) {
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - (uint32_t)t);
+}
+__device__ __forceinline__ int key_pos(uint64_t key) {
+  return (int)(0xFFFFFFFFu - (uint32_t)key);
+}
+
+// Block-wide inclusive scan in thread order (NT threads).
+template <int NT>
+__device__ uint32_t block_scan_incl(uint32_t v, uint32_t* warp_tot) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_tot[w] = v;
+  __syncthreads();
+  uint32_t base = 0;
+  for (int i = 0; i < w; ++i) base += warp_tot[i];
+  __syncthreads();
+  return base + v;
+}
+
+template <int NT>
+__device__ uint32_t block_reduce_max(uint32_t v, uint32_t* tmp) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) tmp[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint32_t r = 0;
+  for (int i = 0; i < NT / 32; ++i) r = max(r, tmp[i]);
+  __syncthreads();
+  return r;
+}
+
+// Finds, in a histogram of `nbins` counts held in shared memory, the bin b
+// (counting from the top) with above(b) < need <= above(b) + h[b].  Writes
+// (b, above) to out[0..1].  Every thread of the NT-thread block takes part.
+template <int NT>
+__device__ void find_crossing(const uint32_t* h, int nbins, uint32_t need, uint32_t* out) {
+  __shared__ uint32_t wt[NT / 32];
+  const int per = (nbins + NT - 1) / NT;
+  const int top = nbins - 1 - threadIdx.x * per;   // this thread owns bins top, top-1, ...
+  uint32_t sum = 0;
+  for (int j = 0; j < per; ++j)
+    if (top - j >= 0) sum += h[top - j];
+  const uint32_t incl = block_scan_incl<NT>(sum, wt);
+  uint32_t above = incl - sum;
+  if (above < need && incl >= need) {
+    for (int j = 0; j < per; ++j) {
+      const uint32_t c = h[top - j];
+      if (above + c >= need) {
+        out[0] = (uint32_t)(top - j);
+        out[1] = above;
+        break;
+      }
+      above += c;
+    }
+  }
+  __syncthreads();
+}
+
+// Bitonic sort, descending, of keys[0, n) in shared memory (zero keys pad to a
+// power of two; every real key is nonzero).  All threads of the CTA; ends
+// with a barrier.
+template <int NT>
+__device__ void sort_desc(uint64_t* keys, int n0) {
+  int n = 1;
+  while (n < n0) n <<= 1;
+  for (int i = n0 + threadIdx.x; i < n; i += NT) keys[i] = 0;
+  __syncthreads();
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (n >> 1); i += NT) {
+        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+        const uint64_t x = keys[lo], y = keys[hi];
+        const bool desc = (lo & size) == 0;
+        if (desc ? (x < y) : (x > y)) {
+          keys[lo] = y;
+          keys[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// One CTA resolves a row exactly.  The candidates are the positions whose
+// ordered key u satisfies in_cand(u) (one histogram bin); every position with
+// a key above the candidates' is taken, plus the k_rem largest candidates, the
+// lowest positions first among equal keys.  Radix passes over the candidates'
+// key range find the exact k_rem-th largest candidate key T; the winners (keys
+// above T, then the first ties of T in index order) are sorted into keys[0, k)
+// by (score desc, position asc).  keys holds at least the next power of two
+// >= k entries.  All NT threads of the CTA take part; ends with a barrier.
+template <int NT, class InCand>
+__device__ void exact_row_keys(const int32_t* s, int len, int k, uint32_t k_rem, InCand in_cand,
+                               uint64_t* keys) {
+  __shared__ uint32_t h[1 << kRadixBits];
+  __shared__ uint32_t tmp[NT / 32];
+  __shared__ uint32_t res[2];
+  __shared__ uint32_t n_list;
+  __shared__ uint32_t tie8[8 * (NT / 32)];
+
+
+  // Key range of the candidates.
+  uint32_t umax = 0, uminv = 0;
+  scan_row<NT>(s, 0, len, [&](int32_t v, int) {
+    const uint32_t u = ordered_key(v);
+    if (in_cand(u)) {
+      umax = max(umax, u);
+      uminv = max(uminv, ~u);
+    }
+  });
+  umax = block_reduce_max<NT>(umax, tmp);
+  uminv = block_reduce_max<NT>(uminv, tmp);
+  const uint32_t diff = umax ^ ~uminv;
+  uint32_t shift = diff ? 32u - __clz(diff) : 0u;
+  uint32_t prefix = shift >= 32 ? 0u : (umax >> shift);
+
+  // Radix passes down to the exact k_rem-th largest candidate key T.
+  while (shift > 0) {
+    const uint32_t bits = min(shift, (uint32_t)kRadixBits);
+    const uint32_t ns = shift - bits;
+    const int nb = 1 << bits;
+    for (int i = threadIdx.x; i < nb; i += NT) h[i] = 0;
+    __syncthreads();
+    scan_row<NT>(s, 0, len, [&](int32_t v, int) {
+      const uint32_t u = ordered_key(v);
+      if (in_cand(u) && (static_cast<uint64_t>(u) >> shift) == prefix)
+        atomicAdd(&h[(u >> ns) & (uint32_t)(nb - 1)], 1u);
+    });
+    __syncthreads();
+    find_crossing<NT>(h, nb, k_rem, res);
+    k_rem -= res[1];
+    prefix = (prefix << bits) | res[0];
+    shift = ns;
+    __syncthreads();
+  }
+  const uint32_t T = prefix;
+
+  // Winners: every key > T (unordered), then the k_rem lowest-index ties in
+  // index order.  n_gt = k - k_rem keys are strictly greater than T.
+  if (threadIdx.x == 0) n_list = 0;
+  __syncthreads();
+  const uint32_t n_gt = (uint32_t)k - k_rem;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint32_t ties_done = 0;
+  for (int base0 = 0; base0 < len; base0 += 8 * NT) {
+    int32_t vv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = base0 + j * NT + threadIdx.x;
+      vv[j] = t < len ? s[t] : 0;
+    }
+    // Ties are numbered in index order: position t = base0 + j * NT + thread,
+    // so (j, warp, lane) order.  All eight ballots first, one barrier.
+    uint32_t tm[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = base0 + j * NT + threadIdx.x;
+      const uint32_t u = ordered_key(vv[j]);
+      if (t < len && u > T) keys[atomicAdd(&n_list, 1u)] = surv_key(u, t);
+      tm[j] = __ballot_sync(0xffffffffu, t < len && u == T);
+      if (lane == 0) tie8[j * (NT / 32) + w] = __popc(tm[j]);
+    }
+    __syncthreads();
+    uint32_t before = ties_done;   // ties ahead of (j, warp w) in index order
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t tot = 0, mine = 0;
+      for (int i = 0; i < NT / 32; ++i) {
+        const uint32_t c = tie8[j * (NT / 32) + i];
+        if (i < w) mine += c;
+        tot += c;
+      }
+      const int t = base0 + j * NT + threadIdx.x;
+      if (tm[j] & (1u << lane)) {
+        const uint32_t pos = before + mine + __popc(tm[j] & lanemask_lt());
+        if (pos < k_rem) keys[n_gt + pos] = surv_key(ordered_key(vv[j]), t);
+      }
+      before += tot;
+    }
+    ties_done = before;
+    __syncthreads();   // tie8 is rewritten next
+  }
+
+  __syncthreads();
+  sort_desc<NT>(keys, k);
+}
+
+
+}  // namespace sel
+}  // namespace dsa

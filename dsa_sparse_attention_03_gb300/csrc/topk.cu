@@ -32,18 +32,20 @@
 //           every key > T plus the lowest-index positions with key == T in
 //           index order, then a bitonic sort.
 // A row with row_len <= k selects every position; an empty row selects none.
-#include "barrier_protocol.h"
 #include "common.cuh"
+#include "ptx.cuh"
+#include "select.cuh"
 
 namespace dsa {
 namespace {
+
+using namespace sel;
 
 constexpr int kThreads = 512;
 constexpr int kRankSlice = 16;                             // survivors ranked per work unit
 constexpr int kRankLanes = kThreads / kRankSlice;          // threads per survivor
 constexpr int kRankSlices = kCapFast / kRankSlice;         // units per row (also covers idx[0, k))
 static_assert(kRankSlices * kRankSlice >= kMaxK, "rank units must cover idx");
-constexpr int kRadixBits = 11;
 constexpr int kSortRows = 8;                               // rank by per-row sort from this many rows
 
 enum Mode : uint32_t { kFast = 0, kAll = 1, kEmpty = 2, kExact = 3 };
@@ -64,12 +66,6 @@ struct TopkArgs {
   int skip_cta;        // test hook: this CTA returns before its first grid barrier (-1: none)
 };
 
-__device__ __forceinline__ uint32_t lanemask_lt() {
-  uint32_t m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
 // Equal-width bins over the row's key range: bin(u) = (u - umin) >> shift,
 // monotone in u and below kBuckets.
 struct Bins {
@@ -87,264 +83,23 @@ struct Bins {
   }
 };
 
-// Visits s[t] for t in [begin, end) with `t += NT` striding, eight loads in
-// flight per thread; f(value, t) is called in increasing t for each thread.
-template <int NT, typename F>
-__device__ __forceinline__ void scan_row(const int32_t* s, int begin, int end, F f) {
-  constexpr int U = 8;
-  for (int base = begin + (int)threadIdx.x; base < end; base += U * NT) {
-    int32_t v[U];
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const int t = base + j * NT;
-      v[j] = t < end ? s[t] : 0;
-    }
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const int t = base + j * NT;
-      if (t < end) f(v[j], t);
-    }
-  }
-}
-
-__device__ __forceinline__ uint64_t surv_key(uint32_t u, int t) {
-  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - (uint32_t)t);
-}
-__device__ __forceinline__ int key_pos(uint64_t key) {
-  return (int)(0xFFFFFFFFu - (uint32_t)key);
-}
-
-template <typename T>
-__device__ __forceinline__ T ld_volatile(const T* p) {
-  return *reinterpret_cast<const volatile T*>(p);
-}
-
-// Block-wide inclusive scan in thread order (NT threads).
-template <int NT>
-__device__ uint32_t block_scan_incl(uint32_t v, uint32_t* warp_tot) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  if (lane == 31) warp_tot[w] = v;
-  __syncthreads();
-  uint32_t base = 0;
-  for (int i = 0; i < w; ++i) base += warp_tot[i];
-  __syncthreads();
-  return base + v;
-}
-
-template <int NT>
-__device__ uint32_t block_reduce_max(uint32_t v, uint32_t* tmp) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((threadIdx.x & 31) == 0) tmp[threadIdx.x >> 5] = v;
-  __syncthreads();
-  uint32_t r = 0;
-  for (int i = 0; i < NT / 32; ++i) r = max(r, tmp[i]);
-  __syncthreads();
-  return r;
-}
-
-// Finds, in a histogram of `nbins` counts held in shared memory, the bin b
-// (counting from the top) with above(b) < need <= above(b) + h[b].  Writes
-// (b, above) to out[0..1].  Every thread of the NT-thread block takes part.
-template <int NT>
-__device__ void find_crossing(const uint32_t* h, int nbins, uint32_t need, uint32_t* out) {
-  __shared__ uint32_t wt[NT / 32];
-  const int per = (nbins + NT - 1) / NT;
-  const int top = nbins - 1 - threadIdx.x * per;   // this thread owns bins top, top-1, ...
-  uint32_t sum = 0;
-  for (int j = 0; j < per; ++j)
-    if (top - j >= 0) sum += h[top - j];
-  const uint32_t incl = block_scan_incl<NT>(sum, wt);
-  uint32_t above = incl - sum;
-  if (above < need && incl >= need) {
-    for (int j = 0; j < per; ++j) {
-      const uint32_t c = h[top - j];
-      if (above + c >= need) {
-        out[0] = (uint32_t)(top - j);
-        out[1] = above;
-        break;
-      }
-      above += c;
-    }
-  }
-  __syncthreads();
-}
-
-// Bitonic sort, descending, of keys[0, n) in shared memory (zero keys pad to a
-// power of two; every real key is nonzero).  All threads of the CTA; ends
-// with a barrier.
-__device__ void sort_desc(uint64_t* keys, int n0) {
-  constexpr int NT = kThreads;
-  int n = 1;
-  while (n < n0) n <<= 1;
-  for (int i = n0 + threadIdx.x; i < n; i += NT) keys[i] = 0;
-  __syncthreads();
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (n >> 1); i += NT) {
-        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
-        const uint64_t x = keys[lo], y = keys[hi];
-        const bool desc = (lo & size) == 0;
-        if (desc ? (x < y) : (x > y)) {
-          keys[lo] = y;
-          keys[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
 
 // ------------------------------------------------------------------ exact fallback
 
 // One CTA resolves a row exactly: the candidates are the positions in bucket
-// b*; k_rem = k - n_above of them are taken.
+// b*; k - n_above of them are taken.
 __device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys) {
-  constexpr int NT = kThreads;
-  __shared__ uint32_t h[1 << kRadixBits];
-  __shared__ uint32_t tmp[NT / 32];
-  __shared__ uint32_t res[2];
-  __shared__ uint32_t n_list;
-  __shared__ uint32_t tie8[8 * (NT / 32)];
   const int len = a.row_len[r];
   const int32_t* s = a.scores + (int64_t)r * a.L_max;
   const uint32_t bstar = st->bstar;
   const Bins bin(st);
-  uint32_t k_rem = (uint32_t)a.k - st->n_above;
-
-  // Key range of the candidates.
-  uint32_t umax = 0, uminv = 0;
-  scan_row<NT>(s, 0, len, [&](int32_t v, int) {
-    const uint32_t u = ordered_key(v);
-    if (bin(u) == bstar) {
-      umax = max(umax, u);
-      uminv = max(uminv, ~u);
-    }
-  });
-  umax = block_reduce_max<NT>(umax, tmp);
-  uminv = block_reduce_max<NT>(uminv, tmp);
-  const uint32_t diff = umax ^ ~uminv;
-  uint32_t shift = diff ? 32u - __clz(diff) : 0u;
-  uint32_t prefix = shift >= 32 ? 0u : (umax >> shift);
-
-  // Radix passes down to the exact k_rem-th largest candidate key T.
-  while (shift > 0) {
-    const uint32_t bits = min(shift, (uint32_t)kRadixBits);
-    const uint32_t ns = shift - bits;
-    const int nb = 1 << bits;
-    for (int i = threadIdx.x; i < nb; i += NT) h[i] = 0;
-    __syncthreads();
-    scan_row<NT>(s, 0, len, [&](int32_t v, int) {
-      const uint32_t u = ordered_key(v);
-      if (bin(u) == bstar && (static_cast<uint64_t>(u) >> shift) == prefix)
-        atomicAdd(&h[(u >> ns) & (uint32_t)(nb - 1)], 1u);
-    });
-    __syncthreads();
-    find_crossing<NT>(h, nb, k_rem, res);
-    k_rem -= res[1];
-    prefix = (prefix << bits) | res[0];
-    shift = ns;
-    __syncthreads();
-  }
-  const uint32_t T = prefix;
-
-  // Winners: every key > T (unordered), then the k_rem lowest-index ties in
-  // index order.  n_gt = k - k_rem keys are strictly greater than T.
-  if (threadIdx.x == 0) n_list = 0;
-  __syncthreads();
-  const uint32_t n_gt = (uint32_t)a.k - k_rem;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  uint32_t ties_done = 0;
-  for (int base0 = 0; base0 < len; base0 += 8 * NT) {
-    int32_t vv[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int t = base0 + j * NT + threadIdx.x;
-      vv[j] = t < len ? s[t] : 0;
-    }
-    // Ties are numbered in index order: position t = base0 + j * NT + thread,
-    // so (j, warp, lane) order.  All eight ballots first, one barrier.
-    uint32_t tm[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int t = base0 + j * NT + threadIdx.x;
-      const uint32_t u = ordered_key(vv[j]);
-      if (t < len && u > T) keys[atomicAdd(&n_list, 1u)] = surv_key(u, t);
-      tm[j] = __ballot_sync(0xffffffffu, t < len && u == T);
-      if (lane == 0) tie8[j * (NT / 32) + w] = __popc(tm[j]);
-    }
-    __syncthreads();
-    uint32_t before = ties_done;   // ties ahead of (j, warp w) in index order
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t tot = 0, mine = 0;
-      for (int i = 0; i < NT / 32; ++i) {
-        const uint32_t c = tie8[j * (NT / 32) + i];
-        if (i < w) mine += c;
-        tot += c;
-      }
-      const int t = base0 + j * NT + threadIdx.x;
-      if (tm[j] & (1u << lane)) {
-        const uint32_t pos = before + mine + __popc(tm[j] & lanemask_lt());
-        if (pos < k_rem) keys[n_gt + pos] = surv_key(ordered_key(vv[j]), t);
-      }
-      before += tot;
-    }
-    ties_done = before;
-    __syncthreads();   // tie8 is rewritten next
-  }
-
-  __syncthreads();
-  sort_desc(keys, a.k);
+  exact_row_keys<kThreads>(s, len, a.k, (uint32_t)a.k - st->n_above,
+                           [&](uint32_t u) { return bin(u) == bstar; }, keys);
   int32_t* idx = a.idx + (size_t)r * a.k;
-  for (int j = threadIdx.x; j < a.k; j += NT) idx[j] = key_pos(keys[j]);
+  for (int j = threadIdx.x; j < a.k; j += kThreads) idx[j] = key_pos(keys[j]);
 }
 
 // ------------------------------------------------------------------ the kernel
-
-__device__ __forceinline__ uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Device operations of the barrier protocol (barrier_protocol.h) on one
-// global counter.
-struct GridOps {
-  uint32_t* c;
-  uint32_t* status;
-  __device__ void fence() { __threadfence(); }
-  __device__ void arrive() { atomicAdd(c, 1u); }
-  __device__ uint32_t count() { return ld_acquire(c); }
-  __device__ uint64_t now() { return gtimer(); }
-  __device__ void timeout() { raise_status(status, DSA_DEVICE_TIMEOUT); }
-};
-
-// Barrier over the whole grid (co-resident by the cooperative launch): the
-// CTA's writes are published before it arrives at counter c, and every later
-// read sees the other CTAs' writes.  Bounded: after limit_ns the CTA raises
-// DSA_DEVICE_TIMEOUT and returns false (the caller then exits).
-__device__ bool grid_barrier(uint32_t* c, uint32_t* status, uint64_t limit_ns) {
-  __shared__ int ok;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    GridOps ops{c, status};
-    ok = barrier_arrive_and_wait(ops, gridDim.x, limit_ns) ? 1 : 0;
-  }
-  __syncthreads();
-  return ok != 0;
-}
 
 // The selection parameters of row r, from its merged histogram (every thread
 // gets the same values).  h: kBuckets words of shared memory.
@@ -507,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
       __syncthreads();   // keys may still be read by the previous row
       for (int i = threadIdx.x; i < U; i += kThreads) keys[i] = surv[i];
       __syncthreads();
-      if (U > 1) sort_desc(keys, U);
+      if (U > 1) sort_desc<kThreads>(keys, U);
       for (int j = threadIdx.x; j < a.k; j += kThreads) idx[j] = j < n_take && j < U ? key_pos(keys[j]) : -1;
     }
     return;

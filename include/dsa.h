@@ -164,6 +164,12 @@ DSA_API const char* dsa_last_error_string(void);
  * DSA_INDEXER_DP4A or DSA_INDEXER_TC (host only; -1 if `p` is invalid). */
 DSA_API int dsa_indexer_kind(const dsa_problem* p);
 
+/* Kernels dsa_decode_step launches for problem `p`: 2 for a single query row
+ * of one request with 64 attention heads and a bf16 cache (indexer, then
+ * selection and attention in one kernel), else 3 (indexer, top-k, attention);
+ * 0 when R = 0; -1 if `p` is invalid (host only). */
+DSA_API int dsa_decode_step_kernels(const dsa_problem* p);
+
 /* Bytes of workspace every entry point below needs for problem `p` (host only;
  * 0 if `p` is invalid -- dsa_last_error_string() says why). */
 DSA_API size_t dsa_workspace_size(const dsa_problem* p);

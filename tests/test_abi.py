@@ -50,9 +50,15 @@ def _prob(dsa, **kw):
 def test_workspace_size_grows_with_rows_and_length(dsa):
     a = dsa.dsa_workspace_size(_prob(dsa))
     b = dsa.dsa_workspace_size(_prob(dsa, L_max=307200, L_total=307200))
-    c = dsa.dsa_workspace_size(_prob(dsa, R=32, B=32))
-    assert 0 < a < b and a < c
+    c = dsa.dsa_workspace_size(_prob(dsa, R=2, B=2))
+    d = dsa.dsa_workspace_size(_prob(dsa, R=32, B=32))
+    assert 0 < a < b and c < d
     assert a % 256 == 0
+    # One query row (the single-row step) reserves the attention units'
+    # partials: 128 units x 64 heads x 512 fp16 values at k = 2048.
+    assert a > 128 * 64 * 512 * 2
+    assert dsa.dsa_decode_step_kernels(_prob(dsa)) == 2
+    assert dsa.dsa_decode_step_kernels(_prob(dsa, R=2, B=2)) == 3
 
 
 def test_host_validation_rejects_before_launch(dsa):

@@ -171,13 +171,19 @@ def test_other_shapes(shape):
 
 
 def test_decode_step_equals_ops_and_is_deterministic():
+    # One query row takes the single-row kernel in the fused step: the same
+    # ordered indices as the separate calls, an output within the tolerance of
+    # the oracle (its accumulation order differs), and the same bits each run.
     x = gen.l64k(L=30000)
     a = run_ops(x, lse=False)
     b = run_step(x)
     c = run_step(x)
     for key in ("idx", "nsel", "out"):
-        assert np.array_equal(a[key], b[key]), key
         assert np.array_equal(b[key], c[key]), key
+    for key in ("idx", "nsel"):
+        assert np.array_equal(a[key], b[key]), key
+    _, _, ref = oracle.decode_step(x)
+    assert_out_close(b["out"][0], ref[0])
     assert b["status"] == 0
 
 
