@@ -44,6 +44,16 @@ indexer)):
                   step of 2,048 tokens, and the gathered sparse prefill over
                   query chunks), keys as ``l64k``.
 
+``front_end(...)`` draws the inputs of the indexer front end: one hidden vector
+per query row, x ~ N(0, 1) in bf16, and synthetic 8-bit affine weights for the
+query projection [H_i * D_i, d] and the head-weight projection [H_i, d]
+("GLM-5.3-Flash-Alis-MLX-4bit", page 3: the indexer projections at 8 bits in
+groups of 64, MLX affine form).  Codes are U{0..255}; each group of 64 inputs
+has scale s0 * U{192..320} / 256 and bias -scale * U{120..135}, both rounded to
+bf16, with s0 = sqrt(12) / (255 sqrt(d)), so each weight has standard deviation
+about 1 / sqrt(d) and each projection is about N(0, 1).  No trained weights
+exist here; these stand in for them.
+
 ``fp8_cache(x)`` turns any of them into the same problem over an FP8 latent
 cache ("glm53-tensorfold-spark", page 4: FP8 KV storage), stored the way a cache
 writer would store it: per row j, scale_j = max_d |kv[j, d]| / 448 (float32;
@@ -76,6 +86,10 @@ TAG_KV = 7
 TAG_LENGTHS = 8
 TAG_DISTINCT_VEC = 9
 TAG_DISTINCT_PICK = 10
+TAG_FE_X = 11
+TAG_FE_CODES = 12      # + 0 (query projection) or + 3 (head-weight projection)
+TAG_FE_SCALE = 13
+TAG_FE_BIAS = 14
 
 _CHUNK = 1 << 22
 
@@ -381,3 +395,39 @@ def fp8_cache(x: DecodeInputs, with_scale: bool = True) -> DecodeInputs:
     codes = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     return dataclasses.replace(x, name=x.name + "_fp8", kv=np.ascontiguousarray(codes),
                                kv_format="e4m3", kv_scale=kv_scale)
+
+
+@dataclasses.dataclass
+class FrontEndInputs:
+    """Inputs of the indexer front end, host arrays only: ``x`` bf16 bits
+    [R, d]; ``wq`` = (codes uint8 [H_i * D_i, d], scale bf16 bits [H_i * D_i, d/64],
+    bias bf16 bits [H_i * D_i, d/64]); ``ww`` the same for [H_i, d]."""
+    name: str
+    R: int
+    d: int
+    H_i: int
+    D_i: int
+    x: np.ndarray
+    wq: tuple
+    ww: tuple
+
+
+def _affine_weights(seed: int, which: int, O: int, d: int):
+    g = d // 64
+    codes = uniform_int(seed, TAG_FE_CODES + 3 * which, O * d, 0, 255).astype(np.uint8).reshape(O, d)
+    s0 = np.sqrt(12.0) / (255.0 * np.sqrt(d))
+    scale = s0 * uniform_int(seed, TAG_FE_SCALE + 3 * which, O * g, 192, 320).astype(np.float64) / 256.0
+    scale_bits = f32_to_bf16_bits(scale.astype(np.float32))
+    bias = -bf16_bits_to_f64(scale_bits) * uniform_int(seed, TAG_FE_BIAS + 3 * which, O * g, 120, 135)
+    bias_bits = f32_to_bf16_bits(bias.astype(np.float32))
+    return codes, scale_bits.reshape(O, g), bias_bits.reshape(O, g)
+
+
+def front_end(R: int = 1, d: int = 6144, H_i: int = 64, D_i: int = 128, seed: int = 0x5EED) -> FrontEndInputs:
+    """Seeded front-end inputs (see the module docstring); ``d`` a multiple of 64."""
+    if d % 64:
+        raise ValueError("d must be a multiple of 64 (the weight group)")
+    x = normal_bf16(seed, TAG_FE_X, R * d).reshape(R, d)
+    return FrontEndInputs(name=f"front_R{R}_d{d}", R=R, d=d, H_i=H_i, D_i=D_i, x=x,
+                          wq=_affine_weights(seed, 0, H_i * D_i, d),
+                          ww=_affine_weights(seed, 1, H_i, d))

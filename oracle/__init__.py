@@ -14,6 +14,10 @@ int64 integers and float64 reals, no blocking and no reordering:
 * ``sparse_attention`` -- softmax attention of every query head over the
   selected latent rows only (page 1: "roughly 2,048 selected positions");
 * ``decode_step``     -- the three in sequence;
+* ``indexer_front_end`` -- the indexer query and head weights of each row,
+  projected from its hidden vector by 8-bit affine weights and quantised to the
+  indexer's integer operands ("GLM-5.3-Flash-Alis-MLX-4bit", page 3: the
+  indexer projections at 8 bits, groups of 64), with ``dequantize_affine``;
 * ``e4m3_to_f64``     -- the FP8 E4M3 code of the FP8 latent cache
   ("glm53-tensorfold-spark", page 4: FP8 KV storage), decoded from the format's
   definition.
@@ -32,6 +36,8 @@ from .dsa import (  # noqa: F401
     attention_lse,
     decode_step,
     e4m3_to_f64,
+    dequantize_affine,
+    indexer_front_end,
     INT32_MIN,
     INT32_MAX,
 )

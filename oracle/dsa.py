@@ -184,3 +184,79 @@ def decode_step(inp, relu=True, rows=None):
         outs.append(sparse_attention(inp.q[r], inp.kv[lo:hi], idx[j], inp.D_v, inp.softmax_scale, sc))
     out = np.stack(outs) if outs else np.zeros((0, inp.H_q, inp.D_v))
     return scores, idx, out
+
+
+def dequantize_affine(codes, scale_bits, bias_bits, group=64):
+    """Weights stored as 8-bit affine codes with one scale and one bias per
+    group of ``group`` consecutive inputs, as float64.
+
+    ``codes`` uint8 [O, d]; ``scale_bits``, ``bias_bits`` bf16 bits [O, d / group].
+    Weight (o, i) is ``scale[o, i // group] * codes[o, i] + bias[o, i // group]``
+    -- the affine group quantisation that "GLM-5.3-Flash-Alis-MLX-4bit" (page 3,
+    the Recipe table and the note under it) keeps the DSA indexer projections in:
+    8 bits, groups of 64, packed in the standard MLX affine form (codes 0..255,
+    scales and biases in the model's 16-bit type).
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.float64)
+    O, d = c.shape
+    s = _bf16_to_f64(scale_bits).reshape(O, d // group)
+    b = _bf16_to_f64(bias_bits).reshape(O, d // group)
+    return c * np.repeat(s, group, axis=1) + np.repeat(b, group, axis=1)
+
+
+def _round_half_even(v):
+    return np.rint(v)   # numpy rounds halves to even
+
+
+def indexer_front_end(x, wq, ww, H_i, D_i, q_max, w_max):
+    """Indexer query and head weights of each row from its hidden vector.
+
+    ``x`` bf16 bits [R, d]; ``wq`` = (codes [H_i * D_i, d], scales, biases) and
+    ``ww`` = (codes [H_i, d], scales, biases), both in the 8-bit affine form of
+    ``dequantize_affine``.  In float64, for each row:
+
+        qf[h, :] = Wq[h * D_i : (h + 1) * D_i] @ x     (the indexer query, per head)
+        wf[h]    = Ww[h] @ x                            (the head weight)
+
+    then the integer operands the indexer takes (int8 q_idx, int32 w_idx within
+    the declared bounds q_max and w_max):
+
+        sigma_h  = max_j |qf[h, j]| / q_max
+        q_idx    = clip(round(qf[h, j] / sigma_h), -q_max, q_max)
+        u_h      = wf[h] * sigma_h
+        tau      = max_h |u_h| / w_max
+        w_idx    = clip(round(u_h / tau), -w_max, w_max)
+
+    with round-half-to-even, and zero codes where sigma_h or tau is 0.  Since
+    sigma_h > 0, sum_h wf_h max(0, qf_h . k) = sum_h u_h max(0, (qf_h / sigma_h) . k),
+    so tau * (the integer score of q_idx, w_idx) approximates the score of the
+    real-valued projections: each head's query scale folds into its weight.
+    The pages fix only the weight format (page 3); the projection from one hidden
+    vector, the per-head symmetric query scale and the per-row weight scale are
+    the readings taken.  Returns a dict of float64 ``proj`` [R, H_i * D_i + H_i]
+    (qf then wf), int8 ``q_idx`` [R, H_i, D_i], int32 ``w_idx`` [R, H_i], float64
+    ``q_scale`` [R, H_i] (sigma) and ``w_scale`` [R] (tau).
+    """
+    X = _bf16_to_f64(x)
+    R = X.shape[0]
+    Wq = dequantize_affine(*wq)
+    Ww = dequantize_affine(*ww)
+    qf = (X @ Wq.T).reshape(R, H_i, D_i)
+    wf = X @ Ww.T                                                  # [R, H_i]
+    amax = np.abs(qf).max(axis=2)                                  # [R, H_i]
+    sigma = amax / q_max
+    safe = np.where(sigma > 0, sigma, 1.0)
+    q = np.where(sigma[:, :, None] > 0, _round_half_even(qf / safe[:, :, None]), 0.0)
+    q = np.clip(q, -q_max, q_max)
+    u = wf * sigma
+    tau = np.abs(u).max(axis=1) / w_max                            # [R]
+    safe_t = np.where(tau > 0, tau, 1.0)
+    w = np.where(tau[:, None] > 0, _round_half_even(u / safe_t[:, None]), 0.0)
+    w = np.clip(w, -w_max, w_max)
+    return {
+        "proj": np.concatenate([qf.reshape(R, H_i * D_i), wf], axis=1),
+        "q_idx": q.astype(np.int8),
+        "w_idx": w.astype(np.int32),
+        "q_scale": sigma,
+        "w_scale": tau,
+    }
