@@ -14,6 +14,10 @@ Entry points mirror the C names::
     dsa_sparse_attn(prob, idx, nsel, out, lse, ws)
     dsa_decode_step(prob, idx, nsel, out, ws)
     dsa_read_device_status(ws)
+
+and the indexer front end (``include/dsa_front_end.h``)::
+
+    dsa_indexer_front_end(prob, d, x, wq, ww, q_idx, w_idx, ws_front, ...)
 """
 from __future__ import annotations
 
@@ -50,6 +54,8 @@ EXPORTS = ("dsa_version", "dsa_last_error_string", "dsa_indexer_kind", "dsa_deco
            "dsa_index_scores",
            "dsa_topk", "dsa_topk_static", "dsa_sparse_attn", "dsa_decode_step",
            "dsa_read_device_status", "dsa_get_device_status",
+           # include/dsa_front_end.h
+           "dsa_front_end_workspace_size", "dsa_indexer_front_end",
            # include/dsa_testing.h
            "dsa_test_topk_missing_arrival", "dsa_test_attn_missing_gather",
            "dsa_test_indexer_missing_tile")
@@ -68,6 +74,10 @@ class dsa_problem(ctypes.Structure):
         ("row_offsets", ctypes.c_void_p), ("row_len", ctypes.c_void_p),
         ("kv_scale", ctypes.c_void_p),
     ]
+
+
+class dsa_affine_weights(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p)]
 
 
 class DsaError(RuntimeError):
@@ -90,6 +100,9 @@ def _load() -> ctypes.CDLL:
     lib.dsa_decode_step_kernels.argtypes = [P]
     lib.dsa_workspace_size.restype = sz
     lib.dsa_workspace_size.argtypes = [P]
+    lib.dsa_front_end_workspace_size.restype = sz
+    lib.dsa_front_end_workspace_size.argtypes = [P, ctypes.c_int32]
+    W = ctypes.POINTER(dsa_affine_weights)
     for name, args in (
         ("dsa_index_scores", [P, vp, vp, sz, vp]),
         ("dsa_topk", [P, vp, vp, vp, vp, sz, vp]),
@@ -98,6 +111,7 @@ def _load() -> ctypes.CDLL:
         ("dsa_decode_step", [P, vp, vp, vp, vp, sz, vp]),
         ("dsa_read_device_status", [vp, vp, ctypes.POINTER(ctypes.c_int32)]),
         ("dsa_get_device_status", [vp, vp]),
+        ("dsa_indexer_front_end", [P, ctypes.c_int32, vp, W, W, vp, vp, vp, vp, vp, vp, sz, vp]),
         ("dsa_test_topk_missing_arrival", [P, vp, vp, vp, vp, sz, ctypes.c_int, ctypes.c_int64, vp]),
         ("dsa_test_attn_missing_gather", [P, vp, vp, vp, vp, vp, sz, ctypes.c_int64, vp]),
         ("dsa_test_indexer_missing_tile", [P, vp, vp, sz, ctypes.c_int64, vp]),
@@ -316,3 +330,30 @@ def dsa_read_device_status(ws, stream=None) -> int:
     if st not in (DSA_OK, DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX):
         _check(st)
     return bits.value
+
+
+# Indexer front end (include/dsa_front_end.h).
+
+def affine_weights(codes, scales, biases) -> dsa_affine_weights:
+    """The three device tensors of one 8-bit affine weight matrix."""
+    return dsa_affine_weights(codes.data_ptr(), scales.data_ptr(), biases.data_ptr())
+
+
+def dsa_front_end_workspace_size(prob: Problem, d: int) -> int:
+    n = _lib.dsa_front_end_workspace_size(ctypes.byref(prob.c), int(d))
+    if n == 0:
+        raise DsaError(DSA_ERR_INVALID_ARG, _lib.dsa_last_error_string().decode())
+    return n
+
+
+def dsa_indexer_front_end(prob: Problem, d: int, x, wq, ww, q_idx, w_idx, ws, q_scale=None,
+                          w_scale=None, proj=None, stream=None) -> None:
+    """``wq``/``ww``: (codes, scales, biases) device tensors or dsa_affine_weights."""
+    if not isinstance(wq, dsa_affine_weights):
+        wq = affine_weights(*wq)
+    if not isinstance(ww, dsa_affine_weights):
+        ww = affine_weights(*ww)
+    _check(_lib.dsa_indexer_front_end(ctypes.byref(prob.c), int(d), _ptr(x), ctypes.byref(wq),
+                                      ctypes.byref(ww), _ptr(q_idx), _ptr(w_idx), _ptr(q_scale),
+                                      _ptr(w_scale), _ptr(proj), _ptr(ws), ws.numel(),
+                                      _stream(stream)))

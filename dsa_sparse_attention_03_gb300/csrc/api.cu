@@ -306,6 +306,106 @@ dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* nsel, ui
   return DSA_OK;
 }
 
+// ------------------------------------------------------------------ front end
+
+namespace {
+
+// Workspace of the front end: status word, one arrival ticket per pass (at most
+// R passes), per-pass head counters and the per-head maxima, all zeroed before
+// the kernel; then the projections, rows padded to a multiple of 4 floats.
+struct FrontPlan {
+  int q_max, w_max, y_stride;
+  size_t off_ticket, off_cnt, off_amax, zero_end, off_y, total;
+};
+
+dsa_status front_plan(const dsa_problem* p, int32_t d, FrontPlan* fp) {
+  if (!p) return fail(DSA_ERR_INVALID_ARG, "problem is NULL");
+  if (p->R < 0 || p->R > 65535) return fail(DSA_ERR_INVALID_ARG, "R=%d outside [0,65535]", p->R);
+  if (p->H_i < 1 || p->H_i > 128) return fail(DSA_ERR_UNSUPPORTED, "H_i=%d outside [1,128]", p->H_i);
+  if (p->D_i != 32 && p->D_i != 64 && p->D_i != 128 && p->D_i != 256)
+    return fail(DSA_ERR_UNSUPPORTED, "D_i=%d not in {32,64,128,256}", p->D_i);
+  if (d < 512 || d > 8192 || d % 512)
+    return fail(DSA_ERR_UNSUPPORTED, "d=%d is not a multiple of 512 in [512,8192]", d);
+  if (p->qk_abs_max < 0 || p->qk_abs_max > 128)
+    return fail(DSA_ERR_INVALID_ARG, "qk_abs_max=%d outside [0,128]", p->qk_abs_max);
+  if (p->w_abs_max < 0 || p->w_abs_max > (1 << 24))
+    return fail(DSA_ERR_INVALID_ARG, "w_abs_max=%d outside [0,2^24]", p->w_abs_max);
+  fp->q_max = (p->qk_abs_max == 0 || p->qk_abs_max == 128) ? 127 : p->qk_abs_max;
+  fp->w_max = p->w_abs_max > 0 ? p->w_abs_max : 4;
+  const size_t R = size_t(p->R);
+  const int O = p->H_i * p->D_i + p->H_i;
+  fp->y_stride = (O + 3) / 4 * 4;
+  size_t off = 256;
+  fp->off_ticket = off; off = align_up(off + R * 4, 256);
+  fp->off_cnt = off; off = align_up(off + R * size_t(p->H_i) * 4, 256);
+  fp->off_amax = off; off = align_up(off + R * size_t(p->H_i) * 4, 256);
+  fp->zero_end = off;
+  fp->off_y = off; off = align_up(off + R * size_t(fp->y_stride) * 4, 256);
+  fp->total = off;
+  return DSA_OK;
+}
+
+dsa_status check_affine(const dsa_affine_weights* w, const char* name) {
+  if (!w || !w->codes || !w->scales || !w->biases)
+    return fail(DSA_ERR_INVALID_ARG, "%s: codes, scales and biases must be set", name);
+  if (!aligned(w->codes, 16) || !aligned(w->scales, 16) || !aligned(w->biases, 16))
+    return fail(DSA_ERR_INVALID_ARG, "%s: codes, scales and biases must be 16-byte aligned", name);
+  return DSA_OK;
+}
+
+}  // namespace
+
+size_t dsa_front_end_workspace_size(const dsa_problem* p, int32_t d) {
+  g_err.clear();
+  FrontPlan fp;
+  if (front_plan(p, d, &fp) != DSA_OK) return 0;
+  return fp.total;
+}
+
+dsa_status dsa_indexer_front_end(const dsa_problem* p, int32_t d, const uint16_t* x,
+                                 const dsa_affine_weights* wq, const dsa_affine_weights* ww,
+                                 int8_t* q_idx, int32_t* w_idx, float* q_scale, float* w_scale,
+                                 float* proj, void* ws, size_t ws_bytes, void* stream) {
+  g_err.clear();
+  FrontPlan fp;
+  dsa_status s = front_plan(p, d, &fp);
+  if (s != DSA_OK) return s;
+  if (p->R == 0) return DSA_OK;
+  if ((s = check_affine(wq, "wq")) != DSA_OK) return s;
+  if ((s = check_affine(ww, "ww")) != DSA_OK) return s;
+  if (!x || !q_idx || !w_idx) return fail(DSA_ERR_INVALID_ARG, "x, q_idx and w_idx must be set");
+  if (!aligned(x, 16) || !aligned(q_idx, 16) || !aligned(w_idx, 4))
+    return fail(DSA_ERR_INVALID_ARG, "x and q_idx must be 16-byte aligned, w_idx 4-byte");
+  if (!aligned(q_scale, 4) || !aligned(w_scale, 4) || !aligned(proj, 4))
+    return fail(DSA_ERR_INVALID_ARG, "q_scale, w_scale and proj must be 4-byte aligned");
+  if (!ws || !aligned(ws, 256)) return fail(DSA_ERR_INVALID_ARG, "ws must be set and 256-byte aligned");
+  if (ws_bytes < fp.total)
+    return fail(DSA_ERR_INVALID_ARG, "ws_bytes=%zu below the required %zu", ws_bytes, fp.total);
+  char* w = static_cast<char*>(ws);
+  FrontArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.wq = wq->codes; a.sq = wq->scales; a.bq = wq->biases;
+  a.ww = ww->codes; a.sw = ww->scales; a.bw = ww->biases;
+  a.x = x;
+  a.R = p->R; a.d = d; a.H_i = p->H_i; a.D_i = p->D_i; a.Oq = p->H_i * p->D_i;
+  a.q_max = fp.q_max; a.w_max = fp.w_max;
+  a.y_stride = fp.y_stride;
+  a.y = reinterpret_cast<float*>(w + fp.off_y);
+  a.proj = proj;
+  a.amax = reinterpret_cast<uint32_t*>(w + fp.off_amax);
+  a.ticket = reinterpret_cast<uint32_t*>(w + fp.off_ticket);
+  a.cnt = reinterpret_cast<uint32_t*>(w + fp.off_cnt);
+  a.status = reinterpret_cast<uint32_t*>(w);
+  a.wait_ns = kDefaultWaitNs;
+  a.q_idx = q_idx; a.w_idx = w_idx; a.q_scale = q_scale; a.w_scale = w_scale;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, fp.zero_end, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear workspace");
+  e = launch_front_end(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "indexer front end");
+  return DSA_OK;
+}
+
 // ------------------------------------------------------------------ test hooks
 
 static dsa_status check_limit(int64_t limit_ns, TestHooks* h) {

@@ -8,6 +8,7 @@
 
 #include "dsa.h"
 #include "dsa_testing.h"
+#include "dsa_front_end.h"
 
 namespace dsa {
 
@@ -214,5 +215,34 @@ constexpr size_t kRowKeepBytes = 256 + 8192 * 4;       // arrival counter of the
 constexpr int kRowRedoWord = 2;    // words 2, 3: a bin cursor ran past its bin in the first / second scatter
 cudaError_t launch_decode_row(const dsa_problem& p, const Plan& pl, const int32_t* scores, int32_t* idx,
                               int32_t* nsel, uint16_t* out, char* ws, cudaStream_t st);
+
+// Indexer front end (front_end.cu): affine 8-bit projections of the hidden rows
+// and their quantisation to q_idx / w_idx.
+struct FrontArgs {
+  const uint8_t* wq;          // [Oq, d] codes
+  const uint16_t* sq;         // [Oq, d / 64] bf16 scales
+  const uint16_t* bq;         // [Oq, d / 64] bf16 biases
+  const uint8_t* ww;          // [H_i, d]
+  const uint16_t* sw;
+  const uint16_t* bw;
+  const uint16_t* x;          // [R, d] bf16
+  int R, d, H_i, D_i, Oq;     // Oq = H_i * D_i
+  int q_max, w_max;
+  int rows_max;               // set by the launcher: output rows per CTA, at most
+  int stages;                 // set by the launcher: weight rows in flight per CTA
+  int y_stride;               // floats per row of y (a multiple of 4)
+  float* y;                   // [R, y_stride] workspace: the projections
+  float* proj;                // [R, Oq + H_i] or null
+  uint32_t* amax;             // [R, H_i] workspace, zeroed: max |qf| per head (float bits)
+  uint32_t* ticket;           // [passes] workspace, zeroed: CTAs done with each pass
+  uint32_t* cnt;              // [passes, H_i] workspace, zeroed: rows done of each query head
+  uint32_t* status;           // the workspace's status word
+  uint64_t wait_ns;           // limit of every bounded wait
+  int8_t* q_idx;
+  int32_t* w_idx;
+  float* q_scale;             // or null
+  float* w_scale;             // or null
+};
+cudaError_t launch_front_end(FrontArgs a, cudaStream_t st);
 
 }  // namespace dsa

@@ -86,9 +86,20 @@ __device__ __forceinline__ void bulk_row(uint32_t dst, const void* src, uint32_t
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
+// One non-blocking test of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase of parity `parity`: false (and DSA_DEVICE_TIMEOUT
-// raised, if `status`) once `limit_ns` have passed.
+// raised, if `status`) once `limit_ns` have passed.  A phase that has already
+// completed returns at once, without reading the clock.
 static __device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status, uint64_t limit_ns) {
+  if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = gtimer();
   for (;;) {
     uint32_t ok;

@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include "dsa.h"
+#include "dsa_front_end.h"
 
 #define BAD_WS ((void*)(uintptr_t)0x100010)
 
@@ -78,6 +79,19 @@ int main(void) {
   CHECK(dsa_index_scores(&p, (int32_t*)(uintptr_t)0x100000, BAD_WS, (size_t)1 << 40, NULL) ==
             DSA_ERR_OVERFLOW_RISK,
         "overflow bound rejected");
+  {
+    dsa_problem f = mla_problem(1, 4096);
+    dsa_affine_weights w;
+    w.codes = (const uint8_t*)(uintptr_t)0x100000;
+    w.scales = (const uint16_t*)(uintptr_t)0x100000;
+    w.biases = (const uint16_t*)(uintptr_t)0x100000;
+    const size_t n = dsa_front_end_workspace_size(&f, 6144);
+    CHECK(n > 0 && n % 256 == 0, "front-end workspace size");
+    CHECK(dsa_indexer_front_end(&f, 6144, (const uint16_t*)(uintptr_t)0x100008, &w, &w,
+                                (int8_t*)(uintptr_t)0x100000, (int32_t*)(uintptr_t)0x100000, NULL,
+                                NULL, NULL, BAD_WS, n, NULL) == DSA_ERR_INVALID_ARG,
+          "misaligned hidden rows rejected");
+  }
   printf("all ok\n");
   return 0;
 }

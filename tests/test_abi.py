@@ -143,3 +143,32 @@ def test_binding_marshals_fp8_cache_and_flags(dsa):
     prob2, t2 = dsa.upload_inputs(y, device="cpu")
     assert prob2.c.flags == dsa.DSA_INDEXER_AUTO and not prob2.c.kv_scale
     assert t2["kv"].dtype.itemsize == 2
+
+
+def test_front_end_validation_and_workspace(dsa):
+    lib = dsa.lib()
+    fake = 1 << 20   # host validation only: nothing is launched when it fails
+    p = _prob(dsa, R=2, qk_abs_max=10, w_abs_max=4)
+    n = dsa.dsa_front_end_workspace_size(p, 6144)
+    O = 64 * 128 + 64
+    assert n % 256 == 0 and n >= 2 * (O + 3) // 4 * 4 * 4 + 2 * 64 * 4 + 256
+    assert lib.dsa_front_end_workspace_size(ctypes.byref(p.c), 640) == 0   # not a multiple of 512
+    assert b"multiple of 512" in lib.dsa_last_error_string()
+    w = dsa.dsa_affine_weights(fake, fake, fake)
+    ws = ctypes.c_void_p(fake)
+
+    def call(prob=p, d=6144, x=fake, wq=w, ww=w, q=fake, wi=fake, ws=ws, nbytes=n):
+        return lib.dsa_indexer_front_end(ctypes.byref(prob.c), d, x, ctypes.byref(wq), ctypes.byref(ww),
+                                         q, wi, None, None, None, ws, nbytes, None)
+
+    assert call(x=None) == dsa.DSA_ERR_INVALID_ARG
+    assert call(x=fake + 8) == dsa.DSA_ERR_INVALID_ARG and b"16-byte" in lib.dsa_last_error_string()
+    assert call(wq=dsa.dsa_affine_weights(fake + 4, fake, fake)) == dsa.DSA_ERR_INVALID_ARG
+    assert call(wq=dsa.dsa_affine_weights(fake, fake + 2, fake)) == dsa.DSA_ERR_INVALID_ARG
+    assert call(ww=dsa.dsa_affine_weights(fake, None, fake)) == dsa.DSA_ERR_INVALID_ARG
+    assert call(nbytes=n - 1) == dsa.DSA_ERR_INVALID_ARG and b"required" in lib.dsa_last_error_string()
+    assert call(ws=ctypes.c_void_p(fake + 16)) == dsa.DSA_ERR_INVALID_ARG
+    assert call(prob=_prob(dsa, R=2, D_i=48)) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(prob=_prob(dsa, R=2, qk_abs_max=200)) == dsa.DSA_ERR_INVALID_ARG
+    assert call(d=65536) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(prob=_prob(dsa, R=0)) == dsa.DSA_OK    # nothing to do, nothing enqueued
