@@ -28,6 +28,12 @@ import sys
 import threading
 import time
 
+# The CPU oracle's float64 matrix products must not spread over several BLAS
+# threads behind a "cores" count: every process that runs it uses one thread
+# (spawned workers inherit this environment).
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
 import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -241,6 +247,7 @@ def bench_ours(args):
     ms_per_step = ms / args.steps
     us_per_layer = job_us_per_layer(ms_per_step, n_layers, world)
     status = dsa.dsa_read_device_status(ws, stream=sp)
+    spread = replay_spread(graph, step, stream, n_layers) if not args.no_extras else None
 
     # Dominant kernel: the indexer alone, back to back over the layers (a CUDA
     # graph of 3 x n_layers launches, so host enqueue time never shows), with
@@ -324,6 +331,7 @@ def bench_ours(args):
                      "traffic_source": "profiles/indexer_tc_l300k_full.md (ncu, same kernel source)",
                      "algorithmic_bytes_per_launch": idx_bytes,
                      "avg_launch_us": round(idx_avg_ms * 1000, 3)},
+        "replay_us_per_layer": spread,
         "stages_us_per_layer": stages,
         "secondary": sec,
         "e2e": e2e,
@@ -332,8 +340,31 @@ def bench_ours(args):
         "device_status": status,
     }
     if not args.no_cpu_baseline and not args.no_extras and world == 1:
-        res["cpu_baseline"] = cpu_baseline(layers_for_cpu=[x for x, _, _ in layers[:4]])
+        res["cpu_baseline"] = cpu_baseline()
     return res
+
+
+def replay_spread(graph, step, stream, n_layers, n=200):
+    """Per-step distribution: n steps timed one by one (CUDA events around each
+    replay), in us per layer."""
+    import torch
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+            e1.record(stream)
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    v = np.array([a.elapsed_time(b) * 1000.0 / n_layers for a, b in evs])
+    return {"n": n, "p10": round(float(np.percentile(v, 10)), 3), "p50": round(float(np.median(v)), 3),
+            "p90": round(float(np.percentile(v, 90)), 3), "min": round(float(v.min()), 3),
+            "max": round(float(v.max()), 3)}
 
 
 def indexer_traffic():
@@ -506,19 +537,59 @@ def bench_l64k(args, stream, device, kv="bf16"):
             "cuda_graph": graph is not None}
 
 
-def cpu_baseline(layers_for_cpu):
-    """The CPU oracle, as it stands, on a bounded sample: full decode steps of a
-    few of the long-context layers."""
+def _oracle_layer_worker(args):
+    """One spawned worker: draw layer `layer` of the L=307200 workload, wait for
+    the others, time one oracle decode step.  Returns (start, end) on the
+    system-wide monotonic clock."""
+    layer, barrier = args
     import oracle
+    x = gen.l300k(layer=layer)
+    barrier.wait()
     t0 = time.perf_counter()
-    for x in layers_for_cpu:
-        oracle.decode_step(x)
-    dt = time.perf_counter() - t0
-    n = len(layers_for_cpu)
-    return {"value": round(dt * 1e6 / n, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} of the 11 L=307200 layers, full decode step each (numpy int64 "
-                      f"scores, stable sort, float64 attention; single-threaded int64 matmul)",
-            "seconds": round(dt, 2)}
+    oracle.decode_step(x)
+    return t0, time.perf_counter()
+
+
+_BARRIER = None
+
+
+def _pool_init(b):
+    global _BARRIER
+    _BARRIER = b
+
+
+def _oracle_layer_task(layer):
+    return _oracle_layer_worker((layer, _BARRIER))
+
+
+def _oracle_layers_parallel(n_proc):
+    """n_proc layers, one per spawned process (one BLAS thread each), all
+    started together; returns the wall time from the first start to the last
+    end."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    b = ctx.Barrier(n_proc)
+    with ctx.Pool(n_proc, initializer=_pool_init, initargs=(b,)) as pool:
+        spans = pool.map(_oracle_layer_task, range(n_proc))
+    return max(e for _, e in spans) - min(s for s, _ in spans)
+
+
+def cpu_baseline():
+    """The CPU oracle, as it stands, on a bounded sample of the workload: full
+    decode steps of single L=307200 layers, on one core and on all host cores
+    (one layer per process, spawned, one BLAS thread per process)."""
+    cores = os.cpu_count() or 1
+    n_all = max(1, min(cores, 16))
+    t1 = _oracle_layers_parallel(1)
+    tn = _oracle_layers_parallel(n_all) if n_all > 1 else t1
+    return {"value": round(tn * 1e6 / n_all, 1), "unit": UNIT, "cores": n_all, "kind": "oracle",
+            "host_cores": cores,
+            "sample": f"{n_all} of the L=307200 layers (layers 0..{n_all - 1}), one full decode step each, "
+                      f"one per process on {n_all} cores at once (numpy int64 scores, stable sort, float64 "
+                      f"attention, one BLAS thread per process); value = wall time / layers",
+            "seconds": round(tn, 2),
+            "single_core": {"value": round(t1 * 1e6, 1), "unit": UNIT, "cores": 1,
+                            "sample": "layer 0, one full decode step, one process, one BLAS thread"}}
 
 
 def _prefix(x, n):
@@ -591,6 +662,74 @@ def bench_workload(args):
             "gpu_launches": reps * kernels_per_step(prob), "device_status": status}
 
 
+def bench_ab(args):
+    """Paired A/B of two variants of the headline step, run in ABBA order: each
+    round times A, B, B, A (one graph replay of all layers each, CUDA events
+    around each replay) and takes the ratio (B1 + B2) / (A1 + A2), so that
+    clock or thermal drift within a round cancels.  Reports the per-round
+    ratio's median and spread, and each arm's median us/layer."""
+    import torch
+    import dsa_sparse_attention_03_gb300 as dsa
+    world, rank, local = _dist_env()
+    if rank != 0:
+        return None
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=device)
+    sp = stream.cuda_stream
+    n_layers = args.layers
+    if args.ab == "indexer":
+        names = ("tc", "dp4a")
+        arms = []
+        for ix in names:
+            layers, ws, idx, nsel, out = make_layers(n_layers, L_LONG, device)
+            for _, prob, _ in layers:
+                prob.set(flags=(prob.c.flags & ~0xF) | dsa.INDEXERS[ix])
+            arms.append((layers, ws, idx, nsel, out))
+    else:
+        names = ("bf16", "fp8")
+        arms = [make_layers(n_layers, L_LONG, device, kv=kv) for kv in names]
+    graphs = []
+    for layers, ws, idx, nsel, out in arms:
+        def step(layers=layers, ws=ws, idx=idx, nsel=nsel, out=out):
+            for i, (_, prob, _) in enumerate(layers):
+                dsa.dsa_decode_step(prob, idx[i], nsel[i], out[i], ws, stream=sp)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        graphs.append(g)
+    rounds = max(20, min(args.steps, 200))
+    evs = []
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
+        for _ in range(rounds):
+            for arm in (0, 1, 1, 0):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graphs[arm].replay()
+                e1.record(stream)
+                evs.append((arm, e0, e1))
+    torch.cuda.synchronize()
+    t = np.array([a.elapsed_time(b) * 1000.0 / n_layers for _, a, b in evs]).reshape(rounds, 4)
+    ratio = (t[:, 1] + t[:, 2]) / (t[:, 0] + t[:, 3])
+    statuses = [dsa.dsa_read_device_status(arm[1], stream=sp) for arm in arms]
+    return {"metric": f"paired ABBA ratio {names[1]} / {names[0]} of the L=300k decode step (us/layer)",
+            "value": round(float(np.median(ratio)), 4), "unit": "ratio", "n_gpus": 1,
+            "rounds": rounds, "higher_is_better": False, "data": "synthetic",
+            "ratio_p10": round(float(np.percentile(ratio, 10)), 4),
+            "ratio_p90": round(float(np.percentile(ratio, 90)), 4),
+            "arms": {names[0]: round(float(np.median(np.r_[t[:, 0], t[:, 3]])), 3),
+                     names[1]: round(float(np.median(np.r_[t[:, 1], t[:, 2]])), 3)},
+            "config": {"workload": f"l300k, {n_layers} layers per replay, CUDA graph per arm", "ab": args.ab},
+            "device_status": statuses}
+
+
 def bench_reference(args):
     """The oracle, as it stands, on the host cores.  One timed step is a decode
     step of one L=307200 layer, or -- when --steps is large -- of its first L'
@@ -648,6 +787,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers per token (the headline workload runs 11)")
+    ap.add_argument("--ab", choices=["indexer", "kv"],
+                    help="paired ABBA comparison instead of the headline: tensor-core vs dp4a indexer, "
+                         "or bf16 vs FP8 latent cache")
     ap.add_argument("--no-extras", action="store_true",
                     help="only the headline timing (no e2e, L=64k point or CPU baseline); for profiling")
     args = ap.parse_args()
@@ -655,6 +797,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         res = bench_reference(args)
+    elif args.ab:
+        res = bench_ab(args)
     elif args.workload != "l300k":
         res = bench_workload(args)
     else:
