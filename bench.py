@@ -293,6 +293,27 @@ def bench_ours(args):
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     step_bytes = n_layers * (L_LONG * x0.D_i + x0.k * kvb + x0.H_q * x0.D_k * 2)
+    # The dominant kernel (ncu launch-list share, profiles/decode_step_l300k_launches.md)
+    # is the single-row selection-and-attention kernel.  It runs inside
+    # dsa_decode_step right after the indexer, so its live duration is the
+    # step's per-layer time minus the indexer's back-to-back launch time, both
+    # timed with CUDA events on the launching stream.  Its algorithmic bytes:
+    # the gathered latent rows, the row's scores, the queries and the output.
+    row_bytes = x0.k * kvb + L_LONG * 4 + x0.H_q * x0.D_k * 2 + x0.H_q * x0.D_v * 2
+    row_us = us_per_layer - idx_avg_ms * 1000.0
+    row_gbs = row_bytes / (row_us * 1e-6) / 1e9 if row_us > 0 else None
+    fused = kernels_per_step(layers[0][1]) == 2
+    row_roofline = {"kernel": "decode_row_kernel" if fused else "top-k + attention",
+                    "bound": "hbm", "achieved": None if row_gbs is None else round(row_gbs, 1),
+                    "peak": hbm_peak, "unit": "GB/s",
+                    "frac": None if row_gbs is None else round(row_gbs / hbm_peak, 4),
+                    "peak_source": peak_src,
+                    "traffic": profiled_traffic("decode_row_l300k_full.md", "decode_row.cu") if fused else None,
+                    "traffic_source": "profiles/decode_row_l300k_full.md (ncu, same kernel source)",
+                    "algorithmic_bytes_per_launch": row_bytes,
+                    "avg_launch_us": round(row_us, 3),
+                    "duration_source": "step us/layer minus the indexer's back-to-back us/launch (CUDA events)",
+                    "note": "latency-bound: a chain of dependent L2 round trips and two grid barriers"}
     in_bytes = n_layers * L_LONG * (x0.D_i + kvb)
     step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
 
@@ -324,13 +345,14 @@ def bench_ours(args):
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(1e6 / (us_per_layer * n_layers * world) * world, 2),
         "step_gbs": round(step_gbs, 1),
-        "roofline": {"kernel": "indexer (" + ("tc" if dsa.indexer_kind(layers[0][1]) == "tc" else "dp4a") + ")",
-                     "bound": "hbm", "achieved": round(idx_gbs, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(idx_gbs / hbm_peak, 4),
-                     "peak_source": peak_src, "traffic": indexer_traffic(),
-                     "traffic_source": "profiles/indexer_tc_l300k_full.md (ncu, same kernel source)",
-                     "algorithmic_bytes_per_launch": idx_bytes,
-                     "avg_launch_us": round(idx_avg_ms * 1000, 3)},
+        "roofline": row_roofline,
+        "roofline_indexer": {"kernel": "indexer (" + ("tc" if dsa.indexer_kind(layers[0][1]) == "tc" else "dp4a") + ")",
+                             "bound": "hbm", "achieved": round(idx_gbs, 1), "peak": hbm_peak,
+                             "unit": "GB/s", "frac": round(idx_gbs / hbm_peak, 4),
+                             "peak_source": peak_src, "traffic": profiled_traffic(),
+                             "traffic_source": "profiles/indexer_tc_l300k_full.md (ncu, same kernel source)",
+                             "algorithmic_bytes_per_launch": idx_bytes,
+                             "avg_launch_us": round(idx_avg_ms * 1000, 3)},
         "replay_us_per_layer": spread,
         "stages_us_per_layer": stages,
         "secondary": sec,
@@ -367,15 +389,15 @@ def replay_spread(graph, step, stream, n_layers, n=200):
             "max": round(float(v.max()), 3)}
 
 
-def indexer_traffic():
-    """DRAM bytes per indexer launch from the committed ncu summary, if the
-    kernel source is still the one it was captured from (else None)."""
+def profiled_traffic(summary="indexer_tc_l300k_full.md", source="indexer_tc.cu"):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    is still the one it was captured from (else None)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "indexer_tc_l300k_full.md")
-    src = os.path.join(ROOT, "dsa_sparse_attention_03_gb300", "csrc", "indexer_tc.cu")
+    path = os.path.join(ROOT, "profiles", summary)
+    src = os.path.join(ROOT, "dsa_sparse_attention_03_gb300", "csrc", source)
     try:
         lines = open(path).read().splitlines()
-        want = [l.split(":", 1)[1].strip() for l in lines if l.startswith("source sha256 indexer_tc.cu:")]
+        want = [l.split(":", 1)[1].strip() for l in lines if l.startswith(f"source sha256 {source}:")]
         val = [l.split(":", 1)[1].strip() for l in lines if l.startswith("dram bytes per launch:")]
         have = hashlib.sha256(open(src, "rb").read()).hexdigest()
     except OSError:
@@ -662,6 +684,82 @@ def bench_workload(args):
             "gpu_launches": reps * kernels_per_step(prob), "device_status": status}
 
 
+def bench_front_end(args):
+    """The indexer front end (dsa_indexer_front_end) of one decode row: hidden
+    width 6144, 64 indexer heads x 128, 8-bit affine weights (54 MB with their
+    scales and biases); four weight sets rotated (216 MB > L2), 20 calls per
+    CUDA graph.  Roofline: the weight, scale, bias and hidden-row bytes of a
+    call over its time, against the measured HBM copy bandwidth."""
+    import torch
+    import dsa_sparse_attention_03_gb300 as dsa
+    world, rank, local = _dist_env()
+    if rank != 0:
+        return None
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    R, d, H_i, D_i = 1, 6144, 64, 128
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    sets = []
+    for sd in range(4):
+        f = gen.front_end(R=R, d=d, H_i=H_i, D_i=D_i, seed=0x5EED + sd)
+        sets.append(([t(f.wq[0]), t(f.wq[1].view(np.int16)), t(f.wq[2].view(np.int16))],
+                     [t(f.ww[0]), t(f.ww[1].view(np.int16)), t(f.ww[2].view(np.int16))],
+                     t(f.x.view(np.int16))))
+    prob = dsa.Problem(R=R, B=1, H_i=H_i, D_i=D_i, H_q=1, D_k=16, D_v=16, k=1, L_max=1, L_total=1,
+                       softmax_scale=1.0, qk_abs_max=10, w_abs_max=4)
+    ws = torch.empty(dsa.dsa_front_end_workspace_size(prob, d), dtype=torch.uint8, device=device)
+    q_idx = torch.empty((R, H_i, D_i), dtype=torch.int8, device=device)
+    w_idx = torch.empty((R, H_i), dtype=torch.int32, device=device)
+    stream = torch.cuda.Stream(device=device)
+    sp = stream.cuda_stream
+    per_graph = 20
+
+    def calls():
+        for i in range(per_graph):
+            wq, ww, x = sets[i % 4]
+            dsa.dsa_indexer_front_end(prob, d, x, wq, ww, q_idx, w_idx, ws, stream=sp)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            calls()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        calls()
+    reps = max(5, min(args.steps, 100))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / (reps * per_graph)
+    status = dsa.dsa_read_device_status(ws, stream=sp)
+    O = H_i * D_i + H_i
+    nbytes = O * d + O * (d // 64) * 4 + R * d * 2 + R * (H_i * D_i + H_i * 4)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"metric": "indexer front end us per call (one decode row)", "value": round(us, 3),
+            "unit": "us/call", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
+            "higher_is_better": False, "dtype": "u8 affine weights x bf16 -> fp32 -> int8/int32",
+            "data": "synthetic",
+            "config": {"workload": "front end: R=1, d=6144, H_i=64, D_i=128, q_max=10, w_max=4",
+                       "l2": "4 weight sets (216 MB) rotated > L2; not flushed", "cuda_graph": True},
+            "roofline": {"kernel": "front_end_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                         "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "note": "time per call includes the memset node of the call's counters"},
+            "gpu_launches": reps * per_graph, "device_status": status}
+
+
 def bench_ab(args):
     """Paired A/B of two variants of the headline step, run in ABBA order: each
     round times A, B, B, A (one graph replay of all layers each, CUDA events
@@ -779,7 +877,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--workload", default="l300k", choices=["l300k", "l64k", "tiny", "batch32", "causal64", "prefill"],
+    ap.add_argument("--workload", default="l300k",
+                    choices=["l300k", "l64k", "tiny", "batch32", "causal64", "prefill", "front_end"],
                     help="l300k: the metric's 11-layer long-context step (default); the others time one "
                          "decode step of that workload")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
@@ -799,6 +898,8 @@ def main():
         res = bench_reference(args)
     elif args.ab:
         res = bench_ab(args)
+    elif args.workload == "front_end":
+        res = bench_front_end(args)
     elif args.workload != "l300k":
         res = bench_workload(args)
     else:
