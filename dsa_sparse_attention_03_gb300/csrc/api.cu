@@ -111,11 +111,15 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   const int hgroups = p->H_q > 0 ? (p->H_q + kAttnHeads - 1) / kAttnHeads : 0;
   P.attn_kc_max = attn_clusters(p->R, hgroups, p->k);
   P.off_acnt = off; off = align_up(off + R * size_t(hgroups) * 16 * 4, 256);
-  // Single-row decode step (one layout for every entry point): its histogram
-  // and arrival counters start at zero.
+  // Single-row decode step (one layout for every entry point): its histogram,
+  // bin cursors and survivor slots start at zero.
   P.fused_row = decode_row_supported(*p) ? 1 : 0;
   P.off_lhist = off;
   if (P.fused_row) off = align_up(off + kRowHistBytes, 256);
+  P.off_lcur = off;
+  if (P.fused_row) off = align_up(off + kRowCursorBytes, 256);
+  P.off_lsurv = off;
+  if (P.fused_row) off = align_up(off + kRowSurvBytes, 256);
   P.zero_end = off;
   P.off_lkeep = off;
   if (P.fused_row) off = align_up(off + kRowKeepBytes, 256);

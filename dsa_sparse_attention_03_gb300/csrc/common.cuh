@@ -44,6 +44,7 @@ struct Plan {
   int attn_kc_max;          // attention: clusters per (row, head group), at most
   int fused_row;            // dsa_decode_step runs the single-row kernel (decode_row.cu)
   size_t off_status, off_state, off_hist, off_acnt, off_lhist, zero_end;
+  size_t off_lcur, off_lsurv;   // single-row step: bin cursors and survivor slots (cleared)
   size_t off_lkeep;         // single-row step: words the indexer must not clear (see decode_row.cu)
   size_t off_surv, off_scores, off_apart, off_rpart, total;
 };
@@ -210,9 +211,9 @@ size_t decode_row_partials_bytes(const dsa_problem& p);
 constexpr int kRowHistCopies = 8;   // CTA c of the indexer adds into copy c % 8 (spreads the atomics)
 constexpr size_t kRowHistWords = 8192 + 64;             // one copy: log-bin histogram and its coarse sums
 constexpr size_t kRowHistBytes = kRowHistCopies * kRowHistWords * 4;
-constexpr size_t kRowKeepBytes = 256 + 8192 * 4;       // arrival counter of the indexer's CTAs; bin cursors
-// Status-block words of the single-row step (the block is cleared by the indexer).
-constexpr int kRowRedoWord = 2;    // words 2, 3: a bin cursor ran past its bin in the first / second scatter
+constexpr size_t kRowCursorBytes = 8192 * 4;          // bin cursors of the scatter (cleared each step)
+constexpr size_t kRowSurvBytes = 4096 * 8;             // survivor slots (cleared each step: 0 = not yet written)
+constexpr size_t kRowKeepBytes = 256;                  // arrival counter of the indexer's CTAs (not cleared)
 cudaError_t launch_decode_row(const dsa_problem& p, const Plan& pl, const int32_t* scores, int32_t* idx,
                               int32_t* nsel, uint16_t* out, char* ws, cudaStream_t st);
 

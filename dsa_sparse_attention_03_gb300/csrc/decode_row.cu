@@ -69,6 +69,29 @@ static_assert(kCoarse == 64, "P phase: two coarse bins per lane of one warp");
 
 enum RowMode : uint32_t { kRowEmpty = 0, kRowFast = 1, kRowExact = 2 };
 
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+// A survivor slot, once its scatterer has written it (keys are never 0).
+// Bounded: 0 and DSA_DEVICE_TIMEOUT once limit_ns have passed.
+__device__ uint64_t wait_key(const uint64_t* p, uint32_t* status, uint64_t limit_ns) {
+  uint64_t v = ld_relaxed_u64(p);
+  if (v) return v;
+  const uint64_t t0 = gtimer();
+  while ((v = ld_relaxed_u64(p)) == 0) {
+    if (gtimer() - t0 > limit_ns) {
+      raise_status(status, DSA_DEVICE_TIMEOUT);
+      return 0;
+    }
+  }
+  return v;
+}
+
 struct RowArgs {
   const int32_t* scores;   // [L] the row's indexer scores
   const int32_t* row_len;  // [1]
@@ -143,6 +166,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   __shared__ uint32_t sh[8];                                    // b*, E(b*), |b*|, mode, C*, total, ...
   __shared__ uint32_t wt[kRowWarps];
   __shared__ float red[kRowWarps];
+  __shared__ int key_lost;                                      // a survivor slot's wait ran out
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = (int)gridDim.x, cta = (int)blockIdx.x;
@@ -150,6 +174,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   const uint32_t qrow = (uint32_t)a.D_k * 2;
 
   if (tid == 0) {
+    key_lost = 0;
     mbar_init(bar_q, 1);
     mbar_init(bar_k, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -335,16 +360,18 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   // E(b - 1) - E(b) = positions in bin b (bins >= b*).
   auto E = [&](int b) -> uint32_t { return b >= kLogBins ? 0u : HS(b); };
 
-  // ---- S: this CTA's survivors into bin order.  A cursor that runs past its
-  // bin (the cursors were not all zero) is not written; then every CTA clears
-  // the cursors and the scatter is done again.
-  auto scatter = [&](uint32_t* redo) {
+  // ---- S: this CTA's survivors into bin order: position t of bin b goes to
+  // slot E(b) + its arrival order in the bin (a cursor per bin; cursors and
+  // slots were cleared by the indexer).  No barrier follows: an attention unit
+  // reads only the slots of its own bins and waits for each to be written
+  // (a survivor's key is never 0).
+  if (mode == kRowFast) {
     auto put = [&](int32_t v, int t) {
       const uint32_t b = score_bin(v);
       if (b >= bstar) {
-        const uint32_t i = atomicAdd(a.cnt + b, 1u);   // any nonzero start shows as i >= |bin|
-        if (i < E((int)b - 1) - E((int)b)) a.surv[HS(b) + i] = surv_key(ordered_key(v), t);
-        else atomicOr(redo, 1u);
+        const uint32_t i = atomicAdd(a.cnt + b, 1u);
+        if (i < E((int)b - 1) - E((int)b)) st_relaxed_u64(a.surv + HS(b) + i, surv_key(ordered_key(v), t));
+        else raise_status(a.status, DSA_DEVICE_CAPACITY);   // cannot happen: the bins were counted
       }
     };
 #pragma unroll
@@ -353,23 +380,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
       if (t < c1) put(sreg[j], t);
     }
     scan_row<kRowThreads>(a.scores, c_reg, c1, put);
-  };
-  uint32_t* redo = a.status + kRowRedoWord;   // [0] first pass, [1] second pass
-  if (mode == kRowFast) scatter(redo);
-  if (!grid_barrier(a.bar + 0, a.status, a.wait_ns)) return bail();
-  if (mode == kRowFast && __ldcg(redo) != 0) {
-    for (int i = cta * kRowThreads + tid; i < kLogBins; i += G * kRowThreads) a.cnt[i] = 0;
-    if (!grid_barrier(a.bar + 5, a.status, a.wait_ns)) return bail();
-    scatter(redo + 1);
-    if (!grid_barrier(a.bar + 6, a.status, a.wait_ns)) return bail();
-    if (__ldcg(redo + 1) != 0) {   // cleared cursors cannot run past their bins
-      if (tid == 0) raise_status(a.status, DSA_DEVICE_CAPACITY);
-      return bail();
-    }
   }
-  // The cursors used go back to zero for the next step (all scattering is done).
-  if (mode == kRowFast)
-    for (int b = (int)bstar + cta * kRowThreads + tid; b < kLogBins; b += G * kRowThreads) a.cnt[b] = 0;
 
   if (mode == kRowExact) {
     if (cta == 0) {
@@ -409,9 +420,39 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
       const int b_top = bin_of_rank((uint32_t)r0), b_bot = bin_of_rank((uint32_t)(r1 - 1));
       const uint32_t s0 = E(b_top), s1 = E(b_bot - 1);   // slots of bins b_top .. b_bot
       const int M = (int)(s1 - s0);
+      if (M <= 64) {
+        // Few members (the usual case: a unit's ranks span a few fine bins):
+        // warp 0 ranks them by comparison.  Keys are unique, so a member's
+        // rank is s0 + the number of members with a larger key.
+        if (warp == 0) {
+          const uint64_t k0 = lane < M ? wait_key(a.surv + s0 + lane, a.status, a.wait_ns) : 0ull;
+          const uint64_t k1 = lane + 32 < M ? wait_key(a.surv + s0 + lane + 32, a.status, a.wait_ns) : 0ull;
+          if ((lane < M && k0 == 0) || (lane + 32 < M && k1 == 0)) key_lost = 1;   // a wait ran out
+          uint32_t n0 = 0, n1 = 0;
+          for (int j = 0; j < 32; ++j) {
+            const uint64_t o0 = __shfl_sync(0xffffffffu, k0, j);
+            const uint64_t o1 = __shfl_sync(0xffffffffu, k1, j);
+            const bool v0 = j < M, v1 = j + 32 < M;
+            n0 += (uint32_t)(v0 && o0 > k0) + (uint32_t)(v1 && o1 > k0);
+            n1 += (uint32_t)(v0 && o0 > k1) + (uint32_t)(v1 && o1 > k1);
+          }
+          const uint32_t ra = s0 + n0, rb = s0 + n1;
+          if (lane < M && ra >= (uint32_t)r0 && ra < (uint32_t)r1) {
+            const int t = key_pos(k0);
+            pos_s[ra - r0] = t;
+            a.idx[ra] = t;
+          }
+          if (lane + 32 < M && rb >= (uint32_t)r0 && rb < (uint32_t)r1) {
+            const int t = key_pos(k1);
+            pos_s[rb - r0] = t;
+            a.idx[rb] = t;
+          }
+        }
+      } else {
       uint32_t umax = 0, uminv = 0;
       for (int i = tid; i < M; i += kRowThreads) {
-        const uint64_t key = __ldcg(a.surv + s0 + i);
+        const uint64_t key = wait_key(a.surv + s0 + i, a.status, a.wait_ns);
+        if (key == 0) key_lost = 1;   // a wait ran out
         keys[i] = key;
         const uint32_t u = (uint32_t)(key >> 32);
         umax = max(umax, u);
@@ -498,8 +539,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
           }
         }
       }
+      }
     }
     __syncthreads();   // pos_s final; the previous unit's reads of Ks, Pb, Ss are done
+    if (key_lost) return bail();
 
     // Gather: one bulk copy per selected latent row; rows past np are zero.
     if (warp == 0) {
@@ -791,8 +834,8 @@ cudaError_t launch_decode_row(const dsa_problem& p, const Plan& pl, const int32_
   a.bar = a.status + kBarrierWord;
   a.hist = reinterpret_cast<uint32_t*>(ws + pl.off_lhist);
   a.zcount = reinterpret_cast<uint32_t*>(ws + pl.off_lkeep);
-  a.cnt = reinterpret_cast<uint32_t*>(ws + pl.off_lkeep + 256);
-  a.surv = reinterpret_cast<uint64_t*>(ws + pl.off_surv);
+  a.cnt = reinterpret_cast<uint32_t*>(ws + pl.off_lcur);
+  a.surv = reinterpret_cast<uint64_t*>(ws + pl.off_lsurv);
   const size_t u = row_units(p);
   char* pp = ws + pl.off_rpart;
   a.po = reinterpret_cast<__half*>(pp);
