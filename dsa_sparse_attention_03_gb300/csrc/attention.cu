@@ -74,26 +74,6 @@ struct AttnArgs {
   int test_no_gather; // test hook: arm the first gather's barrier but issue no copy
 };
 
-// Sixteen e4m3 codes to sixteen bf16 values (eight packed pairs), exactly:
-// e4m3 -> f16 by the hardware conversion, f16 -> f32 -> bf16 lossless for
-// these values (at most 4 significant bits, exponents within both ranges).
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 v, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int hpair = 0; hpair < 2; ++hpair) {
-      const __nv_fp8x2_storage_t b = static_cast<__nv_fp8x2_storage_t>(w[i] >> (16 * hpair));
-      const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(b, __NV_E4M3));
-      const float2 f = __half22float2(h);
-      o[2 * i + hpair] = pack_bf16(f.x, f.y);
-    }
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
 __device__ int row_request(const int32_t* row_offsets, int B, int r) {
   int lo = 0, hi = B - 1;  // largest b with row_offsets[b] <= r
   while (lo < hi) {

@@ -96,7 +96,9 @@ struct RowArgs {
   const int32_t* scores;   // [L] the row's indexer scores
   const int32_t* row_len;  // [1]
   const uint16_t* q;       // bf16 [64, D_k]
-  const uint16_t* kv;      // bf16 [L_total, D_k]
+  const uint16_t* kv;      // bf16 [L_total, D_k]; with f8, e4m3 bytes [L_total, D_k]
+  const float* kv_scale;   // f8: per-row scales, or null (= 1)
+  int f8;                  // the cache holds e4m3 codes with per-row scales (the kernel's F8)
   int32_t* idx;            // [k]
   int32_t* nsel;           // [1] or null
   uint16_t* out;           // bf16 [64, D_v]
@@ -120,8 +122,8 @@ struct RowArgs {
 
 // Shared-memory layout (bytes), for P positions per unit.
 struct RowSmem {
-  uint32_t q, kb, hs, keys, sub, ss, pb, mls, wm, pos, total;
-  __host__ __device__ RowSmem(int P, int qs, int ks) {
+  uint32_t q, kb, hs, keys, sub, ss, pb, mls, wm, pos, f8s, scs, total;
+  __host__ __device__ RowSmem(int P, int qs, int ks, bool f8) {
     q = 0;                                 // [D_k / 64][64 rows][128 B], 128-byte swizzled
     kb = q + kRowHeads * qs * 2;
     hs = kb + P * ks * 2;
@@ -132,13 +134,15 @@ struct RowSmem {
     mls = pb + kRowHeads * (P + 8) * 2;
     wm = mls + kRowHeads * 2 * 4;
     pos = wm + 2 * 256 * 4;
-    total = pos + (P + kWindowList + kCoarse) * 4;
+    f8s = (pos + (P + kWindowList + kCoarse) * 4 + 15) / 16 * 16;   // FP8 cache: [P][D_k] staged codes
+    scs = f8s + P * qs;                                            // FP8 cache: [P] row scales
+    total = f8 ? scs + P * 4 : f8s;
   }
 };
 
 // NT: output n-tiles of 8 columns per warp (four warps per head group cover
 // 32 NT >= D_v columns).  P: selected positions per attention unit (16 or 32).
-template <int NT, int P>
+template <int NT, int P, bool F8>
 __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid_constant__ RowArgs a) {
   constexpr int NTILES = P / 8;            // n-tiles of S per head group
   constexpr int KP = 4 / NTILES;           // K parts of S per n-tile (4 warps per head group)
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem =   // the swizzled query boxes want 1024-byte alignment
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const RowSmem L(P, a.qs, a.ks);
+  const RowSmem L(P, a.qs, a.ks, F8);
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem + L.q);      // [64][qs]
   uint16_t* Ks = reinterpret_cast<uint16_t*>(smem + L.kb);     // [P][ks]
   // hs: [kLogBins] counts, then E(b), one pad word after every 16 bins so that
@@ -160,6 +164,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   float* wm = reinterpret_cast<float*>(smem + L.wm);           // merge: weights / partial sums
   uint32_t* sub = reinterpret_cast<uint32_t*>(smem + L.sub);   // [kSubRange] exact-score counts
   int* pos_s = reinterpret_cast<int*>(smem + L.pos);           // [P]
+  uint8_t* F8s = smem + L.f8s;                                  // FP8 cache: [P][D_k] staged codes
+  float* scs = reinterpret_cast<float*>(smem + L.scs);          // FP8 cache: [P] row scales
   int* wlist = pos_s + P;                                       // [kWindowList] member indices
   uint32_t* coarse_s = reinterpret_cast<uint32_t*>(wlist + kWindowList);   // [kCoarse]
   __shared__ __align__(8) uint64_t bars[2];                     // queries, latent rows
@@ -544,18 +550,27 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
     __syncthreads();   // pos_s final; the previous unit's reads of Ks, Pb, Ss are done
     if (key_lost) return bail();
 
-    // Gather: one bulk copy per selected latent row; rows past np are zero.
+    // Gather: one bulk copy per selected latent row (an FP8 cache's code rows
+    // land in a staging buffer); rows past np are zero.
     if (warp == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      if (lane == 0) mbar_expect_tx(bar_k, (uint32_t)np * qrow);
+      const uint32_t rowb = F8 ? (uint32_t)a.D_k : qrow;
+      if (lane == 0) mbar_expect_tx(bar_k, (uint32_t)np * rowb);
       __syncwarp();
       for (int j = lane; j < P; j += 32) {
-        if (j < np)
-          bulk_row(smem_u32(Ks + j * a.ks), a.kv + (size_t)pos_s[j] * a.D_k, qrow, bar_k);
-        else
+        if (j < np) {
+          if (F8)
+            bulk_row(smem_u32(F8s + j * a.D_k), reinterpret_cast<const uint8_t*>(a.kv) + (size_t)pos_s[j] * a.D_k,
+                     rowb, bar_k);
+          else
+            bulk_row(smem_u32(Ks + j * a.ks), a.kv + (size_t)pos_s[j] * a.D_k, rowb, bar_k);
+        } else {
           for (int c8 = 0; c8 < a.ks / 8; ++c8) *reinterpret_cast<int4*>(Ks + j * a.ks + c8 * 8) = make_int4(0, 0, 0, 0);
+        }
       }
     }
+    if (F8 && warp == 1 && lane < P)   // the rows' scales, while the copies fly
+      scs[lane] = lane < np ? (a.kv_scale ? __ldg(a.kv_scale + pos_s[lane]) : 1.f) : 0.f;
     bool ok = true;
     if (!q_done) ok = mbar_wait(bar_q, 0, a.status, a.wait_ns);
     ok = ok && mbar_wait(bar_k, (uint32_t)it & 1u, a.status, a.wait_ns);
@@ -564,6 +579,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
       return bail();
     }
     q_done = true;
+    if (F8) {   // widen the codes to bf16 in the K buffer (exact)
+      const int chunks = a.D_k / 16;
+      for (int e = tid; e < np * chunks; e += kRowThreads) {
+        const int row = e / chunks, ch = e - row * chunks;
+        uint4 lo, hi;
+        e4m3x16_to_bf16(*reinterpret_cast<const uint4*>(F8s + row * a.D_k + ch * 16), lo, hi);
+        *reinterpret_cast<uint4*>(Ks + row * a.ks + ch * 16) = lo;
+        *reinterpret_cast<uint4*>(Ks + row * a.ks + ch * 16 + 8) = hi;
+      }
+      __syncthreads();
+    }
 
     // S = Q K^T: warp (hg, wq) takes n-tile wq % NTILES of head group hg over
     // K part wq / NTILES.
@@ -606,7 +632,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
         const int p = sub + 8 * j;
         float x = Ss[h * P + p];
         if (KP == 2) x += Ss[kRowHeads * P + h * P + p];
-        v[j] = p < np ? x * a.scale_log2 : -CUDART_INF_F;
+        v[j] = p < np ? x * a.scale_log2 * (F8 ? scs[p] : 1.f) : -CUDART_INF_F;
         m = fmaxf(m, v[j]);
       }
 #pragma unroll
@@ -615,8 +641,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
 #pragma unroll
       for (int j = 0; j < P / 8; ++j) {
         const float e = v[j] == -CUDART_INF_F ? 0.f : exp2f(v[j] - m);
-        l += e;
-        Pb[h * (P + 8) + sub + 8 * j] = __bfloat16_as_ushort(__float2bfloat16_rn(e));
+        l += e;   // an FP8 row's scale weights its values, not the softmax sum
+        const float pw = F8 ? e * scs[sub + 8 * j] : e;
+        Pb[h * (P + 8) + sub + 8 * j] = __bfloat16_as_ushort(__float2bfloat16_rn(pw));
       }
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
@@ -624,26 +651,41 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
         mls[h * 2] = m;
         mls[h * 2 + 1] = l;
       }
-      // Largest |value| among the gathered rows (bf16 bits without the sign).
+      // Largest |value| among the gathered rows (an FP8 row's codes times its
+      // scale), as float bits (monotone for values >= 0).
       uint32_t vb = 0;
       const int cpr = a.D_v / 8;   // 16-byte chunks of a value row
-      for (int e = tid; e < np * cpr; e += kRowThreads) {
-        const uint4 w4 = *reinterpret_cast<const uint4*>(Ks + (e / cpr) * a.ks + (e % cpr) * 8);
-        const uint32_t ws4[4] = {w4.x, w4.y, w4.z, w4.w};
+      if (F8) {
+        float vf = 0.f;
+        for (int e = tid; e < np * cpr; e += kRowThreads) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(Ks + (e / cpr) * a.ks + (e % cpr) * 8);
+          const uint32_t ws4[4] = {w4.x, w4.y, w4.z, w4.w};
+          uint32_t cm = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) vb = max(vb, max(ws4[i] & 0x7FFFu, (ws4[i] >> 16) & 0x7FFFu));
+          for (int i = 0; i < 4; ++i) cm = max(cm, max(ws4[i] & 0x7FFFu, (ws4[i] >> 16) & 0x7FFFu));
+          vf = fmaxf(vf, __uint_as_float(cm << 16) * scs[e / cpr]);
+        }
+        vb = __float_as_uint(vf);
+      } else {
+        for (int e = tid; e < np * cpr; e += kRowThreads) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(Ks + (e / cpr) * a.ks + (e % cpr) * 8);
+          const uint32_t ws4[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vb = max(vb, max(ws4[i] & 0x7FFFu, (ws4[i] >> 16) & 0x7FFFu));
+        }
+        vb <<= 16;   // bf16 bits -> float bits
       }
       vb = __reduce_max_sync(0xffffffffu, vb);
       if (lane == 0) wt[warp] = vb;
     }
     __syncthreads();
-    // psc: 2^(141 - E) for the largest value's bf16 exponent E (clamped), so the
+    // psc: 2^(141 - E) for the largest value's exponent E (clamped), so the
     // stored O / l (a convex combination of these rows) stays below 2^15.
     float sc;
     {
       uint32_t vb = 0;
       for (int i = 0; i < kRowWarps; ++i) vb = max(vb, wt[i]);
-      const int E = min(254, max(20, (int)(vb >> 7)));
+      const int E = min(254, max(20, (int)(vb >> 23)));
       sc = __int_as_float((127 + 141 - E) << 23);
     }
 
@@ -782,21 +824,21 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   }
 }
 
-template <int NT, int P>
+template <int NT, int P, bool F8>
 cudaError_t launch_row(const RowArgs& a, cudaStream_t st) {
-  const RowSmem L(P, a.qs, a.ks);
+  const RowSmem L(P, a.qs, a.ks, F8);
   const size_t smem = L.total + 1024;   // alignment slack
-  cudaError_t e = cudaFuncSetAttribute(decode_row_kernel<NT, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(decode_row_kernel<NT, P, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0, per_sm = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_row_kernel<NT, P>, kRowThreads,
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_row_kernel<NT, P, F8>, kRowThreads,
                                                          smem)) != cudaSuccess)
     return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  return launch_coop(decode_row_kernel<NT, P>, dim3(sms), dim3(kRowThreads), smem, st, a);
+  return launch_coop(decode_row_kernel<NT, P, F8>, dim3(sms), dim3(kRowThreads), smem, st, a);
 }
 
 }  // namespace
@@ -804,8 +846,7 @@ cudaError_t launch_row(const RowArgs& a, cudaStream_t st) {
 constexpr int kRowUnitRows = 16;   // selected positions per attention unit
 
 bool decode_row_supported(const dsa_problem& p) {
-  return p.R == 1 && p.B == 1 && p.H_q == kRowHeads && !(p.flags & DSA_FLAG_KV_FP8) &&
-         p.D_k % 64 == 0 && p.D_k <= 576 && p.D_v <= 512 && p.k <= kCapFast;
+  return p.R == 1 && p.B == 1 && p.H_q == kRowHeads && p.D_k % 64 == 0 && p.D_k <= 576 && p.D_v <= 512 && p.k <= kCapFast;
 }
 
 // Partials of the attention units: fp16 O / l [units][64][D_v], fp32 (m, l)
@@ -826,6 +867,8 @@ cudaError_t launch_decode_row(const dsa_problem& p, const Plan& pl, const int32_
   a.row_len = p.row_len;
   a.q = p.q;
   a.kv = p.kv;
+  a.f8 = (p.flags & DSA_FLAG_KV_FP8) ? 1 : 0;
+  a.kv_scale = a.f8 ? p.kv_scale : nullptr;
   a.idx = idx;
   a.nsel = nsel;
   a.out = out;
@@ -863,11 +906,19 @@ cudaError_t launch_decode_row(const dsa_problem& p, const Plan& pl, const int32_
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  if (a.f8) {
+    switch (NT) {
+      case 2: return launch_row<2, kRowUnitRows, true>(a, st);
+      case 4: return launch_row<4, kRowUnitRows, true>(a, st);
+      case 8: return launch_row<8, kRowUnitRows, true>(a, st);
+      default: return launch_row<16, kRowUnitRows, true>(a, st);
+    }
+  }
   switch (NT) {
-    case 2: return launch_row<2, kRowUnitRows>(a, st);
-    case 4: return launch_row<4, kRowUnitRows>(a, st);
-    case 8: return launch_row<8, kRowUnitRows>(a, st);
-    default: return launch_row<16, kRowUnitRows>(a, st);
+    case 2: return launch_row<2, kRowUnitRows, false>(a, st);
+    case 4: return launch_row<4, kRowUnitRows, false>(a, st);
+    case 8: return launch_row<8, kRowUnitRows, false>(a, st);
+    default: return launch_row<16, kRowUnitRows, false>(a, st);
   }
 }
 

@@ -5,6 +5,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "barrier_protocol.h"
 #include "common.cuh"
@@ -118,6 +120,26 @@ static __device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Sixteen e4m3 codes to sixteen bf16 values (eight packed pairs), exactly:
+// e4m3 -> f16 by the hardware conversion, f16 -> f32 -> bf16 lossless for
+// these values (at most 4 significant bits, exponents within both ranges).
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 v, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int hpair = 0; hpair < 2; ++hpair) {
+      const __nv_fp8x2_storage_t b = static_cast<__nv_fp8x2_storage_t>(w[i] >> (16 * hpair));
+      const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(b, __NV_E4M3));
+      const float2 f = __half22float2(h);
+      o[2 * i + hpair] = pack_bf16(f.x, f.y);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 }  // namespace dsa
