@@ -35,10 +35,12 @@ DSA_ERR_OVERFLOW_RISK = 3
 DSA_ERR_CUDA = 4
 DSA_ERR_TIMEOUT = 5
 DSA_ERR_DEVICE_INDEX = 6
+DSA_ERR_RANGE = 7
 
 DSA_DEVICE_TIMEOUT = 0x1
 DSA_DEVICE_BAD_INDEX = 0x2
 DSA_DEVICE_CAPACITY = 0x4
+DSA_DEVICE_RANGE = 0x8
 
 DSA_INDEXER_AUTO = 0
 DSA_INDEXER_DP4A = 1
@@ -53,7 +55,7 @@ EXPORTS = ("dsa_version", "dsa_last_error_string", "dsa_indexer_kind", "dsa_deco
            "dsa_workspace_size",
            "dsa_index_scores",
            "dsa_topk", "dsa_topk_static", "dsa_sparse_attn", "dsa_decode_step",
-           "dsa_read_device_status", "dsa_get_device_status",
+           "dsa_read_device_status", "dsa_get_device_status", "dsa_check_bounds",
            # include/dsa_front_end.h
            "dsa_front_end_workspace_size", "dsa_indexer_front_end",
            # include/dsa_testing.h
@@ -111,6 +113,7 @@ def _load() -> ctypes.CDLL:
         ("dsa_decode_step", [P, vp, vp, vp, vp, sz, vp]),
         ("dsa_read_device_status", [vp, vp, ctypes.POINTER(ctypes.c_int32)]),
         ("dsa_get_device_status", [vp, vp]),
+        ("dsa_check_bounds", [P, ctypes.c_int64, ctypes.c_int64, vp, sz, vp]),
         ("dsa_indexer_front_end", [P, ctypes.c_int32, vp, W, W, vp, vp, vp, vp, vp, vp, sz, vp]),
         ("dsa_test_topk_missing_arrival", [P, vp, vp, vp, vp, sz, ctypes.c_int, ctypes.c_int64, vp]),
         ("dsa_test_attn_missing_gather", [P, vp, vp, vp, vp, vp, sz, ctypes.c_int64, vp]),
@@ -313,11 +316,19 @@ def dsa_test_indexer_missing_tile(prob: Problem, scores, ws, limit_ns, stream=No
                                               ws.numel(), int(limit_ns), _stream(stream)))
 
 
+def dsa_check_bounds(prob: Problem, ws, key_row0=0, key_rows=None, stream=None) -> None:
+    """Device check of the declared bounds (include/dsa.h); read the result
+    with dsa_read_device_status."""
+    n = int(prob.c.L_total) - int(key_row0) if key_rows is None else int(key_rows)
+    _check(_lib.dsa_check_bounds(ctypes.byref(prob.c), int(key_row0), n, _ptr(ws), ws.numel(),
+                                 _stream(stream)))
+
+
 def dsa_get_device_status(ws, stream=None) -> int:
     """Synchronises the stream; returns DSA_OK, DSA_ERR_TIMEOUT or
     DSA_ERR_DEVICE_INDEX from the device status word (raises on other errors)."""
     st = _lib.dsa_get_device_status(_ptr(ws), _stream(stream))
-    if st not in (DSA_OK, DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX):
+    if st not in (DSA_OK, DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX, DSA_ERR_RANGE):
         _check(st)
     return st
 
@@ -327,7 +338,7 @@ def dsa_read_device_status(ws, stream=None) -> int:
     TIMEOUT / BAD_INDEX with the bits in ``DsaError.status``)."""
     bits = ctypes.c_int32(0)
     st = _lib.dsa_read_device_status(_ptr(ws), _stream(stream), ctypes.byref(bits))
-    if st not in (DSA_OK, DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX):
+    if st not in (DSA_OK, DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX, DSA_ERR_RANGE):
         _check(st)
     return bits.value
 

@@ -482,6 +482,35 @@ dsa_status dsa_test_indexer_missing_tile(const dsa_problem* p, int32_t* scores, 
   return DSA_OK;
 }
 
+dsa_status dsa_check_bounds(const dsa_problem* p, int64_t key_row0, int64_t key_rows, void* ws,
+                            size_t ws_bytes, void* stream) {
+  g_err.clear();
+  if (!p) return fail(DSA_ERR_INVALID_ARG, "problem is NULL");
+  if (!ws || !aligned(ws, 256) || ws_bytes < 256)
+    return fail(DSA_ERR_INVALID_ARG, "ws must be set, 256-byte aligned and at least 256 bytes");
+  if (p->R < 0 || p->H_i < 1 || p->H_i > 128 || p->D_i < 16 || p->D_i % 16)
+    return fail(DSA_ERR_INVALID_ARG, "R=%d, H_i=%d, D_i=%d out of range", p->R, p->H_i, p->D_i);
+  if (p->qk_abs_max < 0 || p->qk_abs_max > 128 || p->w_abs_max < 0)
+    return fail(DSA_ERR_INVALID_ARG, "declared bounds out of range");
+  if (key_row0 < 0 || key_rows < 0 || key_row0 + key_rows > p->L_total)
+    return fail(DSA_ERR_INVALID_ARG, "key rows [%lld, %lld) outside [0, L_total=%lld)", (long long)key_row0,
+                (long long)(key_row0 + key_rows), (long long)p->L_total);
+  if ((key_rows > 0 && !p->k_idx) || (p->R > 0 && (!p->q_idx || !p->w_idx)))
+    return fail(DSA_ERR_INVALID_ARG, "k_idx/q_idx/w_idx must be set");
+  if (!aligned(p->k_idx, 16) || !aligned(p->q_idx, 16) || !aligned(p->w_idx, 4))
+    return fail(DSA_ERR_INVALID_ARG, "k_idx/q_idx must be 16-byte aligned, w_idx 4-byte");
+  const int qk = p->qk_abs_max > 0 ? p->qk_abs_max : 128;
+  const int wm = p->w_abs_max > 0 ? p->w_abs_max : 4;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear status");
+  const size_t D = size_t(p->D_i), R = size_t(p->R), H = size_t(p->H_i);
+  e = launch_check_bounds(p->k_idx ? p->k_idx + size_t(key_row0) * D : nullptr, size_t(key_rows) * D, p->q_idx,
+                          R * H * D, p->w_idx, R * H, qk, wm, static_cast<uint32_t*>(ws), st);
+  if (e != cudaSuccess) return cuda_fail(e, "bound check");
+  return DSA_OK;
+}
+
 dsa_status dsa_get_device_status(void* ws, void* stream) {
   int32_t bits = 0;
   return dsa_read_device_status(ws, stream, &bits);
@@ -499,6 +528,7 @@ dsa_status dsa_read_device_status(void* ws, void* stream, int32_t* bits) {
   *bits = static_cast<int32_t>(v);
   if (v & DSA_DEVICE_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "a bounded device wait ran out");
   if (v & DSA_DEVICE_BAD_INDEX) return fail(DSA_ERR_DEVICE_INDEX, "an out-of-range index was skipped");
+  if (v & DSA_DEVICE_RANGE) return fail(DSA_ERR_RANGE, "an operand exceeds its declared bound");
   return DSA_OK;
 }
 

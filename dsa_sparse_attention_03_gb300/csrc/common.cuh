@@ -246,4 +246,10 @@ struct FrontArgs {
 };
 cudaError_t launch_front_end(FrontArgs a, cudaStream_t st);
 
+// Declared-bound check (check.cu): int8 bytes of k and q (16-byte multiples)
+// against qk (>= 128: not checked), head weights against wmax.
+cudaError_t launch_check_bounds(const int8_t* k, size_t k_bytes, const int8_t* q, size_t q_bytes,
+                                const int32_t* w, size_t nw, int qk, int wmax, uint32_t* status,
+                                cudaStream_t st);
+
 }  // namespace dsa

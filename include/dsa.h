@@ -86,13 +86,15 @@ typedef enum dsa_status {
   DSA_ERR_OVERFLOW_RISK = 3,   /* declared value ranges could overflow int32   */
   DSA_ERR_CUDA = 4,            /* a CUDA runtime call failed                    */
   DSA_ERR_TIMEOUT = 5,         /* device: a bounded wait ran out (status bit)   */
-  DSA_ERR_DEVICE_INDEX = 6     /* device: out-of-range index skipped (status)   */
+  DSA_ERR_DEVICE_INDEX = 6,    /* device: out-of-range index skipped (status)   */
+  DSA_ERR_RANGE = 7            /* device: an operand outside its declared bound */
 } dsa_status;
 
 /* Device status bits, as returned by dsa_read_device_status(). */
 #define DSA_DEVICE_TIMEOUT      0x1
 #define DSA_DEVICE_BAD_INDEX    0x2
 #define DSA_DEVICE_CAPACITY     0x4
+#define DSA_DEVICE_RANGE        0x8   /* dsa_check_bounds: an operand exceeds its declared bound */
 
 /* dsa_problem.flags */
 #define DSA_INDEXER_AUTO   0   /* tensor-core indexer where supported, else dp4a */
@@ -248,16 +250,34 @@ DSA_API dsa_status dsa_decode_step(const dsa_problem* p, int32_t* idx, int32_t* 
                            uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Checks on the device that the operands respect the problem's declared
+ * bounds: every |q_idx| and every |k_idx| of cached rows [key_row0, key_row0 +
+ * key_rows) at most qk_abs_max (0 = no bound to check: int8 always fits), and
+ * every |w_idx| at most w_abs_max (0 = 4).  The bounds are the caller's
+ * promise (the indexer picks its exact operand format from them, and the
+ * int32 overflow check relies on them); a step never re-reads the whole cache
+ * to verify it, so a caller checks each key row once, when it is written to
+ * the cache, and the per-step operands as it sees fit.  A violation sets
+ * DSA_DEVICE_RANGE in the workspace's status word (cleared first by this
+ * call); dsa_read_device_status then returns DSA_ERR_RANGE.  Reads p->R,
+ * H_i, D_i, L_total, q_idx, w_idx (both may be NULL when R = 0), k_idx and the
+ * bounds; ws needs 256 bytes.  One kernel, no host synchronisation.
+ */
+DSA_API dsa_status dsa_check_bounds(const dsa_problem* p, int64_t key_row0, int64_t key_rows, void* ws,
+                                    size_t ws_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then reads the workspace's device status word into
- * *bits (DSA_DEVICE_* bits; 0 = clean).  Returns DSA_ERR_TIMEOUT or
- * DSA_ERR_DEVICE_INDEX when the matching bit is set, else DSA_OK.
+ * *bits (DSA_DEVICE_* bits; 0 = clean).  Returns DSA_ERR_TIMEOUT,
+ * DSA_ERR_DEVICE_INDEX or DSA_ERR_RANGE when the matching bit is set, else
+ * DSA_OK.
  */
 DSA_API dsa_status dsa_read_device_status(void* ws, void* stream, int32_t* bits);
 
 /*
  * The same check without the bits: synchronises `stream` and returns
- * DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX or DSA_OK from the workspace's device
- * status word (a CUDA failure returns DSA_ERR_CUDA).
+ * DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX, DSA_ERR_RANGE or DSA_OK from the
+ * workspace's device status word (a CUDA failure returns DSA_ERR_CUDA).
  */
 DSA_API dsa_status dsa_get_device_status(void* ws, void* stream);
 

@@ -172,3 +172,18 @@ def test_front_end_validation_and_workspace(dsa):
     assert call(prob=_prob(dsa, R=2, qk_abs_max=200)) == dsa.DSA_ERR_INVALID_ARG
     assert call(d=65536) == dsa.DSA_ERR_UNSUPPORTED
     assert call(prob=_prob(dsa, R=0)) == dsa.DSA_OK    # nothing to do, nothing enqueued
+
+
+def test_check_bounds_validation(dsa):
+    lib = dsa.lib()
+    fake = 1 << 20   # host validation only: nothing is launched when it fails
+    p = _prob(dsa, R=1, qk_abs_max=10, w_abs_max=4, L_total=1000, L_max=1000)
+    for f in ("q_idx", "w_idx", "k_idx"):
+        setattr(p.c, f, fake)
+    call = lambda r0, n, ws=fake, nb=256: lib.dsa_check_bounds(ctypes.byref(p.c), r0, n, ctypes.c_void_p(ws), nb, None)
+    assert call(0, 1001) == dsa.DSA_ERR_INVALID_ARG and b"L_total" in lib.dsa_last_error_string()
+    assert call(-1, 10) == dsa.DSA_ERR_INVALID_ARG
+    assert call(0, 10, ws=fake + 16) == dsa.DSA_ERR_INVALID_ARG
+    assert call(0, 10, nb=255) == dsa.DSA_ERR_INVALID_ARG
+    p.c.k_idx = fake + 8
+    assert call(0, 10) == dsa.DSA_ERR_INVALID_ARG and b"aligned" in lib.dsa_last_error_string()
