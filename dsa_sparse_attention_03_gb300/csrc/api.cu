@@ -148,6 +148,15 @@ dsa_status run_indexer(const dsa_problem& p, const Plan& pl, int32_t* scores, ch
   if (p.R == 0) return DSA_OK;
   const int ix = p.flags & DSA_INDEXER_MASK;
   const bool tc = ix == DSA_INDEXER_TC || (ix == DSA_INDEXER_AUTO && indexer_tc_supported(p));
+  // The indexer merges each row's key range into the row state as its CTAs
+  // finish row groups, so the range must be zero before any CTA starts: a
+  // memset here, except for the single-row step, whose indexer clears the
+  // range itself (its row state is unused; its histogram has its own
+  // clearing counter).
+  if (!pl.fused_row) {
+    cudaError_t z = cudaMemsetAsync(ws, 0, pl.zero_end, st);
+    if (z != cudaSuccess) return cuda_fail(z, "clear workspace");
+  }
   cudaError_t e = tc ? launch_indexer_tc(p, pl, scores, ws, st)
                      : launch_indexer_dp4a(p, pl, scores, ws, st);
   if (e != cudaSuccess) return cuda_fail(e, tc ? "indexer (tensor core)" : "indexer (dp4a)");
@@ -476,6 +485,10 @@ dsa_status dsa_test_indexer_missing_tile(const dsa_problem* p, int32_t* scores, 
   if (ix == DSA_INDEXER_DP4A || !indexer_tc_tmem_operand(*p))
     return fail(DSA_ERR_UNSUPPORTED, "the hook needs the tensor-memory-operand indexer");
   h.indexer_no_load = 1;
+  if (!pl.fused_row) {
+    cudaError_t z = cudaMemsetAsync(ws, 0, pl.zero_end, static_cast<cudaStream_t>(stream));
+    if (z != cudaSuccess) return cuda_fail(z, "clear workspace");
+  }
   cudaError_t e = launch_indexer_tc(*p, pl, scores, static_cast<char*>(ws),
                                     static_cast<cudaStream_t>(stream), &h);
   if (e != cudaSuccess) return cuda_fail(e, "indexer (tensor core)");

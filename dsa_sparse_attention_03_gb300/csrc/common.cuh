@@ -187,8 +187,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 EncodeTiledFn encode_tiled_fn();
 
 // Launchers (one per translation unit).  Each returns the launch error.
-// Both indexers also clear the workspace's status word, top-k state and
-// histograms ([0, Plan::zero_end)), so a decode step needs no separate memset.
+// For the single-row step (Plan::fused_row) both indexers also clear the
+// workspace's range [0, Plan::zero_end) (status word, histograms, cursors), so
+// that step needs no separate memset; other callers clear it before the launch.
 cudaError_t launch_indexer_dp4a(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,
                                 cudaStream_t st);
 cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* scores, char* ws,

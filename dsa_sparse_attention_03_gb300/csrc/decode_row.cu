@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
     if (cta == 0) {
       exact_row_keys<kRowThreads>(a.scores, len, a.k, (uint32_t)a.k - n_above,
                                   [&](uint32_t u) { return score_bin((int32_t)(u ^ 0x80000000u)) == bstar; },
-                                  keys);
+                                  keys, a.status);
       for (int j = tid; j < a.k; j += kRowThreads) a.idx[j] = key_pos(keys[j]);
     }
     if (!grid_barrier(a.bar + 1, a.status, a.wait_ns)) return bail();

@@ -178,7 +178,7 @@ cudaError_t launch(const dsa_problem& p, const Plan& pl, int32_t* scores, char* 
   a.scores = scores; a.L_max = p.L_max; a.B = p.B; a.H_i = p.H_i;
   a.relu = (p.flags & DSA_FLAG_NO_RELU) ? 0 : 1;
   a.zero = reinterpret_cast<uint4*>(ws);
-  a.n_zero = (int)(pl.zero_end / 16);
+  a.n_zero = pl.fused_row ? (int)(pl.zero_end / 16) : 0;   // else cleared before the launch
   a.rows = reinterpret_cast<RowState*>(ws + pl.off_state);
   const int64_t bound = p.L_total / TILE + p.B;
   a.total_tiles_bound = (int)bound;

@@ -29,7 +29,8 @@
 // pairs); key tiles arrive through the tensor map (TMA, 128-byte swizzle) in an
 // S-stage ring.  Warp roles:
 //   warp 0        TMA producer; allocates and frees tensor memory
-//   warps 1-4     MMA issuers, one per SM sub-partition, tile i to issuer i % 4,
+//   warps 1-4     MMA issuers, one per SM sub-partition, tile i to issuer i % NI
+//                 (NI = 4, or 2 with two accumulators),
 //                 each committing its tile to the accumulator's barrier
 //                 (epilogue) and to the A buffer's barrier (converters)
 //   warps 5-12    converters, two per sub-partition on alternate tiles: each
@@ -74,7 +75,7 @@ constexpr int kModeExact = 0, kModeBiased = 1, kModeFp8 = 2;
 // over four threads, one per sub-partition, each taking every fourth tile.
 // Conversion is latency-bound within a warp, so two converter warps share
 // each sub-partition, taking alternate tiles:
-//   warp 0       TMA producer              warps 1-4    MMA issuers (tile % 4)
+//   warp 0       TMA producer              warps 1-4    MMA issuers (tile % NI)
 //   warps 5-12   converters, lane quarter = warp % 4, tile parity = (warp - 5) / 4
 //   warps 13-20  epilogue, two groups of four (tile % 2)
 constexpr int kTmMmaWarp0 = 1;
@@ -971,14 +972,18 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
     }
   } else if (warp < kTmConvWarp0) {
     // ------------------------------------------------------------ MMA issuers
-    // Issuer j takes tiles i = j (mod 4): with NA = 4 it always fills A buffer j
-    // and, with NACC = 4, accumulator j.  A tcgen05.commit covers the MMAs of
+    // NI = min(NACC, 4) issuers; issuer j takes tiles i = j (mod NI), so it
+    // always fills accumulator j (mod NACC) and waits at most one phase ahead
+    // on its barriers: with two accumulators and four issuers, an issuer's
+    // consecutive tiles on one accumulator would be two phases apart, and a
+    // parity wait cannot tell those apart.  A tcgen05.commit covers the MMAs of
     // its own thread, so each tile's two commits come from its issuer.
     const int j = warp - kTmMmaWarp0;
-    if (lane == 0) {
+    const int NI = NACC < kTmMmaWarps ? NACC : kTmMmaWarps;
+    if (lane == 0 && j < NI) {
       int last = -1;
       const uint32_t b_base = cvta_smem(Bop) + (uint32_t)(j & 1) * a.b_stride;   // B of this tile parity
-      for (int i = j; i < n_local; i += kTmMmaWarps) {
+      for (int i = j; i < n_local; i += NI) {
         const int acc = i % NACC, ab = i % NA;
         tile_step(a, prefix, gtile(i), ti);
         const uint32_t idesc = idesc_f16(kTile, ti.nrows * a.H_i);
@@ -1025,9 +1030,9 @@ __global__ void __launch_bounds__(kTmThreads, 1) indexer_tc_tm_kernel(const __gr
       const bool new_group = tile_step(a, prefix, gtile(i), ti);
       if (i >= NA && !wait_bar_warp(bar_afree + 8 * ab, ((i / NA) - 1) & 1, abort_flag, a.status, a.wait_ns)) break;
       if (new_group && !(early_b && i == par)) {   // (B does not depend on the key tile)
-        // This parity's B is read by the MMAs of tiles i-2, i-4, ...; issuers
-        // (i-2) % 4 and i % 4 complete theirs in order, and tile i-4 (buffer
-        // ab) was waited for above, so tile i-2 is the one left.
+        // This parity's B is read by the MMAs of tiles i-2, i-4, ...: tile i-4
+        // (buffer ab) was waited for above, tile i-2 is waited for here, and
+        // each earlier one was waited for at an earlier tile of this parity.
         if (i >= 2 &&
             !wait_bar_warp(bar_afree + 8 * ((i - 2) % NA), ((i - 2) / NA) & 1, abort_flag, a.status, a.wait_ns))
           break;
@@ -1288,8 +1293,12 @@ cudaError_t launch_indexer_tc(const dsa_problem& p, const Plan& pl, int32_t* sco
   a.test_no_load = hooks->indexer_no_load;
   a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
   a.rows = reinterpret_cast<RowState*>(ws + pl.off_state);
+  // The single-row step clears the workspace range here (its histogram is
+  // protected by the clearing counter, and its row state is not used); every
+  // other caller clears it before the launch, so that no CTA's clearing can
+  // meet another CTA's row-state merges.
   a.zero = reinterpret_cast<uint4*>(ws);
-  a.n_zero = (int)(pl.zero_end / 16);
+  a.n_zero = pl.fused_row ? (int)(pl.zero_end / 16) : 0;
   a.q_idx = p.q_idx; a.w_idx = p.w_idx; a.k_idx = p.k_idx;
   a.offsets = p.offsets; a.row_offsets = p.row_offsets; a.row_len = p.row_len;
   a.scores = scores; a.L_max = p.L_max;

@@ -134,9 +134,12 @@ __device__ void sort_desc(uint64_t* keys, int n0) {
 // above T, then the first ties of T in index order) are sorted into keys[0, k)
 // by (score desc, position asc).  keys holds at least the next power of two
 // >= k entries.  All NT threads of the CTA take part; ends with a barrier.
+// The count of keys above the candidates comes from the caller's histogram; a
+// key beyond it (a histogram that does not match the scores) is not written
+// and raises DSA_DEVICE_CAPACITY in *status.
 template <int NT, class InCand>
 __device__ void exact_row_keys(const int32_t* s, int len, int k, uint32_t k_rem, InCand in_cand,
-                               uint64_t* keys) {
+                               uint64_t* keys, uint32_t* status) {
   __shared__ uint32_t h[1 << kRadixBits];
   __shared__ uint32_t tmp[NT / 32];
   __shared__ uint32_t res[2];
@@ -201,7 +204,11 @@ __device__ void exact_row_keys(const int32_t* s, int len, int k, uint32_t k_rem,
     for (int j = 0; j < 8; ++j) {
       const int t = base0 + j * NT + threadIdx.x;
       const uint32_t u = ordered_key(vv[j]);
-      if (t < len && u > T) keys[atomicAdd(&n_list, 1u)] = surv_key(u, t);
+      if (t < len && u > T) {
+        const uint32_t slot = atomicAdd(&n_list, 1u);
+        if (slot < n_gt) keys[slot] = surv_key(u, t);
+        else raise_status(status, DSA_DEVICE_CAPACITY);
+      }
       tm[j] = __ballot_sync(0xffffffffu, t < len && u == T);
       if (lane == 0) tie8[j * (NT / 32) + w] = __popc(tm[j]);
     }

@@ -77,9 +77,10 @@ struct Bins {
     umin = lo;
     shift = (uint32_t)max(0, bl - kBucketBits);
   }
-  // (The clamp only guards memory: every key of the row lies in [umin, umax].)
+  // (The clamps only guard memory and keep the bins monotone: every key of the
+  // row lies in [umin, umax].)
   __device__ __forceinline__ uint32_t operator()(uint32_t u) const {
-    return min((u - umin) >> shift, (uint32_t)(kBuckets - 1));
+    return u < umin ? 0u : min((u - umin) >> shift, (uint32_t)(kBuckets - 1));
   }
 };
 
@@ -94,7 +95,7 @@ __device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys
   const uint32_t bstar = st->bstar;
   const Bins bin(st);
   exact_row_keys<kThreads>(s, len, a.k, (uint32_t)a.k - st->n_above,
-                           [&](uint32_t u) { return bin(u) == bstar; }, keys);
+                           [&](uint32_t u) { return bin(u) == bstar; }, keys, a.status);
   int32_t* idx = a.idx + (size_t)r * a.k;
   for (int j = threadIdx.x; j < a.k; j += kThreads) idx[j] = key_pos(keys[j]);
 }

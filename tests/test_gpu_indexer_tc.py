@@ -162,3 +162,15 @@ def test_tc_fp8_with_128_column_accumulators():
     qk = value_bound(x)
     assert qk <= 11
     _check_one(x, None, True, True, qk)
+
+
+@pytest.mark.parametrize("H_i,R,L", [(128, 1, 307200), (32, 8, 150000)])
+def test_tc_two_accumulators_many_tiles_per_cta(H_i, R, L):
+    # 128 accumulator columns per tile (128 heads of one row, or 4 rows x 32
+    # heads) leave room for two accumulators: each CTA here takes dozens of
+    # tiles, so the MMA issuers cycle through both many times.
+    x = gen.make_inputs("acc2", seed=H_i + R, lengths=[L], rows_per_request=[R],
+                        row_len=[L - R + 1 + i for i in range(R)], H_i=H_i, D_i=128, H_q=16,
+                        D_k=64, D_v=64, k=256, softmax_scale=0.125)
+    for qk in (value_bound(x), 0):   # e4m3 operands, then exact fp16
+        _check_one(x, None, True, False, qk)
