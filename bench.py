@@ -313,7 +313,7 @@ def bench_ours(args):
                     "algorithmic_bytes_per_launch": row_bytes,
                     "avg_launch_us": round(row_us, 3),
                     "duration_source": "step us/layer minus the indexer's back-to-back us/launch (CUDA events)",
-                    "note": "latency-bound: a chain of dependent L2 round trips and two grid barriers"}
+                    "note": "latency-bound: a chain of dependent L2 round trips and a grid barrier"}
     in_bytes = n_layers * L_LONG * (x0.D_i + kvb)
     step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
 
