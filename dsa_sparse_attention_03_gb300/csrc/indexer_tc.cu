@@ -21,7 +21,8 @@
 // The epilogue turns max(d + c_h, 1.5 * 2^23) into integer bits (the magic
 // number add folds the ReLU and the bias removal into one fmax), applies the
 // weights with wrapping uint32 multiply-adds, and merges the row's key range
-// for the top-k.
+// for the top-k -- or, for the single-row step, counts every score into the
+// row's log-spaced histogram (shared memory, then one of eight global copies).
 //
 // indexer_tc_tm_kernel (D_i = 128, up to 128 accumulator columns per tile): the
 // A operand lives in tensor memory.  One persistent CTA per SM walks a

@@ -38,6 +38,39 @@ __device__ __forceinline__ void scan_row(const int32_t* s, int begin, int end, F
   }
 }
 
+// The same visit with 16-byte loads (U = 8 in flight per thread): a scalar
+// head up to the first 16-byte boundary, aligned chunks of four, a scalar
+// tail.  f(value, t) sees every t in [begin, end) once, in no fixed order.
+template <int NT, typename F>
+__device__ __forceinline__ void scan_row_v(const int32_t* s, int begin, int end, F f) {
+  constexpr int U = 8;
+  const int mis = (int)((reinterpret_cast<uintptr_t>(s + begin) >> 2) & 3);
+  const int a0 = min(end, begin + ((4 - mis) & 3));
+  for (int t = begin + (int)threadIdx.x; t < a0; t += NT) f(s[t], t);
+  const int nch = (end - a0) >> 2;
+  const int4* c4 = reinterpret_cast<const int4*>(s + a0);
+  for (int cb = (int)threadIdx.x; cb < nch; cb += U * NT) {
+    int4 v[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int c = cb + j * NT;
+      v[j] = c < nch ? c4[c] : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int c = cb + j * NT;
+      if (c < nch) {
+        const int t = a0 + 4 * c;
+        f(v[j].x, t);
+        f(v[j].y, t + 1);
+        f(v[j].z, t + 2);
+        f(v[j].w, t + 3);
+      }
+    }
+  }
+  for (int t = a0 + 4 * nch + (int)threadIdx.x; t < end; t += NT) f(s[t], t);
+}
+
 __device__ __forceinline__ uint64_t surv_key(uint32_t u, int t) {
   return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - (uint32_t)t);
 }
@@ -113,7 +146,7 @@ __device__ void sort_desc(uint64_t* keys, int n0) {
   for (int size = 2; size <= n; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int i = threadIdx.x; i < (n >> 1); i += NT) {
-        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+        const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1)), hi = lo + stride;   // stride: a power of two
         const uint64_t x = keys[lo], y = keys[hi];
         const bool desc = (lo & size) == 0;
         if (desc ? (x < y) : (x > y)) {
@@ -130,26 +163,32 @@ __device__ void sort_desc(uint64_t* keys, int n0) {
 // ordered key u satisfies in_cand(u) (one histogram bin); every position with
 // a key above the candidates' is taken, plus the k_rem largest candidates, the
 // lowest positions first among equal keys.  Radix passes over the candidates'
-// key range find the exact k_rem-th largest candidate key T; the winners (keys
-// above T, then the first ties of T in index order) are sorted into keys[0, k)
-// by (score desc, position asc).  keys holds at least the next power of two
-// >= k entries.  All NT threads of the CTA take part; ends with a barrier.
-// The count of keys above the candidates comes from the caller's histogram; a
-// key beyond it (a histogram that does not match the scores) is not written
-// and raises DSA_DEVICE_CAPACITY in *status.
+// key range find the exact k_rem-th largest candidate key T.  The ties at T
+// are counted per block of positions; the block where the count reaches k_rem
+// is numbered in position order to find the last tie taken; one more pass
+// writes the winners (keys above T, ties up to that position), which are
+// sorted into keys[0, k) by (score desc, position asc).  keys holds at least
+// the next power of two >= k entries.  The count of keys above the candidates
+// comes from the caller's histogram; a key beyond k (a histogram that does not
+// match the scores) is not written and raises DSA_DEVICE_CAPACITY in *status.
+// All NT threads of the CTA take part; ends with a barrier.
+constexpr int kTieBlocks = 32;
 template <int NT, class InCand>
-__device__ void exact_row_keys(const int32_t* s, int len, int k, uint32_t k_rem, InCand in_cand,
-                               uint64_t* keys, uint32_t* status) {
+__device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, uint32_t k_rem, InCand in_cand,
+                                            uint64_t* keys, uint32_t* status) {
   __shared__ uint32_t h[1 << kRadixBits];
   __shared__ uint32_t tmp[NT / 32];
   __shared__ uint32_t res[2];
   __shared__ uint32_t n_list;
   __shared__ uint32_t tie8[8 * (NT / 32)];
-
+  __shared__ uint32_t wcnt[NT / 32][kTieBlocks];
+  __shared__ uint32_t cut[2];
+  __shared__ int pstar;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 
   // Key range of the candidates.
   uint32_t umax = 0, uminv = 0;
-  scan_row<NT>(s, 0, len, [&](int32_t v, int) {
+  scan_row_v<NT>(s, 0, len, [&](int32_t v, int) {
     const uint32_t u = ordered_key(v);
     if (in_cand(u)) {
       umax = max(umax, u);
@@ -169,7 +208,7 @@ __device__ void exact_row_keys(const int32_t* s, int len, int k, uint32_t k_rem,
     const int nb = 1 << bits;
     for (int i = threadIdx.x; i < nb; i += NT) h[i] = 0;
     __syncthreads();
-    scan_row<NT>(s, 0, len, [&](int32_t v, int) {
+    scan_row_v<NT>(s, 0, len, [&](int32_t v, int) {
       const uint32_t u = ordered_key(v);
       if (in_cand(u) && (static_cast<uint64_t>(u) >> shift) == prefix)
         atomicAdd(&h[(u >> ns) & (uint32_t)(nb - 1)], 1u);
@@ -183,60 +222,108 @@ __device__ void exact_row_keys(const int32_t* s, int len, int k, uint32_t k_rem,
   }
   const uint32_t T = prefix;
 
-  // Winners: every key > T (unordered), then the k_rem lowest-index ties in
-  // index order.  n_gt = k - k_rem keys are strictly greater than T.
-  if (threadIdx.x == 0) n_list = 0;
-  __syncthreads();
-  const uint32_t n_gt = (uint32_t)k - k_rem;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  uint32_t ties_done = 0;
-  for (int base0 = 0; base0 < len; base0 += 8 * NT) {
-    int32_t vv[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int t = base0 + j * NT + threadIdx.x;
-      vv[j] = t < len ? s[t] : 0;
-    }
-    // Ties are numbered in index order: position t = base0 + j * NT + thread,
-    // so (j, warp, lane) order.  All eight ballots first, one barrier.
-    uint32_t tm[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int t = base0 + j * NT + threadIdx.x;
-      const uint32_t u = ordered_key(vv[j]);
-      if (t < len && u > T) {
-        const uint32_t slot = atomicAdd(&n_list, 1u);
-        if (slot < n_gt) keys[slot] = surv_key(u, t);
-        else raise_status(status, DSA_DEVICE_CAPACITY);
-      }
-      tm[j] = __ballot_sync(0xffffffffu, t < len && u == T);
-      if (lane == 0) tie8[j * (NT / 32) + w] = __popc(tm[j]);
-    }
-    __syncthreads();
-    uint32_t before = ties_done;   // ties ahead of (j, warp w) in index order
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t tot = 0, mine = 0;
-      for (int i = 0; i < NT / 32; ++i) {
-        const uint32_t c = tie8[j * (NT / 32) + i];
-        if (i < w) mine += c;
-        tot += c;
-      }
-      const int t = base0 + j * NT + threadIdx.x;
-      if (tm[j] & (1u << lane)) {
-        const uint32_t pos = before + mine + __popc(tm[j] & lanemask_lt());
-        if (pos < k_rem) keys[n_gt + pos] = surv_key(ordered_key(vv[j]), t);
-      }
-      before += tot;
-    }
-    ties_done = before;
-    __syncthreads();   // tie8 is rewritten next
+  // Ties at T per block of 2^lb positions (at most kTieBlocks blocks); each
+  // thread visits its positions in increasing order and adds its count when
+  // it moves to another block (into its warp's own counters).
+  int lb = 12;
+  while ((int64_t(1) << lb) * kTieBlocks < (int64_t)len) ++lb;
+  const int nblk = (int)((len + (int64_t(1) << lb) - 1) >> lb);
+  for (int i = threadIdx.x; i < (NT / 32) * kTieBlocks; i += NT) (&wcnt[0][0])[i] = 0;
+  if (threadIdx.x == 0) {
+    n_list = 0;
+    pstar = -1;
   }
+  __syncthreads();
+  if (k_rem > 0) {
+    int cb = -1;
+    uint32_t cnt = 0;
+    scan_row_v<NT>(s, 0, len, [&](int32_t v, int t) {
+      if (ordered_key(v) == T) {
+        const int b = t >> lb;
+        if (b != cb) {
+          if (cnt) atomicAdd(&wcnt[w][cb], cnt);
+          cb = b;
+          cnt = 0;
+        }
+        ++cnt;
+      }
+    });
+    if (cnt) atomicAdd(&wcnt[w][cb], cnt);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {   // the block holding the k_rem-th tie, and the ties before it
+    uint32_t run = 0;
+    int cbk = nblk;
+    for (int b = 0; b < nblk && k_rem > 0; ++b) {
+      uint32_t tb = 0;
+      for (int ww = 0; ww < NT / 32; ++ww) tb += wcnt[ww][b];
+      if (run + tb >= k_rem) {
+        cbk = b;
+        break;
+      }
+      run += tb;
+    }
+    cut[0] = (uint32_t)cbk;
+    cut[1] = run;
+  }
+  __syncthreads();
+  const int cbk = (int)cut[0];
+  if (cbk < nblk) {
+    // Number the ties of that block in position order: position t = base0 +
+    // j * NT + thread, so (j, warp, lane) order; the need-th one is the last
+    // tie taken.
+    const int lo = cbk << lb, hi = (int)min((int64_t)len, (int64_t)(cbk + 1) << lb);
+    const uint32_t need = k_rem - cut[1];
+    uint32_t before = 0;
+    for (int base0 = lo; base0 < hi; base0 += 8 * NT) {
+      uint32_t tm[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int t = base0 + j * NT + threadIdx.x;
+        const bool tie = t < hi && ordered_key(s[t]) == T;
+        tm[j] = __ballot_sync(0xffffffffu, tie);
+        if (lane == 0) tie8[j * (NT / 32) + w] = __popc(tm[j]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t tot = 0, mine = 0;
+        for (int i = 0; i < NT / 32; ++i) {
+          const uint32_t c = tie8[j * (NT / 32) + i];
+          if (i < w) mine += c;
+          tot += c;
+        }
+        if (tm[j] & (1u << lane)) {
+          const uint32_t pos = before + mine + __popc(tm[j] & lanemask_lt());
+          if (pos + 1 == need) pstar = base0 + j * NT + threadIdx.x;
+        }
+        before += tot;
+      }
+      __syncthreads();   // tie8 is rewritten next
+    }
+  }
+  __syncthreads();
+  const int ps = pstar;
 
+  // Winners: every key above T, and the ties at or before position ps; slots
+  // are reserved once per group of lanes that found one.
+  const uint32_t lt = lanemask_lt();
+  scan_row_v<NT>(s, 0, len, [&](int32_t v, int t) {
+    const uint32_t u = ordered_key(v);
+    if (u > T || (u == T && t <= ps)) {
+      const uint32_t m = __activemask();
+      const int leader = __ffs(m) - 1;
+      uint32_t base = 0;
+      if (lane == leader) base = atomicAdd(&n_list, (uint32_t)__popc(m));
+      base = __shfl_sync(m, base, leader);
+      const uint32_t slot = base + __popc(m & lt);
+      if (slot < (uint32_t)k) keys[slot] = surv_key(u, t);
+      else raise_status(status, DSA_DEVICE_CAPACITY);
+    }
+  });
   __syncthreads();
   sort_desc<NT>(keys, k);
 }
-
 
 }  // namespace sel
 }  // namespace dsa
