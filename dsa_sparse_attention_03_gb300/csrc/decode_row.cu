@@ -110,7 +110,7 @@ struct RowArgs {
   uint32_t* zcount;        // the indexer's clearing counter, reset here for the next step
   uint32_t* cnt;           // [kLogBins] bin cursors of S, left at zero for the next step
   uint64_t* surv;          // [kCapFast] survivor keys in bin order
-  __half* po;              // [units][64][D_v] the unit's O / l of each head, times psc[u]
+  __half* po;              // [units][64][32 NT] the unit's O / l of each head, times psc[u]
   float* pml;              // [units][64][2] the unit's max m and sum l of each head
   float* psc;              // [units] a power of two that puts the unit's values near 2^14
   int L1;                  // the request's length (L_total)
@@ -141,9 +141,19 @@ struct RowSmem {
 };
 
 // NT: output n-tiles of 8 columns per warp (four warps per head group cover
-// 32 NT >= D_v columns).  P: selected positions per attention unit (16 or 32).
+// 32 NT >= D_v columns; NT >= 4).  P: selected positions per attention unit
+// (16 or 32).
+//
+// A unit's partial holds 32 NT columns per head (the columns from D_v on are
+// padding), in chunks of 16 bytes: chunk c = (wq NG + ng) 4 + cq of a head
+// holds columns wq 8 NT + (4 ng + t) 8 + 2 cq + {0, 1}, t = 0..3 (NG = NT / 4),
+// the four n-tiles of one accumulator thread.  Each thread then stores 16
+// bytes at a time and a warp's store fills whole 32-byte sectors.
 template <int NT, int P, bool F8>
 __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid_constant__ RowArgs a) {
+  static_assert(NT >= 4 && NT % 4 == 0, "four n-tiles per partial chunk");
+  constexpr int NG = NT / 4;
+  constexpr int Dvp = 32 * NT;             // partial columns per head
   constexpr int NTILES = P / 8;            // n-tiles of S per head group
   constexpr int KP = 4 / NTILES;           // K parts of S per n-tile (4 warps per head group)
   static_assert(NTILES * KP == 4, "four warps per head group");
@@ -712,18 +722,22 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
       }
     }
     // The unit's partial: O / l of each head as fp16 (times sc), and (m, l).
-    __half* po_u = a.po + (size_t)u * kRowHeads * a.D_v;
+    __half* po_u = a.po + (size_t)u * kRowHeads * Dvp;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int h = hg * 16 + g + 8 * j;
       const float lh = mls[h * 2 + 1];
       const float inv = lh > 0.f ? sc / lh : 0.f;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int col = wq * 8 * NT + nt * 8 + 2 * cq;
-        if (col < a.D_v)
-          __stcg(reinterpret_cast<__half2*>(po_u + (size_t)h * a.D_v + col),
-                 __floats2half2_rn(acc[nt][2 * j] * inv, acc[nt][2 * j + 1] * inv));
+      for (int ng = 0; ng < NG; ++ng) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const __half2 hv = __floats2half2_rn(acc[4 * ng + t][2 * j] * inv, acc[4 * ng + t][2 * j + 1] * inv);
+          w4[t] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        __stcg(reinterpret_cast<uint4*>(po_u + (size_t)h * Dvp + ((wq * NG + ng) * 4 + cq) * 8),
+               make_uint4(w4[0], w4[1], w4[2], w4[3]));
       }
     }
     if (tid < 2 * kRowHeads) __stcg(a.pml + (size_t)u * 2 * kRowHeads + tid, mls[tid]);
@@ -732,11 +746,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   if (!q_done && tid == 0) mbar_wait(bar_q, 0, nullptr, a.wait_ns);   // a CTA without a unit
   if (!grid_barrier(a.bar + 2, a.status, a.wait_ns)) return;
 
-  // ---- M: output slices (head h, columns [cb, cb + 256)).  Thread (v, j)
-  // sums eight columns (one 16-byte load) over the units j, j + 16, ...: all
-  // its loads are issued before the sums; then the sixteen groups are added in
-  // order.
-  const int nhalf = (a.D_v + kMergeCols - 1) / kMergeCols;
+  // ---- M: output slices (head h, partial chunks [c0, c0 + 32)).  Thread
+  // (v, j) sums chunk c0 + v (eight columns, one 16-byte load) over the units
+  // j, j + 16, ...: all its loads are issued before the sums; then the sixteen
+  // groups are added in order.
+  const int nhalf = (Dvp + kMergeCols - 1) / kMergeCols;
   float* wgt = wm;                                     // [256] weight of each unit's values
   float* gsum = reinterpret_cast<float*>(keys);        // [16][256] group sums
   constexpr int kVec = kMergeCols / 8;                 // 32 threads cover a slice's columns
@@ -744,16 +758,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   constexpr int kBatch = 8;                            // loads in flight per thread
   for (int sl = cta; sl < kRowHeads * nhalf; sl += G) {
     const int h = sl / nhalf, cb = (sl % nhalf) * kMergeCols;
-    const int width = min(kMergeCols, a.D_v - cb);
+    const int width = min(kMergeCols, Dvp - cb);
     const int v = tid % kVec, grp = tid / kVec;
     const bool live = 8 * v < width;
-    const __half* base = a.po + (size_t)h * a.D_v + cb + 8 * v;
+    const int c = cb / 8 + v;                          // partial chunk
+    const __half* base = a.po + (size_t)h * Dvp + 8 * c;
     // The first batch of values is loaded with the units' (m, l, scale).
     uint4 x[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int uu = grp + kGroups * j;
-      x[j] = live && uu < units ? __ldcg(reinterpret_cast<const uint4*>(base + (size_t)uu * kRowHeads * a.D_v))
+      x[j] = live && uu < units ? __ldcg(reinterpret_cast<const uint4*>(base + (size_t)uu * kRowHeads * Dvp))
                                 : make_uint4(0u, 0u, 0u, 0u);
     }
     float m = -CUDART_INF_F, l = 0.f, scu = 1.f;
@@ -799,7 +814,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const int uu = nx + kGroups * j;
-        x[j] = live && uu < units ? __ldcg(reinterpret_cast<const uint4*>(base + (size_t)uu * kRowHeads * a.D_v))
+        x[j] = live && uu < units ? __ldcg(reinterpret_cast<const uint4*>(base + (size_t)uu * kRowHeads * Dvp))
                                   : make_uint4(0u, 0u, 0u, 0u);
       }
     }
@@ -814,9 +829,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
 #pragma unroll
         for (int i = 0; i < 8; ++i) t[i] += gsum[j * kMergeCols + 8 * v + i];
       const float il = Lsum > 0.f ? 1.f / Lsum : 0.f;
-      uint2* o2 = reinterpret_cast<uint2*>(a.out + (size_t)h * a.D_v + cb + 8 * v);   // out: 8-byte aligned
-      o2[0] = make_uint2(pack_bf16(t[0] * il, t[1] * il), pack_bf16(t[2] * il, t[3] * il));
-      o2[1] = make_uint2(pack_bf16(t[4] * il, t[5] * il), pack_bf16(t[6] * il, t[7] * il));
+      const int cw = c / (4 * NG), cg = (c / 4) % NG, cc = c % 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {   // columns of n-tile 4 cg + q
+        const int col = cw * 8 * NT + (4 * cg + q) * 8 + 2 * cc;
+        if (col < a.D_v)   // D_v is even: a pair is in or out whole
+          *reinterpret_cast<uint32_t*>(a.out + (size_t)h * a.D_v + col) = pack_bf16(t[2 * q] * il, t[2 * q + 1] * il);
+      }
     }
     if (tid == 0 && cb == 0 && a.lse)
       a.lse[h] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -CUDART_INF_F;
@@ -849,14 +868,21 @@ bool decode_row_supported(const dsa_problem& p) {
   return p.R == 1 && p.B == 1 && p.H_q == kRowHeads && p.D_k % 64 == 0 && p.D_k <= 576 && p.D_v <= 512 && p.k <= kCapFast;
 }
 
-// Partials of the attention units: fp16 O / l [units][64][D_v], fp32 (m, l)
-// [units][64][2], fp32 scale [units], each region 256-byte aligned.
+// Partials of the attention units: fp16 O / l [units][64][32 NT] (columns in
+// the kernel's chunk order), fp32 (m, l) [units][64][2], fp32 scale [units],
+// each region 256-byte aligned.
 static size_t row_units(const dsa_problem& p) { return (size_t)(p.k + kRowUnitRows - 1) / kRowUnitRows; }
+// Output n-tiles per warp: the smallest of 4, 8, 16 with 32 NT >= D_v.
+static int row_nt(int D_v) {
+  int NT = 4;
+  while (NT * 32 < D_v) NT *= 2;
+  return NT;
+}
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 size_t decode_row_partials_bytes(const dsa_problem& p) {
   const size_t u = row_units(p);
-  return align256(u * kRowHeads * p.D_v * 2) + align256(u * kRowHeads * 2 * 4) + align256(u * 4);
+  return align256(u * kRowHeads * 32 * row_nt(p.D_v) * 2) + align256(u * kRowHeads * 2 * 4) + align256(u * 4);
 }
 
 cudaError_t launch_decode_row(const dsa_problem& p, const Plan& pl, const int32_t* scores, int32_t* idx,
@@ -882,16 +908,15 @@ cudaError_t launch_decode_row(const dsa_problem& p, const Plan& pl, const int32_
   const size_t u = row_units(p);
   char* pp = ws + pl.off_rpart;
   a.po = reinterpret_cast<__half*>(pp);
-  a.pml = reinterpret_cast<float*>(pp + align256(u * kRowHeads * p.D_v * 2));
-  a.psc = reinterpret_cast<float*>(pp + align256(u * kRowHeads * p.D_v * 2) + align256(u * kRowHeads * 2 * 4));
+  a.pml = reinterpret_cast<float*>(pp + align256(u * kRowHeads * 32 * row_nt(p.D_v) * 2));
+  a.psc = reinterpret_cast<float*>(pp + align256(u * kRowHeads * 32 * row_nt(p.D_v) * 2) + align256(u * kRowHeads * 2 * 4));
   a.L1 = (int)p.L_total;
   a.k = p.k;
   a.D_k = p.D_k;
   a.D_v = p.D_v;
   a.scale_log2 = p.softmax_scale * 1.4426950408889634f;
   a.wait_ns = kDefaultWaitNs;
-  int NT = 2;
-  while (NT * 32 < p.D_v) NT *= 2;
+  const int NT = row_nt(p.D_v);
   a.qs = p.D_k;   // the swizzled query boxes need no padding
   a.ks = (p.D_k > NT * 32 ? p.D_k : NT * 32) + 8;
   EncodeTiledFn encode = encode_tiled_fn();
@@ -908,14 +933,12 @@ cudaError_t launch_decode_row(const dsa_problem& p, const Plan& pl, const int32_
   }
   if (a.f8) {
     switch (NT) {
-      case 2: return launch_row<2, kRowUnitRows, true>(a, st);
       case 4: return launch_row<4, kRowUnitRows, true>(a, st);
       case 8: return launch_row<8, kRowUnitRows, true>(a, st);
       default: return launch_row<16, kRowUnitRows, true>(a, st);
     }
   }
   switch (NT) {
-    case 2: return launch_row<2, kRowUnitRows, false>(a, st);
     case 4: return launch_row<4, kRowUnitRows, false>(a, st);
     case 8: return launch_row<8, kRowUnitRows, false>(a, st);
     default: return launch_row<16, kRowUnitRows, false>(a, st);
