@@ -39,9 +39,9 @@
 // output is the same on every run.
 //
 // State kept across steps (Plan::off_lkeep): the indexer's clearing counter,
-// reset here, and the bin cursors of S, returned to zero here for the next
-// step.  A cursor found not at zero (a fresh workspace) shows as a cursor
-// running past its bin; the cursors are then cleared and S done again.
+// reset here for the next step.  The bin cursors and survivor slots of S are
+// cleared with the rest of the workspace's zero range by the indexer at the
+// start of every step.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "select.cuh"
@@ -108,7 +108,7 @@ struct RowArgs {
   uint32_t* hist;          // [kRowHistCopies][kRowHistWords]: the row's histogram, as partial
                            // copies filled by the indexer's epilogue, then kCoarse sums over 128 bins
   uint32_t* zcount;        // the indexer's clearing counter, reset here for the next step
-  uint32_t* cnt;           // [kLogBins] bin cursors of S, left at zero for the next step
+  uint32_t* cnt;           // [kLogBins] bin cursors of S (cleared by the indexer)
   uint64_t* surv;          // [kCapFast] survivor keys in bin order
   __half* po;              // [units][64][32 NT] the unit's O / l of each head, times psc[u]
   float* pml;              // [units][64][2] the unit's max m and sum l of each head
@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   float* scs = reinterpret_cast<float*>(smem + L.scs);          // FP8 cache: [P] row scales
   int* wlist = pos_s + P;                                       // [kWindowList] member indices
   uint32_t* coarse_s = reinterpret_cast<uint32_t*>(wlist + kWindowList);   // [kCoarse]
+  uint32_t* cab = sub + kRowThreads;                            // [kCoarse] positions above each coarse bin
   __shared__ __align__(8) uint64_t bars[2];                     // queries, latent rows
   __shared__ uint32_t sh[8];                                    // b*, E(b*), |b*|, mode, C*, total, ...
   __shared__ uint32_t wt[kRowWarps];
@@ -272,6 +273,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
         if (lane >= o) incl += v;
       }
       const uint32_t above = incl - n_hi - n_lo;
+      cab[ch] = above;   // positions in the coarse bins above ch
+      cab[ch - 1] = above + n_hi;
       if (above < (uint32_t)n_take && above + n_hi >= (uint32_t)n_take) sh[4] = (uint32_t)ch;
       else if (above + n_hi < (uint32_t)n_take && incl >= (uint32_t)n_take) sh[4] = (uint32_t)(ch - 1);
       if (lane == 31) sh[5] = incl;   // all positions counted
@@ -313,32 +316,41 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
     }
     __syncthreads();
     {
-      const int top = kLogBins - 1 - tid * 16;   // this thread's bins top, ..., top - 15 (one coarse bin)
-      uint32_t cv[16];
-      uint32_t sum = 0;
+      // E(b) for every bin of the coarse bins C* and above: the positions in
+      // the coarse bins above b's plus those in the bins above b within it.
+      // One warp per coarse bin, four bins per lane (top down); each coarse
+      // bin's fine counts must add up to its coarse sum.
+      const int cstar = fb_lo >> 7;
+      for (int c = kCoarse - 1 - warp; c >= cstar; c -= kRowWarps) {
+        const int b0 = c * 128 + 127 - 4 * lane;   // this lane's bins b0, ..., b0 - 3
+        uint32_t v[4] = {0u, 0u, 0u, 0u};
+        const uint32_t cs = coarse_s[c];
+        if (cs != 0) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        cv[j] = top - j >= fb_lo ? HS(top - j) : 0u;
-        sum += cv[j];
-      }
-      uint32_t csum = sum;   // eight threads per coarse bin
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) csum += __shfl_xor_sync(0xffffffffu, csum, o);
-      if ((tid & 7) == 0 && top >= fb_lo && csum != coarse_s[top >> 7]) sh[7] = 1;
-      const uint32_t incl = block_scan_incl<kRowThreads>(sum, wt);
-      if (tid == kRowThreads - 1 && fb_lo > 0) HS(fb_lo - 1) = incl;   // E(fb_lo - 1): all bins read
-      uint32_t above = incl - sum;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (top - j >= fb_lo) HS(top - j) = above;
-        if (above < (uint32_t)n_take && above + cv[j] >= (uint32_t)n_take) {
-          sh[0] = (uint32_t)(top - j);
-          sh[1] = above;
-          sh[2] = cv[j];
-          sh[3] = above + cv[j] <= (uint32_t)kCapFast ? kRowFast : kRowExact;
+          for (int j = 0; j < 4; ++j) v[j] = HS(b0 - j);
         }
-        above += cv[j];
+        const uint32_t s4 = (v[0] + v[1]) + (v[2] + v[3]);
+        uint32_t incl = s4;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        if (lane == 31 && incl != cs) sh[7] = 1;
+        uint32_t above = cab[c] + incl - s4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          HS(b0 - j) = above;
+          if (above < (uint32_t)n_take && above + v[j] >= (uint32_t)n_take) {
+            sh[0] = (uint32_t)(b0 - j);
+            sh[1] = above;
+            sh[2] = v[j];
+            sh[3] = above + v[j] <= (uint32_t)kCapFast ? kRowFast : kRowExact;
+          }
+          above += v[j];
+        }
       }
+      if (tid == 0 && cstar > 0 && cstar < kCoarse) HS(fb_lo - 1) = cab[cstar] + coarse_s[cstar];   // all bins read
     }
     __syncthreads();
     if (sh[5] == (uint32_t)len && sh[7] == 0) {
