@@ -290,28 +290,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
     }
     __syncthreads();
     const int fb_lo = n_take > 0 ? (int)(sh[4] << 7) : kLogBins;   // lowest bin read
-    for (int b = kLogBins - 1 - tid; b >= fb_lo; b -= kRowThreads) HS(b) = 0;
-    __syncthreads();
-    {   // fine bins of those coarse bins, summed over the copies (loads batched)
-      const int items = (int)sh[6] * 128 * kRowHistCopies;
-      for (int i0 = tid; i0 < items; i0 += 8 * kRowThreads) {
-        uint32_t v[8];
-        int bb[8];
+    {   // fine bins of those coarse bins: each thread sums one bin over the copies
+      const int nb = (int)sh[6] * 128;
+      for (int i = tid; i < nb; i += kRowThreads) {
+        const int b = wlist[i >> 7] * 128 + (i & 127);
+        uint32_t v[kRowHistCopies];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int it2 = i0 + j * kRowThreads;
-          bb[j] = -1;
-          v[j] = 0;
-          if (it2 < items) {
-            const int cb = wlist[it2 / (128 * kRowHistCopies)];
-            const int cp = (it2 / 128) % kRowHistCopies;
-            bb[j] = cb * 128 + (it2 % 128);
-            v[j] = __ldcg(a.hist + (size_t)cp * kRowHistWords + bb[j]);
-          }
-        }
+        for (int cp = 0; cp < kRowHistCopies; ++cp) v[cp] = __ldcg(a.hist + (size_t)cp * kRowHistWords + b);
+        uint32_t sum = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (bb[j] >= 0 && v[j]) atomicAdd(&HS(bb[j]), v[j]);
+        for (int cp = 0; cp < kRowHistCopies; ++cp) sum += v[cp];
+        HS(b) = sum;
       }
     }
     __syncthreads();
