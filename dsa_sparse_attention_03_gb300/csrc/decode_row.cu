@@ -249,21 +249,22 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   // here from the scores (H) and read again.
   uint32_t bstar = 0, n_above = 0, mode = kRowEmpty;
   for (int attempt = 0;; ++attempt) {
-    if (tid < 8) sh[tid] = 0;
-    __syncthreads();
-    {   // the coarse sums of all copies, summed by one warp
-      const int c = tid % kCoarse, cp = tid / kCoarse;   // kCoarse * kRowHistCopies = 512 threads
-      sub[tid] = __ldcg(a.hist + (size_t)cp * kRowHistWords + kLogBins + c);
-    }
-    __syncthreads();
-    if (warp == 0) {
+    if (warp == 0) {   // the coarse sums of all copies, loaded and summed by one warp
+      if (lane < 8) sh[lane] = 0;
       const int ch = kCoarse - 1 - 2 * lane;   // this lane's coarse bins ch, ch - 1 (top down)
+      uint32_t vh[kRowHistCopies], vl[kRowHistCopies];
+#pragma unroll
+      for (int cp = 0; cp < kRowHistCopies; ++cp) {
+        vh[cp] = __ldcg(a.hist + (size_t)cp * kRowHistWords + kLogBins + ch);
+        vl[cp] = __ldcg(a.hist + (size_t)cp * kRowHistWords + kLogBins + ch - 1);
+      }
       uint32_t n_hi = 0, n_lo = 0;
 #pragma unroll
       for (int cp = 0; cp < kRowHistCopies; ++cp) {
-        n_hi += sub[cp * kCoarse + ch];
-        n_lo += sub[cp * kCoarse + ch - 1];
+        n_hi += vh[cp];
+        n_lo += vl[cp];
       }
+      __syncwarp();   // sh is cleared before any lane sets it
       coarse_s[ch] = n_hi;
       coarse_s[ch - 1] = n_lo;
       uint32_t incl = n_hi + n_lo;
