@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
   uint32_t* cab = sub + kRowThreads;                            // [kCoarse] positions above each coarse bin
   __shared__ __align__(8) uint64_t bars[2];                     // queries, latent rows
   __shared__ uint32_t sh[8];                                    // b*, E(b*), |b*|, mode, C*, total, ...
-  __shared__ uint32_t wt[kRowWarps];
+  __shared__ uint32_t wt[2 * kRowWarps];
   __shared__ float red[kRowWarps];
   __shared__ int key_lost;                                      // a survivor slot's wait ran out
 
@@ -476,8 +476,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
         umax = max(umax, u);
         uminv = max(uminv, ~u);
       }
-      umax = block_reduce_max<kRowThreads>(umax, wt);
-      uminv = block_reduce_max<kRowThreads>(uminv, wt);
+      block_reduce_max2<kRowThreads>(umax, uminv, wt);
       // Rank of a member = E(b_top) + (members with a larger score) + (members
       // with its score and a lower position).  The first count comes from a
       // histogram of the members' exact scores; the second only matters for
@@ -695,8 +694,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
     // stored O / l (a convex combination of these rows) stays below 2^15.
     float sc;
     {
-      uint32_t vb = 0;
-      for (int i = 0; i < kRowWarps; ++i) vb = max(vb, wt[i]);
+      const uint32_t vb = __reduce_max_sync(0xffffffffu, lane < kRowWarps ? wt[lane] : 0u);
       const int E = min(254, max(20, (int)(vb >> 23)));
       sc = __int_as_float((127 + 141 - E) << 23);
     }
@@ -785,8 +783,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (lane == 0) red[warp] = M;
     __syncthreads();
-    M = red[0];
-    for (int i = 1; i < kRowWarps; ++i) M = fmaxf(M, red[i]);
+    M = lane < kRowWarps ? red[lane] : -CUDART_INF_F;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float w = (tid < units && l > 0.f) ? exp2f(m - M) : 0.f;
     float Lw = w * l;
     __syncthreads();   // red is rewritten
@@ -795,8 +794,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
     if (lane == 0) red[warp] = Lw;
     if (tid < 256) wgt[tid] = w * l / scu;
     __syncthreads();
-    float Lsum = 0.f;
-    for (int i = 0; i < kRowWarps; ++i) Lsum += red[i];
+    float Lsum = lane < kRowWarps ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
     float o8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int u0 = grp;; u0 += kGroups * kBatch) {
 #pragma unroll

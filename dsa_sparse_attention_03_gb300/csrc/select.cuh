@@ -89,22 +89,37 @@ __device__ uint32_t block_scan_incl(uint32_t v, uint32_t* warp_tot) {
   }
   if (lane == 31) warp_tot[w] = v;
   __syncthreads();
-  uint32_t base = 0;
-  for (int i = 0; i < w; ++i) base += warp_tot[i];
+  uint32_t base = lane < w ? warp_tot[lane] : 0u;   // the totals of the warps before this one
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) base += __shfl_xor_sync(0xffffffffu, base, o);
   __syncthreads();
   return base + v;
 }
 
+// Block-wide maxima of two values at once (NT threads); tmp holds 2 NT / 32
+// words.
 template <int NT>
-__device__ uint32_t block_reduce_max(uint32_t v, uint32_t* tmp) {
+__device__ void block_reduce_max2(uint32_t& a, uint32_t& b, uint32_t* tmp) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((threadIdx.x & 31) == 0) tmp[threadIdx.x >> 5] = v;
+  for (int o = 16; o > 0; o >>= 1) {
+    a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  if (lane == 0) {
+    tmp[w] = a;
+    tmp[NW + w] = b;
+  }
   __syncthreads();
-  uint32_t r = 0;
-  for (int i = 0; i < NT / 32; ++i) r = max(r, tmp[i]);
+  a = lane < NW ? tmp[lane] : 0u;
+  b = lane < NW ? tmp[NW + lane] : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
   __syncthreads();
-  return r;
 }
 
 // Finds, in a histogram of `nbins` counts held in shared memory, the bin b
@@ -177,7 +192,7 @@ template <int NT, class InCand>
 __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, uint32_t k_rem, InCand in_cand,
                                             uint64_t* keys, uint32_t* status) {
   __shared__ uint32_t h[1 << kRadixBits];
-  __shared__ uint32_t tmp[NT / 32];
+  __shared__ uint32_t tmp[2 * NT / 32];
   __shared__ uint32_t res[2];
   __shared__ uint32_t n_list;
   __shared__ uint32_t tie8[8 * (NT / 32)];
@@ -195,8 +210,7 @@ __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, ui
       uminv = max(uminv, ~u);
     }
   });
-  umax = block_reduce_max<NT>(umax, tmp);
-  uminv = block_reduce_max<NT>(uminv, tmp);
+  block_reduce_max2<NT>(umax, uminv, tmp);
   const uint32_t diff = umax ^ ~uminv;
   uint32_t shift = diff ? 32u - __clz(diff) : 0u;
   uint32_t prefix = shift >= 32 ? 0u : (umax >> shift);

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
   extern __shared__ uint64_t keys[];   // [max(kCapFast, pow2 >= k)]: ranks / exact fallback
   __shared__ uint32_t h[kBuckets];
   __shared__ uint32_t res[2];
-  __shared__ uint32_t wt[kThreads / 32];
+  __shared__ uint32_t wt[2 * kThreads / 32];
   __shared__ uint32_t slot0;
   pdl_wait();
   pdl_trigger();
@@ -157,8 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
         umax = max(umax, x);
         uminv = max(uminv, ~x);
       });
-      umax = block_reduce_max<kThreads>(umax, wt);
-      uminv = block_reduce_max<kThreads>(uminv, wt);
+      block_reduce_max2<kThreads>(umax, uminv, wt);
       if (threadIdx.x == 0) {
         if (umax) atomicMax(&a.state[r].umax, umax);
         if (uminv) atomicMax(&a.state[r].uminv, uminv);
