@@ -823,20 +823,33 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
 #pragma unroll
     for (int i = 0; i < 8; ++i) gsum[grp * kMergeCols + 8 * v + i] = o8[i];
     __syncthreads();
-    if (grp == 0 && live) {
-      float t[8];
+    {   // the sixteen group sums of each column, in two steps over all threads:
+        // thread (pair p, quarter r) adds groups 4r .. 4r + 3 of columns 2p, 2p + 1
+      float2* part = reinterpret_cast<float2*>(gsum + kGroups * kMergeCols);   // [4][128]
+      const int pp = tid & (kMergeCols / 2 - 1), r = tid / (kMergeCols / 2);
+      float2 t = reinterpret_cast<const float2*>(gsum + 4 * r * kMergeCols)[pp];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) t[i] = gsum[8 * v + i];
-      for (int j = 1; j < kGroups; ++j)
+      for (int j = 1; j < 4; ++j) {
+        const float2 g = reinterpret_cast<const float2*>(gsum + (4 * r + j) * kMergeCols)[pp];
+        t.x += g.x;
+        t.y += g.y;
+      }
+      part[r * (kMergeCols / 2) + pp] = t;
+      __syncthreads();
+      if (tid < kMergeCols / 2 && 8 * (tid / 4) < width) {   // pair tid of the slice: chunk tid / 4
+        float2 u = part[tid];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] += gsum[j * kMergeCols + 8 * v + i];
-      const float il = Lsum > 0.f ? 1.f / Lsum : 0.f;
-      const int cw = c / (4 * NG), cg = (c / 4) % NG, cc = c % 4;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {   // columns of n-tile 4 cg + q
+        for (int q = 1; q < 4; ++q) {
+          const float2 g = part[q * (kMergeCols / 2) + tid];
+          u.x += g.x;
+          u.y += g.y;
+        }
+        const float il = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        const int cc2 = cb / 8 + tid / 4, q = tid % 4;   // partial chunk, and its n-tile
+        const int cw = cc2 / (4 * NG), cg = (cc2 / 4) % NG, cc = cc2 % 4;
         const int col = cw * 8 * NT + (4 * cg + q) * 8 + 2 * cc;
         if (col < a.D_v)   // D_v is even: a pair is in or out whole
-          *reinterpret_cast<uint32_t*>(a.out + (size_t)h * a.D_v + col) = pack_bf16(t[2 * q] * il, t[2 * q + 1] * il);
+          *reinterpret_cast<uint32_t*>(a.out + (size_t)h * a.D_v + col) = pack_bf16(u.x * il, u.y * il);
       }
     }
     if (tid == 0 && cb == 0 && a.lse)
