@@ -468,13 +468,24 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
         }
       } else {
       uint32_t umax = 0, uminv = 0;
-      for (int i = tid; i < M; i += kRowThreads) {
-        const uint64_t key = wait_key(a.surv + s0 + i, a.status, a.wait_ns);
-        if (key == 0) key_lost = 1;   // a wait ran out
-        keys[i] = key;
-        const uint32_t u = (uint32_t)(key >> 32);
-        umax = max(umax, u);
-        uminv = max(uminv, ~u);
+      for (int i0 = tid; i0 < M; i0 += 8 * kRowThreads) {   // eight slot loads in flight per thread
+        uint64_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + j * kRowThreads;
+          v[j] = i < M ? ld_relaxed_u64(a.surv + s0 + i) : 0ull;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + j * kRowThreads;
+          if (i >= M) break;
+          const uint64_t key = v[j] ? v[j] : wait_key(a.surv + s0 + i, a.status, a.wait_ns);
+          if (key == 0) key_lost = 1;   // a wait ran out
+          keys[i] = key;
+          const uint32_t u = (uint32_t)(key >> 32);
+          umax = max(umax, u);
+          uminv = max(uminv, ~u);
+        }
       }
       block_reduce_max2<kRowThreads>(umax, uminv, wt);
       // Rank of a member = E(b_top) + (members with a larger score) + (members
@@ -530,8 +541,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) decode_row_kernel(const __grid
             const uint64_t key = keys[wlist[j]];
             const uint32_t u = (uint32_t)(key >> 32);
             uint32_t before = 0;
-            for (int m = lane; m < M; m += 32) {
-              const uint64_t o = keys[m];
+            // Every member of a score group that meets the window is in
+            // wlist, so the group's larger keys are counted there.
+            for (int m = lane; m < nl; m += 32) {
+              const uint64_t o = keys[wlist[m]];
               before += ((uint32_t)(o >> 32) == u) & (o > key);
             }
             before = __reduce_add_sync(0xffffffffu, before);
