@@ -83,10 +83,10 @@ def test_k_4096_more_units_than_ctas():
 
 
 def test_one_workspace_for_consecutive_steps():
-    # The single-row step leaves its bin cursors cleared for the next step on the
-    # same workspace; the first step on a fresh (garbage) workspace finds them
-    # dirty and scatters again.  Steps of different lengths, and a separate top-k
-    # call in between, share one workspace.
+    # The indexer clears the single-row step's workspace range (histogram, bin
+    # cursors, survivor slots) at the start of every step, so one workspace,
+    # filled with garbage before the first step, serves steps of different
+    # lengths and a separate top-k call in between.
     import torch
     import dsa_sparse_attention_03_gb300 as dsa
     xs = [gen.l64k(layer=i, L=L) for i, L in enumerate((30000, 65536, 9000, 30000))]
