@@ -111,6 +111,9 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
   const int hgroups = p->H_q > 0 ? (p->H_q + kAttnHeads - 1) / kAttnHeads : 0;
   P.attn_kc_max = attn_clusters(p->R, hgroups, p->k);
   P.off_acnt = off; off = align_up(off + R * size_t(hgroups) * 16 * 4, 256);
+  const bool pairs = p->R >= kTopkSortRows && p->R <= kPairRows;
+  P.off_pairc = off;
+  if (pairs) off = align_up(off + R * kPairPhases * 4, 256);
   // Single-row decode step (one layout for every entry point): its histogram,
   // bin cursors and survivor slots start at zero.
   P.fused_row = decode_row_supported(*p) ? 1 : 0;
@@ -131,6 +134,11 @@ dsa_status make_plan(const dsa_problem* p, int need, Plan* pl) {
     off = align_up(off + R * size_t(hgroups) * P.attn_kc_max * (16 * dv + 32 * 16) * 4, 256);
   P.off_rpart = off;
   if (P.fused_row) off = align_up(off + decode_row_partials_bytes(*p), 256);
+  P.off_pairx = 0;
+  if (pairs) {
+    P.off_pairx = off;
+    off = align_up(off + R * pair_x_bytes(p->k), 256);
+  }
   P.total = off;
   return DSA_OK;
 }
@@ -261,7 +269,9 @@ dsa_status dsa_topk_static(const dsa_problem* p, const int32_t* scores, int32_t*
   cudaError_t e = cudaGetSymbolAddress(&base, g_topk_scratch);
   if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The status block, row state and histograms must start at zero.
+  // The status block, row state and histograms must start at zero; the exact
+  // fallback runs on single CTAs (its pair buffers lie past the scratch).
+  pl.off_pairx = 0;
   e = cudaMemsetAsync(base, 0, pl.zero_end, st);
   if (e != cudaSuccess) return cuda_fail(e, "clear static scratch");
   if (p->R == 0) return DSA_OK;

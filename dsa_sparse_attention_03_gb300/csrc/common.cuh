@@ -47,7 +47,22 @@ struct Plan {
   size_t off_lcur, off_lsurv;   // single-row step: bin cursors and survivor slots (cleared)
   size_t off_lkeep;         // single-row step: words the indexer must not clear (see decode_row.cu)
   size_t off_surv, off_scores, off_apart, off_rpart, total;
+  size_t off_pairc, off_pairx;  // top-k, exact fallback by CTA pairs: counters (cleared), buffers (0: none)
 };
+
+// Top-k: from kTopkSortRows rows on, each CTA sorts whole rows; up to
+// kPairRows rows, a row in the exact fallback is resolved by two CTAs when
+// the grid holds two per row.  Per row the pair has kPairPhases barrier
+// counters (cleared with the status block) and an exchange buffer:
+// [0, 256) scalars, then two radix histograms per part (alternate passes),
+// the per-block tie counts of both parts, and part 1's winners.
+constexpr int kTopkSortRows = 8;
+constexpr int kPairRows = 80;
+constexpr int kPairPhases = 8;
+constexpr size_t kPairHistOff = 256;
+constexpr size_t kPairTieOff = kPairHistOff + 4 * 2048 * 4;
+constexpr size_t kPairWinOff = kPairTieOff + 2 * 32 * 4 + 256;
+__host__ __device__ constexpr size_t pair_x_bytes(int k) { return kPairWinOff + size_t(k) * 8; }
 
 // Attention cluster size for k selected positions: one 64-position tile per
 // CTA, clusters of 4 (one CTA per SM) up to 32 tiles, else of 8, so that at

@@ -1,6 +1,6 @@
 // The decode step of one query row after its indexer scores: the exact ordered
 // top-k and the sparse attention over the selected latent rows, in one
-// cooperative kernel (one CTA per SM, two grid barriers).
+// cooperative kernel (one CTA per SM; one grid barrier, before the merge).
 //
 // "ds4 glm53-m3ultra" (page 1): parallel scans narrow the candidates, a small
 // surviving list is sorted, the original exact algorithm settles ambiguous
@@ -10,28 +10,34 @@
 //      (score_bin: 128 per octave of |score|, monotone, independent of the
 //      data) and adds them into one of eight copies of the row's histogram,
 //      with their sums over coarse bins of 128.
-//   P  every CTA sums the copies: the coarse sums give the coarse bin C*
-//      holding the k-th largest score; the bins of C* and above (only the
-//      coarse bins that hold positions) give E(b) = positions in bins above
-//      b, and the bin b* of the k-th largest.  The histogram is checked (its
-//      total is the row length, each coarse sum the sum of its bins); if the
-//      indexer could not complete it, the CTAs rebuild it from the scores (H).
+//   P  every CTA sums the copies: warp 0 adds the coarse sums, which give
+//      the coarse bin C* holding the k-th largest score; the fine bins of C*
+//      and above (only the coarse bins that hold positions) are summed one
+//      per thread and scanned one coarse bin per warp: E(b) = positions in
+//      bins above b, and the bin b* of the k-th largest.  The histogram is
+//      checked (its total is the row length, each coarse sum the sum of its
+//      bins); if the indexer could not complete it, the CTAs rebuild it from
+//      the scores (H).
 //   S  if the bins >= b* hold at most 4096 positions, each CTA scatters its
 //      positions in bins >= b* into bin order: position t of bin b goes to
-//      slot E(b) + (arrival order within the bin).                 barrier
+//      slot E(b) + (arrival order within the bin).  No barrier follows: a
+//      unit waits (bounded) for the slots of its own bins, and a survivor's
+//      key is never 0.
 //   R  attention unit u takes ranks [uP, uP + P) of the selection.  Its CTA
 //      loads the slots of the bins holding those ranks and ranks the members
-//      by their 64-bit keys (score desc, position asc): a histogram of their
-//      exact scores gives the members above each score, and equal scores are
-//      ordered by position.  It writes idx[rank] for its ranks, and
+//      by their 64-bit keys (score desc, position asc): up to 64 members by
+//      one warp's comparisons; more by a histogram of their exact scores
+//      (the members above each score), equal scores ordered by position
+//      within their group.  It writes idx[rank] for its ranks, and
 //   A  gathers its P latent rows once (one bulk copy per row) for all 64
 //      heads -- the queries arrived by tensor-map copies at the start -- :
 //      S = Q K^T and O = P V on bf16 mma.sync with an fp32 softmax.  The
 //      unit's O / l goes to the workspace as fp16 scaled by a power of two
-//      (from its rows' largest value), with the max m and sum l per head.
-//                                                                   barrier
-//   M  CTA c merges output slices (a head, 256 columns) over the units in
-//      unit order: weights exp2(m_u - M) l_u, divided by their sum, bf16.
+//      (from its rows' largest value), in the accumulators' chunk order, with
+//      the max m and sum l per head.                               barrier
+//   M  CTA c merges output slices (a head, 256 columns) over the units:
+//      weights exp2(m_u - M) l_u, divided by their sum, bf16; every sum in a
+//      fixed order.
 // When the bins >= b* hold more than 4096 positions (heavy ties at the
 // threshold), CTA 0 selects the row exactly (radix passes to the k-th key,
 // ties by position) into idx, and after one more barrier the units read their

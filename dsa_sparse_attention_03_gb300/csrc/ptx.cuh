@@ -52,6 +52,19 @@ static __device__ __noinline__ bool grid_barrier(uint32_t* c, uint32_t* status, 
   return ok != 0;
 }
 
+// The same protocol among `n` CTAs that share the counter c (all of them
+// co-resident): every thread of each CTA takes part.
+static __device__ __noinline__ bool group_barrier(uint32_t* c, uint32_t n, uint32_t* status, uint64_t limit_ns) {
+  __shared__ int ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    GridOps ops{c, status};
+    ok = barrier_arrive_and_wait(ops, n, limit_ns) ? 1 : 0;
+  }
+  __syncthreads();
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -6,6 +6,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace sel {
@@ -187,10 +188,27 @@ __device__ void sort_desc(uint64_t* keys, int n0) {
 // comes from the caller's histogram; a key beyond k (a histogram that does not
 // match the scores) is not written and raises DSA_DEVICE_CAPACITY in *status.
 // All NT threads of the CTA take part; ends with a barrier.
+//
+// With a pair (px != nullptr), two co-resident CTAs resolve the row together:
+// part 0 takes the tie blocks [0, ceil(nblk / 2)), part 1 the rest, for every
+// pass over the row, and they exchange their partial results through a global
+// buffer at each step (key range, radix histograms, tie counts per block, the
+// last tie taken, part 1's winners), each exchange behind a two-CTA barrier.
+// Part 0 ends with the sorted keys; part 1's keys are not meaningful.  A
+// barrier that runs out raises DSA_DEVICE_TIMEOUT and both parts return early
+// (the result is then unspecified).
 constexpr int kTieBlocks = 32;
+struct PairX {
+  int part;                // 0 or 1
+  unsigned char* xb;       // kPairXBytes of global memory for this row
+  uint32_t* xc;            // kPairPhases barrier counters for this row, zero at the start
+  uint64_t wait_ns;
+};
+static_assert((1 << kRadixBits) == 2048 && kTieBlocks == 32, "the pair exchange layout (common.cuh)");
+
 template <int NT, class InCand>
 __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, uint32_t k_rem, InCand in_cand,
-                                            uint64_t* keys, uint32_t* status) {
+                                            uint64_t* keys, uint32_t* status, const PairX* px = nullptr) {
   __shared__ uint32_t h[1 << kRadixBits];
   __shared__ uint32_t tmp[2 * NT / 32];
   __shared__ uint32_t res[2];
@@ -200,10 +218,20 @@ __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, ui
   __shared__ uint32_t cut[2];
   __shared__ int pstar;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  // Tie blocks of 2^lb positions (at most kTieBlocks); a pair splits the row
+  // at a block boundary.
+  int lb = 12;
+  while ((int64_t(1) << lb) * kTieBlocks < (int64_t)len) ++lb;
+  const int nblk = (int)((len + (int64_t(1) << lb) - 1) >> lb);
+  const int mid = (int)min((int64_t)len, (int64_t)((nblk + 1) / 2) << lb);
+  const int r0 = px ? (px->part ? mid : 0) : 0, r1 = px ? (px->part ? len : mid) : len;
+  int phase = 0;
+  auto exchange = [&]() { return group_barrier(px->xc + phase++, 2u, status, px->wait_ns); };
+  uint32_t* xw = px ? reinterpret_cast<uint32_t*>(px->xb) : nullptr;
 
   // Key range of the candidates.
   uint32_t umax = 0, uminv = 0;
-  scan_row_v<NT>(s, 0, len, [&](int32_t v, int) {
+  scan_row_v<NT>(s, r0, r1, [&](int32_t v, int) {
     const uint32_t u = ordered_key(v);
     if (in_cand(u)) {
       umax = max(umax, u);
@@ -211,6 +239,15 @@ __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, ui
     }
   });
   block_reduce_max2<NT>(umax, uminv, tmp);
+  if (px) {
+    if (threadIdx.x == 0) {
+      __stcg(xw + 2 * px->part, umax);
+      __stcg(xw + 2 * px->part + 1, uminv);
+    }
+    if (!exchange()) return;
+    umax = max(__ldcg(xw), __ldcg(xw + 2));
+    uminv = max(__ldcg(xw + 1), __ldcg(xw + 3));
+  }
   const uint32_t diff = umax ^ ~uminv;
   uint32_t shift = diff ? 32u - __clz(diff) : 0u;
   uint32_t prefix = shift >= 32 ? 0u : (umax >> shift);
@@ -222,12 +259,19 @@ __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, ui
     const int nb = 1 << bits;
     for (int i = threadIdx.x; i < nb; i += NT) h[i] = 0;
     __syncthreads();
-    scan_row_v<NT>(s, 0, len, [&](int32_t v, int) {
+    scan_row_v<NT>(s, r0, r1, [&](int32_t v, int) {
       const uint32_t u = ordered_key(v);
       if (in_cand(u) && (static_cast<uint64_t>(u) >> shift) == prefix)
         atomicAdd(&h[(u >> ns) & (uint32_t)(nb - 1)], 1u);
     });
     __syncthreads();
+    if (px) {   // buffer (pass mod 2): the other part has read the older one
+      uint32_t* hx = reinterpret_cast<uint32_t*>(px->xb + kPairHistOff) + (size_t)((phase & 1) * 2) * (1 << kRadixBits);
+      for (int i = threadIdx.x; i < nb; i += NT) __stcg(hx + (size_t)px->part * (1 << kRadixBits) + i, h[i]);
+      if (!exchange()) return;
+      for (int i = threadIdx.x; i < nb; i += NT) h[i] = __ldcg(hx + i) + __ldcg(hx + (1 << kRadixBits) + i);
+      __syncthreads();
+    }
     find_crossing<NT>(h, nb, k_rem, res);
     k_rem -= res[1];
     prefix = (prefix << bits) | res[0];
@@ -236,12 +280,9 @@ __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, ui
   }
   const uint32_t T = prefix;
 
-  // Ties at T per block of 2^lb positions (at most kTieBlocks blocks); each
-  // thread visits its positions in increasing order and adds its count when
-  // it moves to another block (into its warp's own counters).
-  int lb = 12;
-  while ((int64_t(1) << lb) * kTieBlocks < (int64_t)len) ++lb;
-  const int nblk = (int)((len + (int64_t(1) << lb) - 1) >> lb);
+  // Ties at T per block of 2^lb positions; each thread visits its positions
+  // in increasing order and adds its count when it moves to another block
+  // (into its warp's own counters).
   for (int i = threadIdx.x; i < (NT / 32) * kTieBlocks; i += NT) (&wcnt[0][0])[i] = 0;
   if (threadIdx.x == 0) {
     n_list = 0;
@@ -251,7 +292,7 @@ __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, ui
   if (k_rem > 0) {
     int cb = -1;
     uint32_t cnt = 0;
-    scan_row_v<NT>(s, 0, len, [&](int32_t v, int t) {
+    scan_row_v<NT>(s, r0, r1, [&](int32_t v, int t) {
       if (ordered_key(v) == T) {
         const int b = t >> lb;
         if (b != cb) {
@@ -265,6 +306,20 @@ __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, ui
     if (cnt) atomicAdd(&wcnt[w][cb], cnt);
   }
   __syncthreads();
+  if (px) {   // per-block totals of both parts (each block is counted by one part)
+    uint32_t* tx = reinterpret_cast<uint32_t*>(px->xb + kPairTieOff);
+    if (threadIdx.x < kTieBlocks) {
+      uint32_t tb = 0;
+      for (int ww = 0; ww < NT / 32; ++ww) tb += wcnt[ww][threadIdx.x];
+      __stcg(tx + px->part * kTieBlocks + threadIdx.x, tb);
+    }
+    if (!exchange()) return;
+    if (threadIdx.x < kTieBlocks) {
+      wcnt[0][threadIdx.x] = __ldcg(tx + threadIdx.x) + __ldcg(tx + kTieBlocks + threadIdx.x);
+      for (int ww = 1; ww < NT / 32; ++ww) wcnt[ww][threadIdx.x] = 0;
+    }
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {   // the block holding the k_rem-th tie, and the ties before it
     uint32_t run = 0;
     int cbk = nblk;
@@ -282,7 +337,7 @@ __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, ui
   }
   __syncthreads();
   const int cbk = (int)cut[0];
-  if (cbk < nblk) {
+  if (cbk < nblk && (!px || ((cbk << lb) >= mid) == (px->part == 1))) {   // (a pair: the block's owner)
     // Number the ties of that block in position order: position t = base0 +
     // j * NT + thread, so (j, warp, lane) order; the need-th one is the last
     // tie taken.
@@ -317,12 +372,19 @@ __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, ui
     }
   }
   __syncthreads();
+  if (px && cbk < nblk) {   // the block's owner passes on the last tie taken
+    const bool owner = ((cbk << lb) >= mid) == (px->part == 1);
+    if (owner && threadIdx.x == 0) __stcg(reinterpret_cast<int*>(xw) + 4, pstar);
+    if (!exchange()) return;
+    if (threadIdx.x == 0) pstar = __ldcg(reinterpret_cast<const int*>(xw) + 4);
+    __syncthreads();
+  }
   const int ps = pstar;
 
   // Winners: every key above T, and the ties at or before position ps; slots
   // are reserved once per group of lanes that found one.
   const uint32_t lt = lanemask_lt();
-  scan_row_v<NT>(s, 0, len, [&](int32_t v, int t) {
+  scan_row_v<NT>(s, r0, r1, [&](int32_t v, int t) {
     const uint32_t u = ordered_key(v);
     if (u > T || (u == T && t <= ps)) {
       const uint32_t m = __activemask();
@@ -336,6 +398,22 @@ __device__ __noinline__ void exact_row_keys(const int32_t* s, int len, int k, ui
     }
   });
   __syncthreads();
+  if (px) {   // part 1's winners join part 0's
+    uint64_t* wx = reinterpret_cast<uint64_t*>(px->xb + kPairWinOff);
+    const uint32_t mine = min(n_list, (uint32_t)k);
+    if (px->part == 1) {
+      for (uint32_t i = threadIdx.x; i < mine; i += NT) __stcg(wx + i, keys[i]);
+      if (threadIdx.x == 0) __stcg(xw + 5, mine);
+    }
+    if (!exchange()) return;
+    if (px->part == 1) return;
+    const uint32_t other = __ldcg(xw + 5);
+    for (uint32_t i = threadIdx.x; i < other; i += NT) {
+      if (mine + i < (uint32_t)k) keys[mine + i] = __ldcg(wx + i);
+      else raise_status(status, DSA_DEVICE_CAPACITY);
+    }
+    __syncthreads();
+  }
   sort_desc<NT>(keys, k);
 }
 

@@ -46,7 +46,7 @@ constexpr int kRankSlice = 16;                             // survivors ranked p
 constexpr int kRankLanes = kThreads / kRankSlice;          // threads per survivor
 constexpr int kRankSlices = kCapFast / kRankSlice;         // units per row (also covers idx[0, k))
 static_assert(kRankSlices * kRankSlice >= kMaxK, "rank units must cover idx");
-constexpr int kSortRows = 8;                               // rank by per-row sort from this many rows
+constexpr int kSortRows = kTopkSortRows;                   // rank by per-row sort from this many rows
 
 enum Mode : uint32_t { kFast = 0, kAll = 1, kEmpty = 2, kExact = 3 };
 
@@ -64,6 +64,8 @@ struct TopkArgs {
   int R, k, chunk, nchunk, hist_rep, range;
   uint64_t wait_ns;    // grid barrier limit
   int skip_cta;        // test hook: this CTA returns before its first grid barrier (-1: none)
+  unsigned char* pair_x;   // [R][pair_x_bytes(k)] exchange buffers of the two-CTA exact fallback, or null
+  uint32_t* pair_c;        // [R][kPairPhases] its barrier counters (zeroed with the status block)
 };
 
 // Equal-width bins over the row's key range: bin(u) = (u - umin) >> shift,
@@ -87,15 +89,24 @@ struct Bins {
 
 // ------------------------------------------------------------------ exact fallback
 
-// One CTA resolves a row exactly: the candidates are the positions in bucket
-// b*; k - n_above of them are taken.
-__device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys) {
+// One CTA (or, with part >= 0, part `part` of a pair of CTAs) resolves a row
+// exactly: the candidates are the positions in bucket b*; k - n_above of them
+// are taken.  Part 0 (or the single CTA) writes idx.
+__device__ void exact_row(const TopkArgs& a, RowState* st, int r, uint64_t* keys, int part = -1) {
   const int len = a.row_len[r];
   const int32_t* s = a.scores + (int64_t)r * a.L_max;
   const uint32_t bstar = st->bstar;
   const Bins bin(st);
+  PairX px;
+  if (part >= 0) {
+    px.part = part;
+    px.xb = a.pair_x + (size_t)r * pair_x_bytes(a.k);
+    px.xc = a.pair_c + (size_t)r * kPairPhases;
+    px.wait_ns = a.wait_ns;
+  }
   exact_row_keys<kThreads>(s, len, a.k, (uint32_t)a.k - st->n_above,
-                           [&](uint32_t u) { return bin(u) == bstar; }, keys, a.status);
+                           [&](uint32_t u) { return bin(u) == bstar; }, keys, a.status, part >= 0 ? &px : nullptr);
+  if (part > 0) return;
   int32_t* idx = a.idx + (size_t)r * a.k;
   for (int j = threadIdx.x; j < a.k; j += kThreads) idx[j] = key_pos(keys[j]);
 }
@@ -246,6 +257,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
 
   // ---- rank by sort: whole rows per CTA (many rows).
   if (a.R >= kSortRows) {
+    // With two CTAs per row, CTA R + r is the second part of row r's exact
+    // fallback (and idle otherwise).
+    const bool pairs = a.pair_x != nullptr && 2 * a.R <= (int)gridDim.x;
+    if (pairs && (int)blockIdx.x >= a.R) {
+      const int r = (int)blockIdx.x - a.R;
+      if (r < a.R && a.state[r].mode == kExact) exact_row(a, a.state + r, r, keys, 1);
+      return;
+    }
     for (int r = blockIdx.x; r < a.R; r += gridDim.x) {
       RowState* st = a.state + r;
       const uint32_t mode = st->mode;
@@ -253,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a) {
       int32_t* idx = a.idx + (size_t)r * a.k;
       if (threadIdx.x == 0 && a.nsel) a.nsel[r] = n_take;
       if (mode == kExact) {
-        exact_row(a, st, r, keys);
+        exact_row(a, st, r, keys, pairs ? 0 : -1);
         __syncthreads();
         continue;
       }
@@ -335,6 +354,8 @@ cudaError_t launch_topk(const dsa_problem& p, const Plan& pl, const int32_t* sco
   a.surv = reinterpret_cast<uint64_t*>(ws + pl.off_surv);
   a.status = reinterpret_cast<uint32_t*>(ws + pl.off_status);
   a.bar = a.status + kBarrierWord;
+  a.pair_x = pl.off_pairx ? reinterpret_cast<unsigned char*>(ws + pl.off_pairx) : nullptr;
+  a.pair_c = reinterpret_cast<uint32_t*>(ws + pl.off_pairc);
   a.L_max = pl.L_max;
   a.R = pl.R;
   a.k = pl.k;

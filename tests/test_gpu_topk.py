@@ -3,7 +3,8 @@ long random rows, the largest scores on a regular stride, a crowded threshold
 bin and heavy ties (the exact fallback), scores spanning the whole int32 range
 (rows of only INT32_MIN or only INT32_MAX included), and rows of every kind in
 one call, with one row (survivors ranked across the grid) and with many rows
-(each row's survivors sorted by one CTA).  Scores are given directly, so each
+(each row's survivors sorted by one CTA; a row in the exact fallback resolved
+by a pair of CTAs).  Scores are given directly, so each
 path is reached on purpose."""
 import numpy as np
 import pytest
@@ -107,6 +108,24 @@ def test_small_k_and_lengths_around_8192():
     rng = np.random.default_rng(7)
     rows = [rng.integers(-100, 100, n).astype(np.int32) for n in (8191, 8192, 8193, 20000)]
     _check(rows, k=300)
+
+
+def test_many_tied_rows_resolved_by_cta_pairs():
+    # Ten or more rows, each in the exact fallback (the threshold bin holds more
+    # than the survivor cap), so each is resolved by a pair of CTAs that split
+    # the row at a tie block: lengths that split unevenly, rows whose winners
+    # all lie in the second half, rows whose last tie taken lies in the first,
+    # and a row with keys above the ties in both halves.
+    rng = np.random.default_rng(12)
+    rows = [rng.integers(0, 2, n).astype(np.int32) for n in (9000, 20001, 65537, 131071, 8193, 77777)]
+    late = np.zeros(90000, np.int32)
+    late[-10000:] = rng.integers(1, 3, 10000)          # ties at 2 only in the last 10000 positions
+    early = np.zeros(90000, np.int32)
+    early[:10000] = rng.integers(1, 3, 10000)          # ... only in the first 10000
+    both = rng.integers(0, 2, 100000).astype(np.int32)
+    both[[3, 60000, 99999]] = 7                        # a few keys above the ties, one in each half
+    rows += [late, early, both, np.full(12345, 5, np.int32)]
+    _check(rows)
 
 
 def _int32_extreme_rows(rng):
