@@ -274,16 +274,28 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (no wait).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+// Eight 8-column groups of 16 TMEM lanes in the 16x256b shape (no wait):
+// thread t gets, for group g, columns 8g + 2(t % 4) and + 1 of lane t / 4
+// (v[4g], v[4g + 1]) and of lane t / 4 + 8 (v[4g + 2], v[4g + 3]).
+__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
       "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
         "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
         "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
         "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+// The same for four 8-column groups (16 registers).
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
 }
 
@@ -637,7 +649,6 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
     const int ew = warp - kEpiWarp0;         // 0..7
     const int grp = ew >> 2;                 // tiles i with i % 2 == grp
     const int quarter = warp & 3;            // TMEM lanes this warp may read
-    const int m = quarter * 32 + lane;       // key row of the tile = TMEM lane
     const int wstride = a.RG * a.H_i + kMaxRG;
     int2* wc = wc_s + ew * wstride;          // (w_h, bits of M - bias_h) per (row, head)
     int* wsum = reinterpret_cast<int*>(wc + a.RG * a.H_i);
@@ -686,42 +697,62 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(TcArgs a) {
       const int accb = i % NACC;
       if (!wait_bar_warp(bar_accfull + 8 * accb, (i / NACC) & 1, abort_flag, a.status, a.wait_ns)) break;
       tc_fence_after();
-      const int t = ti.j * kTile + m;
+      // The accumulator in the 16x256b shape: the quad of threads t = 4 kq +
+      // cq holds keys kq, kq + 8 (lanes 0..15 of this warp's 32) and kq + 16,
+      // kq + 24 (lanes 16..31), heads 8g + 2 cq and + 1 of each 8-head group g:
+      // one (w, c) load serves four keys, and the quad adds its four partial
+      // sums of each key by shuffles.  Thread cq then owns key cq of its four.
+      const int kq = lane >> 2, cq = lane & 3;
+      const int mk = quarter * 32 + (cq & 1) * 8 + (cq >> 1) * 16 + kq;   // this thread's key row
+      const int t = ti.j * kTile + mk;
       const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + accb * N_max;
 #pragma unroll
       for (int jr = 0; jr < kMaxRG; ++jr) {
         if (jr >= ti.nrows) break;
-        // Four independent sums (wrapping mod 2^32; the true score fits int32).
-        uint32_t acc4[4] = {0u, 0u, 0u, 0u};
+        // One sum per key (wrapping mod 2^32; the true score fits int32).
+        uint32_t s0 = 0u, s1 = 0u, s2 = 0u, s3 = 0u;
         const int4* wr = reinterpret_cast<const int4*>(wc + jr * a.H_i);
-        for (int h0 = 0; h0 < a.H_i; h0 += 64) {
-          uint32_t va[32], vb[32];
-          const bool two = h0 + 32 < a.H_i;
-          tmem_ld32(trow + jr * a.H_i + h0, va);
-          if (two) tmem_ld32(trow + jr * a.H_i + h0 + 32, vb);
+        // x = max(d - bias + M, floor) = M + ReLU(q.k): an exact integer in
+        // [2^23, 2^24), so its bit pattern is 0x4B400000 + score part.
+        auto group = [&](const uint32_t* va, const uint32_t* vb, int g, int hp) {
+          const int4 p = wr[hp];   // (w, c) of the two heads
+          const float ca = __int_as_float(p.y), cb = __int_as_float(p.w);
+          const uint32_t wa = (uint32_t)p.x, wb = (uint32_t)p.z;
+          s0 += (uint32_t)__float_as_int(fmaxf(__uint_as_float(va[4 * g]) + ca, floor_v)) * wa +
+                (uint32_t)__float_as_int(fmaxf(__uint_as_float(va[4 * g + 1]) + cb, floor_v)) * wb;
+          s1 += (uint32_t)__float_as_int(fmaxf(__uint_as_float(va[4 * g + 2]) + ca, floor_v)) * wa +
+                (uint32_t)__float_as_int(fmaxf(__uint_as_float(va[4 * g + 3]) + cb, floor_v)) * wb;
+          s2 += (uint32_t)__float_as_int(fmaxf(__uint_as_float(vb[4 * g]) + ca, floor_v)) * wa +
+                (uint32_t)__float_as_int(fmaxf(__uint_as_float(vb[4 * g + 1]) + cb, floor_v)) * wb;
+          s3 += (uint32_t)__float_as_int(fmaxf(__uint_as_float(vb[4 * g + 2]) + ca, floor_v)) * wa +
+                (uint32_t)__float_as_int(fmaxf(__uint_as_float(vb[4 * g + 3]) + cb, floor_v)) * wb;
+        };
+        if (a.H_i == 32) {   // four 8-head groups: the row's 32 columns only
+          uint32_t va[16], vb[16];   // lanes 0..15 and 16..31 of this warp's quarter
+          tmem_ld16x256_x4(trow + jr * a.H_i, va);
+          tmem_ld16x256_x4(trow + (16u << 16) + jr * a.H_i, vb);
           tmem_wait_ld();
 #pragma unroll
-          for (int h2 = 0; h2 < 16; ++h2) {
-            const int4 p = wr[(h0 >> 1) + h2];     // (w, c) of heads h0+2*h2 and h0+2*h2+1
-            // x = max(d - bias + M, floor) = M + ReLU(q.k): an exact integer in
-            // [2^23, 2^24), so its bit pattern is 0x4B400000 + score part.
-            const float x0 = fmaxf(__uint_as_float(va[2 * h2]) + __int_as_float(p.y), floor_v);
-            const float x1 = fmaxf(__uint_as_float(va[2 * h2 + 1]) + __int_as_float(p.w), floor_v);
-            acc4[(h2 & 1) * 2] += (uint32_t)__float_as_int(x0) * (uint32_t)p.x;
-            acc4[(h2 & 1) * 2 + 1] += (uint32_t)__float_as_int(x1) * (uint32_t)p.z;
-          }
-          if (two) {
+          for (int g = 0; g < 4; ++g) group(va, vb, g, 4 * g + cq);   // heads 8g + 2cq and + 1
+        } else {
+          for (int h0 = 0; h0 < a.H_i; h0 += 64) {
+            uint32_t va[32], vb[32];
+            tmem_ld16x256_x8(trow + jr * a.H_i + h0, va);
+            tmem_ld16x256_x8(trow + (16u << 16) + jr * a.H_i + h0, vb);
+            tmem_wait_ld();
 #pragma unroll
-            for (int h2 = 0; h2 < 16; ++h2) {
-              const int4 p = wr[(h0 >> 1) + 16 + h2];
-              const float x0 = fmaxf(__uint_as_float(vb[2 * h2]) + __int_as_float(p.y), floor_v);
-              const float x1 = fmaxf(__uint_as_float(vb[2 * h2 + 1]) + __int_as_float(p.w), floor_v);
-              acc4[(h2 & 1) * 2] += (uint32_t)__float_as_int(x0) * (uint32_t)p.x;
-              acc4[(h2 & 1) * 2 + 1] += (uint32_t)__float_as_int(x1) * (uint32_t)p.z;
-            }
+            for (int g = 0; g < 8; ++g) group(va, vb, g, (h0 >> 1) + 4 * g + cq);
           }
         }
-        uint32_t acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+        // Sum over the quad; thread cq keeps key cq (kq, kq + 8, kq + 16, kq + 24).
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+          s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+          s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+          s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+          s3 += __shfl_xor_sync(0xffffffffu, s3, o);
+        }
+        uint32_t acc = cq == 0 ? s0 : (cq == 1 ? s1 : (cq == 2 ? s2 : s3));
         acc -= 0x4B400000u * (uint32_t)wsum[jr];
         const int rl = jr == 0 ? rlen0 : (jr == 1 ? rlen1 : (jr == 2 ? rlen2 : rlen3));
         if (t < rl) {
